@@ -1,0 +1,235 @@
+/*
+ * lmh.h -- C ABI of liblmh, the LM-head logprob library for one NVIDIA GB300
+ * GPU (sm_103a).
+ *
+ * The library computes the output-head hot path of LLM serving:
+ *
+ *   1. lmh_select_rows          pick the rows of a packed batch that are
+ *                               sampled and emit compacted prefix sums;
+ *   2. lmh_project_logprobs     gather those rows, project them through the
+ *                               [hidden x vocab] head on the tensor cores and
+ *                               reduce every row over the full vocabulary to
+ *                               an O(k+1) result without writing the
+ *                               [rows x vocab] logits to memory;
+ *   3. lmh_logprobs_from_logits the same reduction for logits that already
+ *                               exist (prompt scoring of logits chunks).
+ *
+ * The O(k+1) result of a row is: lse (fp32 log-sum-exp over the vocabulary),
+ * the selected token's logprob, and the exact top-k (ids and logprobs),
+ * sorted by logit descending with exact ties ordered by ascending token id.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named "device" are device memory owned by the caller (for
+ *   example PyTorch tensors).  The library allocates no memory per call and
+ *   keeps no per-call state; scratch memory is the caller's `workspace`.
+ * - Every call is enqueued on `stream` and returns without waiting for the
+ *   GPU: no host synchronisation and no device->host copy happens inside.
+ * - Host-side argument checks return an error status and launch nothing.
+ *   Errors only visible on the device (bad cu_seqlens, an id out of range)
+ *   set bits (LMH_DS_*) in the caller's optional `dev_status` word with an
+ *   atomic OR; kernels never trap.  The caller zeroes that word.
+ * - Matrices are row-major; `*_stride` arguments are in elements.
+ * - The first call on a device performs a one-time set-up (kernel attributes,
+ *   driver entry points) under a once-flag.
+ */
+#ifndef LMH_H
+#define LMH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LMH_VERSION 1
+
+/* Largest k (top-k entries per row) any entry point accepts. */
+#define LMH_K_MAX 128
+
+typedef enum lmh_status {
+    LMH_OK = 0,
+    LMH_ERR_INVALID_ARG = 1,         /* null required pointer, bad size, k > vocab, ... */
+    LMH_ERR_UNSUPPORTED = 2,         /* valid request this version does not implement    */
+    LMH_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < lmh_workspace_bytes(...)       */
+    LMH_ERR_CUDA = 4,                /* a CUDA runtime/driver call failed                 */
+    LMH_ERR_TIMEOUT = 5              /* reserved: device waits report LMH_DS_TIMEOUT      */
+} lmh_status;
+
+typedef enum lmh_dtype { LMH_BF16 = 0, LMH_F16 = 1, LMH_F32 = 2 } lmh_dtype;
+
+/* Storage of the head weight W, whose math shape is [H x V]. */
+typedef enum lmh_w_layout {
+    LMH_W_VH = 0, /* stored [V x H] row-major: PyTorch lm_head.weight (H contiguous) */
+    LMH_W_HV = 1  /* stored [H x V] row-major (not implemented: LMH_ERR_UNSUPPORTED)  */
+} lmh_w_layout;
+
+/* Which entry point a workspace is sized for. */
+typedef enum lmh_path { LMH_PATH_PROJECT = 0, LMH_PATH_FROM_LOGITS = 1 } lmh_path;
+
+/* Device status bits (OR-ed into *dev_status). */
+#define LMH_DS_BAD_CU_SEQLENS 0x1u       /* cu[0] != 0, cu decreasing, or an empty prefill segment */
+#define LMH_DS_SEL_OUT_OF_RANGE 0x2u     /* a selected id outside [0, V) other than -1 (row gets NaN) */
+#define LMH_DS_ROWS_OVERFLOW 0x4u        /* more selected rows than max_out_rows (extra rows dropped) */
+#define LMH_DS_ROW_IDX_OUT_OF_RANGE 0x8u /* a row index outside [0, num_tokens) (row reads zeros)   */
+#define LMH_DS_TIMEOUT 0x10u             /* a bounded device-side wait gave up (kernel returned)     */
+
+/*
+ * lmh_select_rows -- which rows of a packed batch are sampled.
+ *
+ * Defined by the vllm-metal release v0.4.0.dev20260831, "Summary": decode
+ * rows are kept; prefill segment j is sampled at its last row,
+ * cu_seqlens[num_decode + j + 1] - 1; pure-decode steps are unchanged; since
+ * logits are no longer row-aligned with the input, compacted prefix sums
+ * (logits_cu_seqlens) are emitted while cu_seqlens itself stays valid for
+ * other consumers.  Readings where the page is silent: a decode sequence of
+ * several rows keeps all of them; all_rows_mask[s] != 0 keeps every row of
+ * prefill segment s (prompt scoring of every position, openinfer issue #719,
+ * "Description").
+ *
+ *   cu_seqlens        device int32 [num_seqs + 1], cu[0] = 0, non-decreasing.
+ *   num_seqs          number of sequences S (>= 0).
+ *   num_decode        sequences [0, num_decode) are decode sequences.
+ *   all_rows_mask     device uint8 [num_seqs] or NULL (all zero).
+ *   max_out_rows      capacity of row_idx.
+ *   row_idx           device int32 [max_out_rows], out: selected rows, ascending.
+ *   logits_cu_seqlens device int32 [num_seqs + 1], out: logits_cu[0] = 0,
+ *                     logits_cu[s+1] = logits_cu[s] + rows taken from s.
+ *   dev_status        device uint32 or NULL.
+ * Bad cu_seqlens set LMH_DS_BAD_CU_SEQLENS; an offending sequence contributes
+ * no row.  More than max_out_rows rows set LMH_DS_ROWS_OVERFLOW (the rows
+ * beyond the capacity are dropped; logits_cu_seqlens keeps the full counts).
+ * Errors: LMH_ERR_INVALID_ARG for null pointers, negative sizes or
+ * num_decode > num_seqs.
+ */
+lmh_status lmh_select_rows(const int32_t* cu_seqlens, int32_t num_seqs, int32_t num_decode,
+                           const uint8_t* all_rows_mask, int32_t max_out_rows, int32_t* row_idx,
+                           int32_t* logits_cu_seqlens, uint32_t* dev_status, cudaStream_t stream);
+
+/*
+ * lmh_count_selected_rows -- host helper: the number of rows lmh_select_rows
+ * selects, computed from a HOST copy of cu_seqlens / all_rows_mask, so that a
+ * caller can size buffers and pass `rows` without a device synchronisation.
+ * Returns -1 for an invalid batch (same rules as above).
+ */
+int32_t lmh_count_selected_rows(const int32_t* cu_seqlens_host, int32_t num_seqs,
+                                int32_t num_decode, const uint8_t* all_rows_mask_host);
+
+/*
+ * lmh_workspace_bytes -- bytes of scratch the given entry point needs for
+ * these sizes on the current device (the split of the vocabulary depends on
+ * its SM count).  `hidden` is ignored for LMH_PATH_FROM_LOGITS.  Returns 0
+ * for sizes the entry point rejects.  The workspace must be 256-byte aligned.
+ */
+size_t lmh_workspace_bytes(int32_t rows, int32_t hidden, int32_t vocab, int32_t k_max,
+                           lmh_path path);
+
+/*
+ * lmh_project_logprobs -- selective head projection with a fused reduction.
+ *
+ * Defined by: vllm-metal release v0.4.0.dev20260831, "Summary" (gather the
+ * sampled rows and run the head on those alone); mlxcel PR #1969 (the row
+ * sliced before the head equals the full forward's row); MTPLX PR #532,
+ * "Change" (one fp32 logsumexp per row, a 64-logit block-max prefilter for
+ * the exact top-k, fp32(logit) - lse at the survivors and the scored token,
+ * exact ties by ascending id); openinfer issue #719, "Suggested direction"
+ * and "Acceptance criteria" (compute lse, the selected logprob and the top-k
+ * on the device and return an O(k+1) result).
+ *
+ * For row i: A[i] = hidden[row_idx[i]] (or hidden[i] when row_idx is NULL),
+ * z[i][v] = sum_h A[i][h] * W[h][v] with bf16 inputs and fp32 accumulation;
+ * lse[i] = log sum_v exp(z[i][v]); sel_logprob[i] = z[i][sel] - lse[i];
+ * topk_ids[i][r], topk_logprobs[i][r] for r < k_i = row_k[i] (or k_max):
+ * the r-th best (z desc, id asc); ranks r >= k_i hold id -1 and -inf.
+ *
+ *   hidden            device bf16 [num_tokens x H], row stride hidden_row_stride
+ *                     (>= H); 16-byte aligned base.
+ *   num_tokens        rows of `hidden` (bounds for row_idx).
+ *   row_idx           device int32 [rows] or NULL.
+ *   rows, H, V        sizes; H % 8 == 0.
+ *   W                 device bf16, layout w_layout (LMH_W_VH only), 16-byte aligned.
+ *   sel_ids           device int32 [rows] or NULL; -1 = no selected token (NaN).
+ *   row_k             device int32 [rows] or NULL (= k_max); values clamped to [0, k_max].
+ *   k_max             0..LMH_K_MAX and <= V.
+ *   lse               device fp32 [rows], out.
+ *   sel_logprob       device fp32 [rows], out (required when sel_ids != NULL).
+ *   topk_ids          device int32 [rows x k_max], out (required when k_max > 0).
+ *   topk_logprobs     device fp32 [rows x k_max], out (required when k_max > 0).
+ *   logits_out        device fp32 [rows x V] or NULL (16-byte aligned): when
+ *                     given, the fp32 logits are also written (the
+ *                     materializing arm and debugging); the reduction
+ *                     results are unchanged.
+ *   workspace         device, >= lmh_workspace_bytes(rows, H, V, k_max,
+ *                     LMH_PATH_PROJECT) bytes, 256-byte aligned.
+ * Errors: LMH_ERR_INVALID_ARG, LMH_ERR_UNSUPPORTED (k_max < 0 or > LMH_K_MAX,
+ * W layout LMH_W_HV, H % 8 != 0, misaligned pointers),
+ * LMH_ERR_WORKSPACE_TOO_SMALL, LMH_ERR_CUDA.  Device: LMH_DS_SEL_OUT_OF_RANGE,
+ * LMH_DS_ROW_IDX_OUT_OF_RANGE, LMH_DS_TIMEOUT.
+ */
+lmh_status lmh_project_logprobs(const void* hidden, int64_t hidden_row_stride, int32_t num_tokens,
+                                const int32_t* row_idx, int32_t rows, int32_t H, const void* W,
+                                lmh_w_layout w_layout, int32_t V, const int32_t* sel_ids,
+                                const int32_t* row_k, int32_t k_max, float* lse,
+                                float* sel_logprob, int32_t* topk_ids, float* topk_logprobs,
+                                float* logits_out, void* workspace, size_t workspace_bytes,
+                                uint32_t* dev_status, cudaStream_t stream);
+
+/*
+ * lmh_logprobs_from_logits -- the same per-row reduction for logits that are
+ * already in device memory (prompt scoring of logits chunks).
+ *
+ * Defined by MTPLX PR #532, "Summary" and "Change" (per 256-row chunk of
+ * 248,320 logits: one fp32 logsumexp per row; top-k through the 64-logit
+ * block-max prefilter that keeps the k blocks with the largest maxima and
+ * selects the exact top-k among their entries; fp32(logit) - lse only at the
+ * survivors and the scored token; exact ties by ascending id) and openinfer
+ * issue #719 (reusable for decode rows and batches of prompt positions).
+ *
+ *   logits            device [rows x V] of dtype, row stride row_stride (>= V);
+ *                     base 16-byte aligned and row_stride * sizeof(dtype) a
+ *                     multiple of 16.
+ *   sel_ids, row_k, k_max, lse, sel_logprob, topk_ids, topk_logprobs:
+ *                     as for lmh_project_logprobs (logit = the given value
+ *                     widened exactly to fp32).
+ *   workspace         >= lmh_workspace_bytes(rows, 0, V, k_max,
+ *                     LMH_PATH_FROM_LOGITS) bytes, 256-byte aligned.
+ * Results for NaN or +inf logits are unspecified.  A row of only -inf gives
+ * lse = -inf and NaN logprobs (ids 0..k-1).
+ * Errors: as lmh_project_logprobs.
+ */
+lmh_status lmh_logprobs_from_logits(const void* logits, lmh_dtype dtype, int32_t rows, int32_t V,
+                                    int64_t row_stride, const int32_t* sel_ids,
+                                    const int32_t* row_k, int32_t k_max, float* lse,
+                                    float* sel_logprob, int32_t* topk_ids, float* topk_logprobs,
+                                    void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                    cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* lmh_status_string(lmh_status status);
+
+/* LMH_VERSION of the loaded library. */
+int32_t lmh_version(void);
+
+/*
+ * Kernel tracing (device time per kernel, measured with CUDA events recorded
+ * on the launching stream around every launch while enabled).  Not for use
+ * while a stream is being captured into a CUDA graph.
+ *
+ * lmh_trace_enable(1) starts recording, lmh_trace_enable(0) stops.
+ * lmh_trace_read waits for the recorded events, then reports the launches
+ * and total milliseconds of the named kernel ("select_rows", "gather_rows",
+ * "head_logprobs", "logits_reduce", "merge_partials") since the last reset.
+ * lmh_trace_reset clears the totals.
+ */
+lmh_status lmh_trace_enable(int32_t enable);
+lmh_status lmh_trace_read(const char* kernel, int64_t* launches, double* total_ms);
+void lmh_trace_reset(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LMH_H */

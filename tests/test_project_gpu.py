@@ -1,0 +1,177 @@
+"""lmh_project_logprobs (row gather + tcgen05 head + fused reduction) vs the oracle.
+
+Fused-head acceptance (tests/parity.py): logits, lse and logprobs within 2e-2
+absolute of the f64 oracle; top-k ids bit-exact or a certified near-tie.
+Workloads: the tiny packed batch, the decode batch (K 5 and 1), the
+selective prefill batch, the mixed Llama-3-8B-shaped step and the full
+16384-row projection arm (sampled rows), plus ragged shapes and invariants.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity import TOL_FUSED, assert_close, check_fused
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return workloads.bits(t)
+
+
+def gpu_select(lmh, b):
+    cu = b["cu_seqlens"].cuda()
+    mask = None if b["all_rows_mask"] is None else b["all_rows_mask"].cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ri, _ = lmh.select_rows(cu, b["num_decode"], mask, max_out_rows=b["n_sel"], dev_status=st)
+    return ri, st
+
+
+def gpu_project(lmh, hidden_d, W_d, row_idx=None, rows=None, sel=None, row_k=None, k=5, materialize=False):
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    n = rows if rows is not None else (row_idx.numel() if row_idx is not None else hidden_d.shape[0])
+    logits = torch.empty((n, W_d.shape[0]), dtype=torch.float32, device="cuda") if materialize else None
+    o = lmh.project_logprobs(hidden_d, W_d, row_idx=row_idx, rows=rows, sel=sel, row_k=row_k, k_max=k,
+                             logits_out=logits, dev_status=st)
+    torch.cuda.synchronize()
+    return o, int(st.item()), logits
+
+
+def oracle_rows(b, packed_rows, sel, k, row_k=None):
+    """Oracle projection + reduction of the given packed rows."""
+    rows = np.asarray(packed_rows, dtype=np.int32)
+    z = oracle.project(_bits(b["hidden"]), _bits(b["W"]), row_idx=rows)
+    orc = oracle.logprobs(z, sel=None if sel is None else np.asarray(sel), row_k=row_k, k_max=k)
+    A = b["hidden"][torch.as_tensor(rows.astype(np.int64))].float().double().numpy()
+    return z, orc, A
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return workloads.tiny_batch()
+
+
+@pytest.fixture(scope="module")
+def decode():
+    b = workloads.decode_batch()
+    b["hidden_d"], b["W_d"] = b["hidden"].cuda(), b["W"].cuda()
+    return b
+
+
+@pytest.fixture(scope="module")
+def prefill():
+    b = workloads.prefill_batch()
+    b["hidden_d"], b["W_d"] = b["hidden"].cuda(), b["W"].cuda()
+    return b
+
+
+def test_tiny_batch(lmh, tiny):
+    b = tiny
+    ri, st_sel = gpu_select(lmh, b)
+    o, st, logits = gpu_project(lmh, b["hidden"].cuda(), b["W"].cuda(), row_idx=ri, sel=b["sel"], k=5,
+                                materialize=True)
+    assert st == 0 and int(st_sel.item()) == 0
+    want_ri, _ = oracle.select_rows(b["cu_seqlens"].numpy(), b["num_decode"])
+    assert np.array_equal(ri.cpu().numpy(), want_ri)
+    z, orc, A = oracle_rows(b, want_ri, b["sel"], 5)
+    assert_close(logits.cpu().numpy(), z, TOL_FUSED, "tiny logits")
+    assert check_fused(o, orc, z, A, b["W"], 5, what="tiny") == 0
+
+
+@pytest.mark.parametrize("k", [5, 1])
+def test_decode_batch(lmh, decode, k):
+    b = decode
+    o, st, _ = gpu_project(lmh, b["hidden_d"], b["W_d"], sel=b["sel"], k=k)
+    assert st == 0
+    z, orc, A = oracle_rows(b, np.arange(32), b["sel"], k)
+    check_fused(o, orc, z, A, b["W"], k, what="decode K=%d" % k)
+
+
+def test_prefill_selective(lmh, prefill):
+    b = prefill
+    ri, _ = gpu_select(lmh, b)
+    o, st, _ = gpu_project(lmh, b["hidden_d"], b["W_d"], row_idx=ri, sel=b["sel"], k=20)
+    assert st == 0
+    assert ri.cpu().tolist() == [2048 * (j + 1) - 1 for j in range(8)]
+    z, orc, A = oracle_rows(b, ri.cpu().numpy(), b["sel"], 20)
+    check_fused(o, orc, z, A, b["W"], 20, what="prefill selective")
+
+
+def test_full_projection_arm_sampled(lmh, prefill):
+    """All 16384 rows through the head (the 'before' arm), K=20; sampled rows vs the oracle."""
+    b = prefill
+    o, st, _ = gpu_project(lmh, b["hidden_d"], b["W_d"], sel=b["sel_all"], k=20)
+    assert st == 0
+    rng = np.random.default_rng(0)
+    sample = np.unique(np.concatenate([[0, 127, 128, 2047, 16383], rng.choice(16384, 11, replace=False)]))
+    z, orc, A = oracle_rows(b, sample, b["sel_all"][sample], 20)
+    sub = {key: v[torch.as_tensor(sample)] for key, v in o.items() if v is not None}
+    check_fused(sub, orc, z, A, b["W"], 20, what="full arm")
+
+
+def test_mixed_step_sampled(lmh):
+    b = workloads.mixed_batch()
+    hidden_d, W_d = b["hidden"].cuda(), b["W"].cuda()
+    ri, st_sel = gpu_select(lmh, b)
+    o, st, _ = gpu_project(lmh, hidden_d, W_d, row_idx=ri, sel=b["sel"], row_k=b["row_k"], k=20)
+    assert st == 0 and int(st_sel.item()) == 0
+    want_ri, _ = oracle.select_rows(b["cu_seqlens"].numpy(), b["num_decode"], b["all_rows_mask"].numpy())
+    assert np.array_equal(ri.cpu().numpy(), want_ri)
+    sample = np.array([0, 5, 31, 32, 63, 64, 65, 67, 68, 69, 500, 1000, 1090, 1091])
+    rk = b["row_k"][sample].numpy()
+    z, orc, A = oracle_rows(b, want_ri[sample], b["sel"][sample], 20, row_k=rk)
+    sub = {key: v[torch.as_tensor(sample)] for key, v in o.items() if v is not None}
+    check_fused(sub, orc, z, A, b["W"], 20, row_k=rk, what="mixed")
+
+
+@pytest.mark.parametrize("rows,H,V,k", [(200, 136, 4100, 20), (129, 64, 1000, 128), (3, 520, 70000, 0),
+                                        (1, 8, 300, 7), (300, 1024, 20000, 33)])
+def test_ragged_shapes(lmh, rows, H, V, k):
+    g = torch.Generator().manual_seed(rows * 7 + H)
+    T = rows + 5
+    b = {"hidden": torch.randn(T, H, generator=g).to(torch.bfloat16),
+         "W": (torch.randn(V, H, generator=g) / H ** 0.5).to(torch.bfloat16)}
+    ri = torch.randperm(T, generator=g)[:rows].to(torch.int32)
+    sel = torch.randint(-1, V, (rows,), generator=g, dtype=torch.int32)
+    o, st, logits = gpu_project(lmh, b["hidden"].cuda(), b["W"].cuda(), row_idx=ri.cuda(), sel=sel, k=k,
+                                materialize=True)
+    assert st == 0
+    z, orc, A = oracle_rows(b, ri.numpy(), sel, k)
+    assert_close(logits.cpu().numpy(), z, TOL_FUSED, "ragged logits")
+    check_fused(o, orc, z, A, b["W"], k, what="ragged %s" % ((rows, H, V, k),))
+
+
+def test_fused_equals_reduction_of_its_own_logits(lmh, decode):
+    """The fused epilogue reduces exactly the fp32 logits the same kernel writes out."""
+    b = decode
+    o, st, logits = gpu_project(lmh, b["hidden_d"], b["W_d"], sel=b["sel"], k=20, materialize=True)
+    assert st == 0
+    r = lmh.logprobs_from_logits(logits, sel=b["sel"], k_max=20)
+    torch.cuda.synchronize()
+    assert torch.equal(o["topk_ids"], r["topk_ids"])
+    assert torch.allclose(o["lse"], r["lse"], rtol=1e-6, atol=0)
+    assert torch.allclose(o["topk_logprobs"], r["topk_logprobs"], rtol=0, atol=1e-5)
+    assert torch.allclose(o["sel_logprob"], r["sel_logprob"], rtol=0, atol=1e-5)
+
+
+def test_selected_rows_equal_full_projection_sliced(lmh, tiny):
+    """mlxcel PR #1969: the row sliced before the head equals the full forward's row."""
+    b = tiny
+    hidden_d, W_d = b["hidden"].cuda(), b["W"].cuda()
+    ri, _ = gpu_select(lmh, b)
+    _, _, sel_logits = gpu_project(lmh, hidden_d, W_d, row_idx=ri, k=0, materialize=True)
+    _, _, full_logits = gpu_project(lmh, hidden_d, W_d, k=0, materialize=True)
+    assert torch.equal(sel_logits, full_logits[ri.long()])
+    shifted = torch.clamp(ri + 1, max=63)
+    assert not torch.equal(sel_logits, full_logits[shifted.long()])
+
+
+def test_row_idx_out_of_range_sets_status(lmh, tiny):
+    from top_reduction_gb300 import lmh as L
+    b = tiny
+    ri = torch.tensor([0, 64, 5], dtype=torch.int32, device="cuda")  # 64 == num_tokens
+    o, st, logits = gpu_project(lmh, b["hidden"].cuda(), b["W"].cuda(), row_idx=ri, k=3, materialize=True)
+    assert st & L.DS_ROW_IDX_OUT_OF_RANGE
+    assert torch.count_nonzero(logits[1]) == 0

@@ -1,0 +1,558 @@
+// head_gemm.cu -- selective head projection with a fused per-row reduction
+// (K2 row gather + K3 tensor-core kernel).
+//
+// vllm-metal release v0.4.0.dev20260831, "Summary": gather the sampled rows
+// and run the head on those alone.  MTPLX PR #532, "Change" and openinfer
+// issue #719, "Suggested direction": per row one fp32 logsumexp, the selected
+// token's logprob and the exact top-k, returned as an O(k+1) result; for
+// finite k the [rows x vocab] logits are never written to memory.
+//
+// GB300 design (sm_103a):
+//   * D[128 rows x 256 vocab] tiles, z = A . W^T with A = gathered hidden rows
+//     [rows x H] and W = lm_head.weight [V x H]; both operands are K-major.
+//   * warp 0: TMA producer.  64-element (128-byte) slices of A and W are
+//     loaded with cp.async.bulk.tensor into a ring of shared-memory stages
+//     using the 128-byte swizzle, completing on "full" mbarriers.
+//   * warp 1: allocates 512 TMEM columns (two 256-column fp32 accumulators)
+//     and one thread issues tcgen05.mma (kind::f16, bf16 in, fp32 out in
+//     TMEM); tcgen05.commit frees a stage ("empty") once its MMAs have read
+//     it and signals an accumulator ("acc_full") when a tile is complete.
+//   * warps 2..5: epilogue.  Warp w reads TMEM lanes 32*(w%4)..+31, so each
+//     thread owns one row.  Per 64-column block it keeps the running max m
+//     and sum exp(z - m) (online rescaling), the block maximum, and inserts
+//     into the row's sorted top-k list only the entries of blocks whose
+//     maximum exceeds the current k-th value tau (the block-max prefilter
+//     applied while streaming; ids ascend within a CTA's range, so an equal
+//     value never displaces an earlier id).  It also captures z[row][sel].
+//   * Persistent CTAs walk "units" = (128-row tile, vocabulary range); the
+//     per-row state lives across the n-tiles of a unit and is flushed as one
+//     partial per (row, range) that merge_partials.cu combines.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "device_common.cuh"
+#include "lmh_internal.h"
+
+namespace lmh {
+
+constexpr int kBM = 128;    // rows per tile = TMEM lanes
+constexpr int kBN = 256;    // vocabulary columns per tile = fp32 TMEM columns per accumulator
+constexpr int kBK = 64;     // hidden elements per stage: one 128-byte swizzle row
+constexpr int kUmmaK = 16;  // K of one tcgen05.mma kind::f16
+constexpr int kHeadThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr uint32_t kStageBytesA = kBM * kBK * 2;  // 16 KB
+constexpr uint32_t kStageBytesB = kBN * kBK * 2;  // 32 KB
+
+template <int KCAP>
+struct HeadCfg {
+  static constexpr int kStages = KCAP <= 32 ? 4 : 2;
+  static constexpr size_t kListBytes = static_cast<size_t>(kBM) * KCAP * 8;
+  static constexpr size_t kSmem = 1024 /*alignment slack*/ + kStages * (kStageBytesA + kStageBytesB) +
+                                  kListBytes + (2 * kStages + 4) * 8 + 16;
+};
+
+struct HeadArgs {
+  int rows, H, V, k_max;
+  int m_tiles, n_tiles, splits, tiles_per_split, num_units;
+  const int32_t* sel;
+  const int32_t* row_k;
+  Partials parts;
+  float* logits_out;
+  uint32_t* dev_status;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers: TMA, tcgen05
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+      "[%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), descriptor
+// version 1, leading byte offset unused for this layout (set to 16 bytes).
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(16u >> 4) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N = kBN, M = kBM.
+constexpr uint32_t kIdesc = (1u << 4)                                   // D format: f32
+                            | (1u << 7)                                 // A format: bf16
+                            | (1u << 10)                                // B format: bf16
+                            | (static_cast<uint32_t>(kBN >> 3) << 17)   // N / 8
+                            | (static_cast<uint32_t>(kBM >> 4) << 24);  // M / 16
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Load 64 consecutive fp32 columns of this thread's TMEM lane and wait for
+// them in the same asm statement, so no use of the registers can be scheduled
+// before tcgen05.wait::ld.  Warp-collective: the whole warp must be converged.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Wait on an mbarrier unless the CTA has aborted; on timeout mark the abort.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              uint32_t* dev_status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      set_status(dev_status, LMH_DS_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// per-row sorted candidate list in shared memory (slot-major: list[j*128+r])
+// ---------------------------------------------------------------------------
+struct ListState {
+  float tau;  // value of the k-th entry once the list is full, else -inf
+  int cnt;
+};
+
+__device__ __noinline__ ListState list_insert(uint64_t* list, int r, ListState st, int k, uint64_t key) {
+  int pos;
+  if (st.cnt < k) {
+    pos = st.cnt++;
+  } else {
+    pos = k - 1;  // the caller only inserts keys above the current k-th
+  }
+  while (pos > 0) {
+    const uint64_t up = list[(pos - 1) * kBM + r];
+    if (up >= key) break;
+    list[pos * kBM + r] = up;
+    --pos;
+  }
+  list[pos * kBM + r] = key;
+  st.tau = (st.cnt == k) ? key_value(list[(k - 1) * kBM + r]) : -INFINITY;
+  return st;
+}
+
+// ---------------------------------------------------------------------------
+// the fused kernel
+// ---------------------------------------------------------------------------
+template <int KCAP, bool kMaterialize>
+__global__ void __launch_bounds__(kHeadThreads, 1)
+    head_logprobs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                         const HeadArgs a) {
+  using Cfg = HeadCfg<KCAP>;
+  constexpr int S = Cfg::kStages;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* sA = smem;
+  unsigned char* sB = sA + S * kStageBytesA;
+  uint64_t* lists = reinterpret_cast<uint64_t*>(sB + S * kStageBytesB);
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(lists) + Cfg::kListBytes);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int k_blocks = (a.H + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4 * 32);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------- TMA producer -------------------------
+    if (lane == 0) {
+      prefetch_tmap(&tmap_a);
+      prefetch_tmap(&tmap_b);
+      uint32_t it = 0;
+      bool live = true;
+      for (int u = blockIdx.x; u < a.num_units && live; u += gridDim.x) {
+        const int m_tile = u % a.m_tiles, split = u / a.m_tiles;
+        const int n_begin = split * a.tiles_per_split;
+        const int n_end = min(n_begin + a.tiles_per_split, a.n_tiles);
+        for (int n = n_begin; n < n_end && live; ++n) {
+          for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (it / S) & 1u;
+            if (!wait_or_abort(&empty[s], ph ^ 1u, abort_flag, a.dev_status)) {
+              live = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[s], kStageBytesA + kStageBytesB);
+            tma_load_2d(sA + s * kStageBytesA, &tmap_a, kb * kBK, m_tile * kBM, &full[s]);
+            tma_load_2d(sB + s * kStageBytesB, &tmap_b, kb * kBK, n * kBN, &full[s]);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------- MMA issuer -------------------------
+    if (lane == 0) {
+      uint32_t it = 0, t = 0;
+      bool live = true;
+      for (int u = blockIdx.x; u < a.num_units && live; u += gridDim.x) {
+        const int split = u / a.m_tiles;
+        const int n_begin = split * a.tiles_per_split;
+        const int n_end = min(n_begin + a.tiles_per_split, a.n_tiles);
+        for (int n = n_begin; n < n_end && live; ++n, ++t) {
+          const uint32_t b = t & 1u, aph = (t >> 1) & 1u;
+          if (!wait_or_abort(&acc_empty[b], aph ^ 1u, abort_flag, a.dev_status)) {
+            live = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + b * kBN;
+          for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (it / S) & 1u;
+            if (!wait_or_abort(&full[s], ph, abort_flag, a.dev_status)) {
+              live = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(sA + s * kStageBytesA);
+            const uint32_t b_addr = smem_u32(sB + s * kStageBytesB);
+#pragma unroll
+            for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+              const uint64_t ad = sw128_kmajor_desc(a_addr + kk * kUmmaK * 2);
+              const uint64_t bd = sw128_kmajor_desc(b_addr + kk * kUmmaK * 2);
+              umma_bf16(d_tmem, ad, bd, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(&empty[s]);
+          }
+          if (live) umma_commit(&acc_full[b]);
+        }
+      }
+    }
+  } else {
+    // ------------------------- epilogue -------------------------
+    const int q = warp & 3;             // TMEM lane quarter of this warp
+    const int r_local = q * 32 + lane;  // row within the tile
+    const float L = kLog2e;
+    uint32_t t = 0;
+    bool live = true;
+    for (int u = blockIdx.x; u < a.num_units && live; u += gridDim.x) {
+      const int m_tile = u % a.m_tiles, split = u / a.m_tiles;
+      const int n_begin = split * a.tiles_per_split;
+      const int n_end = min(n_begin + a.tiles_per_split, a.n_tiles);
+      const int row = m_tile * kBM + r_local;
+      const bool valid = row < a.rows;
+      const bool warp_active = (m_tile * kBM + q * 32) < a.rows;
+      int k_row = 0, sel_id = -1;
+      if (valid) {
+        k_row = a.k_max;
+        if (a.row_k) k_row = min(max(a.row_k[row], 0), a.k_max);
+        if (a.sel) sel_id = a.sel[row];
+      }
+      float m = -INFINITY, ssum = 0.0f, sel_val = 0.0f;
+      bool has_sel = false;
+      ListState st;
+      st.tau = -INFINITY;
+      st.cnt = 0;
+      for (int n = n_begin; n < n_end; ++n, ++t) {
+        const uint32_t b = t & 1u, aph = (t >> 1) & 1u;
+        if (!wait_or_abort(&acc_full[b], aph, abort_flag, a.dev_status)) {
+          live = false;
+          break;
+        }
+        tc_fence_after();
+        if (warp_active) {
+#pragma unroll 1
+          for (int c = 0; c < kBN / kBlock; ++c) {
+            const int col0 = n * kBN + c * kBlock;
+            if (col0 >= a.V) break;  // uniform across the warp
+            float v[kBlock];
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kBN + c * kBlock;
+            __syncwarp();
+            tmem_ld64(taddr, v);
+            const int nvalid = a.V - col0;
+            if (nvalid < kBlock) {
+#pragma unroll
+              for (int j = 0; j < kBlock; ++j)
+                if (j >= nvalid) v[j] = -INFINITY;
+            }
+            if (!valid) continue;
+            if (kMaterialize) {
+              float* dst = a.logits_out + static_cast<int64_t>(row) * a.V + col0;
+              if ((a.V & 3) == 0 && nvalid >= kBlock) {
+#pragma unroll
+                for (int j = 0; j < kBlock; j += 4)
+                  *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < kBlock; ++j)
+                  if (j < nvalid) dst[j] = v[j];
+              }
+            }
+            float bm = v[0];
+#pragma unroll
+            for (int j = 1; j < kBlock; ++j) bm = fmaxf(bm, v[j]);
+            if (bm > m) {
+              ssum *= ex2_approx((m - bm) * L);
+              m = bm;
+            }
+            const float mL = m * L;
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < kBlock; j += 2) {
+              acc0 += ex2_approx(fmaf(v[j], L, -mL));
+              acc1 += ex2_approx(fmaf(v[j + 1], L, -mL));
+            }
+            ssum += acc0 + acc1;
+            const unsigned rel = static_cast<unsigned>(sel_id - col0);
+            if (rel < static_cast<unsigned>(kBlock)) {
+              float sv = 0.0f;
+#pragma unroll
+              for (int j = 0; j < kBlock; ++j) sv = (static_cast<unsigned>(j) == rel) ? v[j] : sv;
+              sel_val = sv;
+              has_sel = true;
+            }
+            if (k_row > 0 && bm > st.tau) {
+#pragma unroll
+              for (int j = 0; j < kBlock; ++j)
+                if (v[j] > st.tau) st = list_insert(lists, r_local, st, k_row, make_key(v[j], col0 + j));
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[b]);
+      }
+      if (!live) break;
+      if (valid) {
+        const int64_t pidx = static_cast<int64_t>(row) * a.splits + split;
+        a.parts.part_ms[pidx] = make_float2(m, ssum);
+        unsigned long long* out = a.parts.part_keys + pidx * a.k_max;
+        for (int j = 0; j < k_row; ++j) out[j] = (j < st.cnt) ? lists[j * kBM + r_local] : 0ull;
+        if (has_sel) a.parts.sel_logit[row] = sel_val;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// row gather (K2): out[i, :] = hidden[row_idx[i], :]
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ hidden, int64_t stride,
+                                                          int num_tokens, const int32_t* __restrict__ row_idx,
+                                                          int H, uint16_t* __restrict__ out, uint32_t* dev_status) {
+  const int i = blockIdx.x;
+  const int src = row_idx ? row_idx[i] : i;
+  const bool ok = src >= 0 && src < num_tokens;
+  if (!ok && threadIdx.x == 0) set_status(dev_status, LMH_DS_ROW_IDX_OUT_OF_RANGE);
+  uint16_t* dst = out + static_cast<int64_t>(i) * H;
+  const uint16_t* s = hidden + static_cast<int64_t>(ok ? src : 0) * stride;
+  const bool vec = ((stride & 7) == 0) && ((reinterpret_cast<uintptr_t>(hidden) & 15) == 0);
+  if (vec) {
+    const int nv = H / 8;
+    for (int j = threadIdx.x; j < nv; j += blockDim.x)
+      reinterpret_cast<uint4*>(dst)[j] = ok ? reinterpret_cast<const uint4*>(s)[j] : make_uint4(0, 0, 0, 0);
+  } else {
+    for (int j = threadIdx.x; j < H; j += blockDim.x) dst[j] = ok ? s[j] : static_cast<uint16_t>(0);
+  }
+}
+
+cudaError_t launch_gather_rows(const void* hidden, int64_t hidden_stride, int num_tokens, const int32_t* row_idx,
+                               int rows, int H, void* out, uint32_t* dev_status, cudaStream_t stream) {
+  gather_rows_kernel<<<rows, 256, 0, stream>>>(static_cast<const uint16_t*>(hidden), hidden_stride, num_tokens,
+                                               row_idx, H, static_cast<uint16_t*>(out), dev_status);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// host side: plan, tensor maps, launch
+// ---------------------------------------------------------------------------
+
+HeadPlan head_plan(int rows, int H, int V, int k_max, int num_sms) {
+  (void)H;
+  HeadPlan p;
+  p.m_tiles = (rows + kBM - 1) / kBM;
+  p.n_tiles = (V + kBN - 1) / kBN;
+  p.kcap = k_max <= 32 ? 32 : 128;
+  const int G = num_sms > 0 ? num_sms : 1;
+  // choose the vocabulary split that minimises the busiest CTA's tile count
+  // (plus a small cost per unit for its flush and pipeline refill)
+  double best = 1e300;
+  int best_s = 1;
+  for (int s = 1; s <= p.n_tiles; ++s) {
+    const int tps = (p.n_tiles + s - 1) / s;
+    const int units = p.m_tiles * ((p.n_tiles + tps - 1) / tps);
+    const int waves = (units + G - 1) / G;
+    const double cost = static_cast<double>(waves) * (tps + 0.25);
+    if (cost < best - 1e-9) {
+      best = cost;
+      best_s = s;
+    }
+  }
+  p.tiles_per_split = (p.n_tiles + best_s - 1) / best_s;
+  p.splits = (p.n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+  const int units = p.m_tiles * p.splits;
+  p.grid = units < G ? units : G;
+  return p;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+static cudaError_t get_encode(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::call_once(g_encode_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  *fn = g_encode;
+  return g_encode ? cudaSuccess : cudaErrorNotSupported;
+}
+
+// 2-D bf16 tensor map over a row-major [outer x inner] matrix with `pitch` elements per row.
+static cudaError_t make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
+                             uint32_t box_inner, uint32_t box_outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  cudaError_t e = get_encode(&enc);
+  if (e != cudaSuccess) return e;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int KCAP, bool M>
+static cudaError_t set_head_attr() {
+  return cudaFuncSetAttribute(head_logprobs_kernel<KCAP, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(HeadCfg<KCAP>::kSmem));
+}
+
+cudaError_t head_setup() {
+  cudaError_t e = set_head_attr<32, false>();
+  if (e == cudaSuccess) e = set_head_attr<32, true>();
+  if (e == cudaSuccess) e = set_head_attr<128, false>();
+  if (e == cudaSuccess) e = set_head_attr<128, true>();
+  return e;
+}
+
+cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const void* W, int V, const HeadPlan& plan,
+                        const int32_t* sel, const int32_t* row_k, int k_max, Partials parts, float* logits_out,
+                        uint32_t* dev_status, cudaStream_t stream) {
+  CUtensorMap ta, tb;
+  cudaError_t e = make_tmap(&ta, A, static_cast<uint64_t>(H), static_cast<uint64_t>(rows),
+                            static_cast<uint64_t>(a_stride), kBK, kBM);
+  if (e != cudaSuccess) return e;
+  e = make_tmap(&tb, W, static_cast<uint64_t>(H), static_cast<uint64_t>(V), static_cast<uint64_t>(H), kBK, kBN);
+  if (e != cudaSuccess) return e;
+  HeadArgs a;
+  a.rows = rows;
+  a.H = H;
+  a.V = V;
+  a.k_max = k_max;
+  a.m_tiles = plan.m_tiles;
+  a.n_tiles = plan.n_tiles;
+  a.splits = plan.splits;
+  a.tiles_per_split = plan.tiles_per_split;
+  a.num_units = plan.m_tiles * plan.splits;
+  a.sel = sel;
+  a.row_k = row_k;
+  a.parts = parts;
+  a.logits_out = logits_out;
+  a.dev_status = dev_status;
+  const dim3 grid(plan.grid), block(kHeadThreads);
+  if (plan.kcap == 32) {
+    if (logits_out)
+      head_logprobs_kernel<32, true><<<grid, block, HeadCfg<32>::kSmem, stream>>>(ta, tb, a);
+    else
+      head_logprobs_kernel<32, false><<<grid, block, HeadCfg<32>::kSmem, stream>>>(ta, tb, a);
+  } else {
+    if (logits_out)
+      head_logprobs_kernel<128, true><<<grid, block, HeadCfg<128>::kSmem, stream>>>(ta, tb, a);
+    else
+      head_logprobs_kernel<128, false><<<grid, block, HeadCfg<128>::kSmem, stream>>>(ta, tb, a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace lmh

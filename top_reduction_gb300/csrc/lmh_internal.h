@@ -1,0 +1,81 @@
+// lmh_internal.h -- host-side interfaces between the C ABI (lmh_api.cu) and
+// the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "lmh.h"
+
+namespace lmh {
+
+constexpr int kBlock = 64;  // logits per prefilter block (MTPLX PR #532, "Change")
+
+// Split of one row's vocabulary into per-CTA chunks of whole 64-blocks.
+struct VocabSplit {
+  int splits;            // chunks per row
+  int blocks_per_split;  // 64-blocks per chunk (the last chunk may have fewer)
+};
+
+// Per-(row, split) partial results, laid out in the caller's workspace:
+//   part_ms   float2 [rows * splits]            (chunk max m, sum exp(x - m))
+//   part_keys uint64 [rows * splits * k_max]    sorted top-k keys of the chunk
+//   sel_logit float  [rows]                     logit of the selected token
+struct Partials {
+  float2* part_ms;
+  unsigned long long* part_keys;
+  float* sel_logit;
+};
+
+size_t partials_bytes(int rows, int splits, int k_max);
+Partials carve_partials(void* base, int rows, int splits, int k_max);
+
+// One-time per-device set-up (kernel attributes).  Returns cudaSuccess or the error.
+cudaError_t logits_reduce_setup();
+cudaError_t merge_setup();
+cudaError_t head_setup();
+
+VocabSplit logits_reduce_split(int rows, int V, int num_sms);
+
+cudaError_t launch_select_rows(const int32_t* cu, int num_seqs, int num_decode, const uint8_t* mask,
+                               int max_out, int32_t* row_idx, int32_t* logits_cu, uint32_t* dev_status,
+                               cudaStream_t stream);
+
+cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t row_stride, int rows, int V,
+                                 VocabSplit split, const int32_t* sel, const int32_t* row_k, int k_max,
+                                 Partials parts, uint32_t* dev_status, cudaStream_t stream);
+
+cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts, const int32_t* sel,
+                         const int32_t* row_k, float* lse, float* sel_logprob, int32_t* topk_ids,
+                         float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream);
+
+// ---- head projection (head_gemm.cu) ----
+
+// Tile scheduling of the fused head kernel.
+struct HeadPlan {
+  int m_tiles;          // ceil(rows / 128)
+  int n_tiles;          // ceil(V / 256)
+  int splits;           // vocabulary ranges per row (units = m_tiles * splits)
+  int tiles_per_split;  // n-tiles per range
+  int grid;             // persistent CTAs
+  int kcap;             // per-row candidate capacity variant (32 or 128)
+};
+
+HeadPlan head_plan(int rows, int H, int V, int k_max, int num_sms);
+
+cudaError_t launch_gather_rows(const void* hidden, int64_t hidden_stride, int num_tokens,
+                               const int32_t* row_idx, int rows, int H, void* out, uint32_t* dev_status,
+                               cudaStream_t stream);
+
+cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const void* W, int V,
+                        const HeadPlan& plan, const int32_t* sel, const int32_t* row_k, int k_max,
+                        Partials parts, float* logits_out, uint32_t* dev_status, cudaStream_t stream);
+
+// ---- tracing (lmh_api.cu) ----
+enum TraceKernel { kTraceSelect = 0, kTraceGather, kTraceHead, kTraceReduce, kTraceMerge, kTraceCount };
+void trace_begin(TraceKernel k, cudaStream_t s);
+void trace_end(TraceKernel k, cudaStream_t s);
+
+}  // namespace lmh

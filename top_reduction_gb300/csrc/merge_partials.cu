@@ -1,0 +1,164 @@
+// merge_partials.cu -- combine the per-chunk partials of every row (K5).
+//
+// openinfer issue #719, "Suggested direction": a numerically sound
+// multi-stage reduction that returns lse, the selected-token logprob and the
+// top-k as an O(k+1) result.  MTPLX PR #532, "Change": logprob = fp32(logit)
+// - lse, evaluated only at the survivors and at the scored token; exact ties
+// by ascending id.
+//
+// One CTA per row:
+//   lse = M + log(sum_j s_j * exp(m_j - M)) over the row's chunks j, with
+//         M = max_j m_j (lse = -inf when every logit is -inf);
+//   top-k = the k best keys of the union of the chunks' sorted top-k lists.
+//         Every chunk list holds that chunk's k best, so the union holds the
+//         row's k best.  L = max over chunks of their k-th key is a lower
+//         bound of the row's k-th key (one chunk alone has k keys >= L), so
+//         only keys >= L are gathered and sorted.
+#include "device_common.cuh"
+#include "lmh_internal.h"
+
+namespace lmh {
+
+constexpr int kMergeThreads = 256;
+constexpr int kMergeCap = 1024;
+
+struct MergeArgs {
+  int rows, splits, V, k_max;
+  Partials parts;
+  const int32_t* sel;
+  const int32_t* row_k;
+  float* lse;
+  float* sel_logprob;
+  int32_t* topk_ids;
+  float* topk_logprobs;
+  uint32_t* dev_status;
+};
+
+__global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const MergeArgs a) {
+  __shared__ uint64_t cand[kMergeCap];
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t misc[4];
+  __shared__ float red[32];
+  __shared__ uint64_t red64[32];
+
+  const int row = blockIdx.x;
+  const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.splits;
+
+  // ---- lse ----
+  float tm = -INFINITY, ts = 0.0f;
+  for (int j = threadIdx.x; j < a.splits; j += kMergeThreads) {
+    const float2 p = ms[j];
+    if (p.x > tm) {
+      ts = (tm == -INFINITY) ? 0.0f : ts * expf(tm - p.x);
+      tm = p.x;
+    }
+    if (p.x != -INFINITY) ts += p.y * expf(p.x - tm);
+  }
+  const float M = block_max(tm, red);
+  const float S = block_sum((tm == -INFINITY) ? 0.0f : ts * expf(tm - M), red);
+  const float lse = (M == -INFINITY) ? -INFINITY : M + logf(S);
+
+  if (threadIdx.x == 0) {
+    a.lse[row] = lse;
+    if (a.sel) {
+      const int t = a.sel[row];
+      float v = __int_as_float(0x7fc00000);  // NaN: no selected token / out of range
+      if (t >= 0 && t < a.V)
+        v = a.parts.sel_logit[row] - lse;
+      else if (t != -1)
+        set_status(a.dev_status, LMH_DS_SEL_OUT_OF_RANGE);
+      a.sel_logprob[row] = v;
+    }
+    misc[0] = 0;
+  }
+  if (a.k_max == 0) return;
+
+  int k = a.k_max;
+  if (a.row_k) k = min(max(a.row_k[row], 0), a.k_max);
+  int32_t* out_ids = a.topk_ids + static_cast<int64_t>(row) * a.k_max;
+  float* out_lp = a.topk_logprobs + static_cast<int64_t>(row) * a.k_max;
+  for (int r = k + threadIdx.x; r < a.k_max; r += kMergeThreads) {
+    out_ids[r] = -1;
+    out_lp[r] = -INFINITY;
+  }
+  if (k == 0) return;
+
+  const unsigned long long* keys = a.parts.part_keys + static_cast<int64_t>(row) * a.splits * a.k_max;
+  // lower bound of the row's k-th key
+  uint64_t lb = 0;
+  for (int j = threadIdx.x; j < a.splits; j += kMergeThreads) {
+    const uint64_t kk = keys[static_cast<int64_t>(j) * a.k_max + (k - 1)];
+    lb = kk > lb ? kk : lb;
+  }
+  lb = block_max_u64(lb, red64);
+
+  const int n_items = a.splits * k;
+  auto in_set = [&](int i, uint64_t* key) -> bool {
+    const int j = i / k, r = i - j * k;
+    const uint64_t kk = keys[static_cast<int64_t>(j) * a.k_max + r];
+    if (kk == 0ull || kk < lb) return false;
+    *key = kk;
+    return true;
+  };
+  __syncthreads();
+  for (int i = threadIdx.x; i < n_items; i += kMergeThreads) {
+    uint64_t key = 0;
+    if (in_set(i, &key)) {
+      const uint32_t pos = atomicAdd(&misc[0], 1u);
+      if (pos < kMergeCap) cand[pos] = key;
+    }
+  }
+  __syncthreads();
+  const int cnt = static_cast<int>(misc[0]);
+  int nsort = cnt;
+  if (cnt > kMergeCap) {
+    int above;
+    const uint64_t T64 = cta_radix_select(in_set, n_items, k, 64, hist, misc + 1, &above);
+    __syncthreads();
+    if (threadIdx.x == 0) misc[0] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n_items; i += kMergeThreads) {
+      uint64_t key = 0;
+      if (in_set(i, &key) && key >= T64) cand[atomicAdd(&misc[0], 1u)] = key;
+    }
+    __syncthreads();
+    nsort = k;
+  }
+  const int n2 = next_pow2(nsort);
+  for (int i = nsort + threadIdx.x; i < n2; i += kMergeThreads) cand[i] = 0ull;
+  cta_bitonic_sort_desc(cand, n2);
+  for (int r = threadIdx.x; r < k; r += kMergeThreads) {
+    const uint64_t key = (r < nsort) ? cand[r] : 0ull;
+    if (key != 0ull) {
+      out_ids[r] = key_id(key);
+      out_lp[r] = key_value(key) - lse;
+    } else {
+      out_ids[r] = -1;
+      out_lp[r] = -INFINITY;
+    }
+  }
+}
+
+cudaError_t merge_setup() { return cudaSuccess; }
+
+cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts, const int32_t* sel,
+                         const int32_t* row_k, float* lse, float* sel_logprob, int32_t* topk_ids,
+                         float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream) {
+  MergeArgs a;
+  a.rows = rows;
+  a.splits = splits;
+  a.V = V;
+  a.k_max = k_max;
+  a.parts = parts;
+  a.sel = sel;
+  a.row_k = row_k;
+  a.lse = lse;
+  a.sel_logprob = sel_logprob;
+  a.topk_ids = topk_ids;
+  a.topk_logprobs = topk_logprobs;
+  a.dev_status = dev_status;
+  merge_partials_kernel<<<rows, kMergeThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace lmh

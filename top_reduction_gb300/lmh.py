@@ -1,0 +1,239 @@
+"""Thin ctypes binding of liblmh (include/lmh.h).
+
+Argument marshalling only: tensors are passed as device pointers and the
+current torch CUDA stream as the launch stream; outputs and the workspace are
+allocated with torch (the caching allocator), and every step of the path runs
+in the library's CUDA kernels.  There is no fallback: if liblmh.so is missing
+or no CUDA device is present, the calls raise.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblmh.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_TIMEOUT = range(6)
+BF16, F16, F32 = 0, 1, 2
+W_VH, W_HV = 0, 1
+PATH_PROJECT, PATH_FROM_LOGITS = 0, 1
+K_MAX = 128
+
+DS_BAD_CU_SEQLENS = 0x1
+DS_SEL_OUT_OF_RANGE = 0x2
+DS_ROWS_OVERFLOW = 0x4
+DS_ROW_IDX_OUT_OF_RANGE = 0x8
+DS_TIMEOUT = 0x10
+
+EXPORTS = ("lmh_select_rows", "lmh_count_selected_rows", "lmh_workspace_bytes",
+           "lmh_project_logprobs", "lmh_logprobs_from_logits", "lmh_status_string",
+           "lmh_version", "lmh_trace_enable", "lmh_trace_read", "lmh_trace_reset")
+
+_lib = None
+
+
+class LMHError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__("%s failed: %s" % (what, status_string(status)))
+
+
+def load():
+    """Load liblmh.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("liblmh.so is not built (%s); run __graft_entry__.build() or "
+                          "python top_reduction_gb300/_build.py" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    lib.lmh_select_rows.argtypes = [P, i32, i32, P, i32, P, P, P, P]
+    lib.lmh_select_rows.restype = ctypes.c_int
+    lib.lmh_count_selected_rows.argtypes = [P, i32, i32, P]
+    lib.lmh_count_selected_rows.restype = i32
+    lib.lmh_workspace_bytes.argtypes = [i32, i32, i32, i32, ctypes.c_int]
+    lib.lmh_workspace_bytes.restype = u64
+    lib.lmh_project_logprobs.argtypes = [P, i64, i32, P, i32, i32, P, ctypes.c_int, i32, P, P, i32,
+                                         P, P, P, P, P, P, u64, P, P]
+    lib.lmh_project_logprobs.restype = ctypes.c_int
+    lib.lmh_logprobs_from_logits.argtypes = [P, ctypes.c_int, i32, i32, i64, P, P, i32, P, P, P, P,
+                                             P, u64, P, P]
+    lib.lmh_logprobs_from_logits.restype = ctypes.c_int
+    lib.lmh_status_string.argtypes = [ctypes.c_int]
+    lib.lmh_status_string.restype = ctypes.c_char_p
+    lib.lmh_version.restype = i32
+    lib.lmh_trace_enable.argtypes = [i32]
+    lib.lmh_trace_enable.restype = ctypes.c_int
+    lib.lmh_trace_read.argtypes = [ctypes.c_char_p, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]
+    lib.lmh_trace_read.restype = ctypes.c_int
+    lib.lmh_trace_reset.restype = None
+    _lib = lib
+    return lib
+
+
+def status_string(status):
+    return load().lmh_status_string(int(status)).decode()
+
+
+def _check(status, what):
+    if status != OK:
+        raise LMHError(status, what)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev_i32(t, device, n=None, name="array"):
+    if t is None:
+        return None
+    t = torch.as_tensor(t, dtype=torch.int32, device=device).contiguous()
+    if n is not None and t.numel() != n:
+        raise ValueError("%s must have %d entries" % (name, n))
+    return t
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+
+def count_selected_rows(cu_seqlens_host, num_decode, all_rows_mask_host=None):
+    """Rows lmh_select_rows will select, from host copies (no device sync)."""
+    cu = torch.as_tensor(cu_seqlens_host, dtype=torch.int32).cpu().contiguous()
+    mask = None
+    if all_rows_mask_host is not None:
+        mask = torch.as_tensor(all_rows_mask_host, dtype=torch.uint8).cpu().contiguous()
+    n = load().lmh_count_selected_rows(ctypes.c_void_p(cu.data_ptr()), cu.numel() - 1, int(num_decode),
+                                       None if mask is None else ctypes.c_void_p(mask.data_ptr()))
+    if n < 0:
+        raise ValueError("invalid packed batch (cu_seqlens / num_decode)")
+    return int(n)
+
+
+def select_rows(cu_seqlens, num_decode, all_rows_mask=None, max_out_rows=None, dev_status=None,
+                stream=None):
+    """Device row selection.  Returns (row_idx int32[max_out_rows], logits_cu_seqlens int32[S+1]).
+
+    Pass max_out_rows (e.g. from count_selected_rows on a host copy) to avoid
+    the device synchronisation needed to read cu_seqlens[-1].
+    """
+    cu = cu_seqlens
+    assert cu.is_cuda and cu.dtype == torch.int32 and cu.is_contiguous()
+    S = cu.numel() - 1
+    if max_out_rows is None:
+        max_out_rows = int(cu[-1].item()) if cu.numel() else 0
+    row_idx = torch.empty(max(int(max_out_rows), 1), dtype=torch.int32, device=cu.device)
+    lcu = torch.empty(S + 1, dtype=torch.int32, device=cu.device)
+    mask = None
+    if all_rows_mask is not None:
+        mask = torch.as_tensor(all_rows_mask, dtype=torch.uint8, device=cu.device).contiguous()
+    _check(load().lmh_select_rows(_p(cu), S, int(num_decode), _p(mask), int(max_out_rows), _p(row_idx),
+                                  _p(lcu), _p(dev_status), _stream(stream)), "lmh_select_rows")
+    return row_idx[:max_out_rows], lcu
+
+
+def workspace_bytes(rows, hidden, vocab, k_max, path):
+    n = load().lmh_workspace_bytes(int(rows), int(hidden), int(vocab), int(k_max), int(path))
+    if n == 0:
+        raise LMHError(ERR_INVALID_ARG, "lmh_workspace_bytes")
+    return int(n)
+
+
+def _outputs(rows, k_max, with_sel, device):
+    out = {"lse": torch.empty(rows, dtype=torch.float32, device=device)}
+    out["sel_logprob"] = torch.empty(rows, dtype=torch.float32, device=device) if with_sel else None
+    out["topk_ids"] = torch.empty((rows, k_max), dtype=torch.int32, device=device)
+    out["topk_logprobs"] = torch.empty((rows, k_max), dtype=torch.float32, device=device)
+    return out
+
+
+def _workspace(workspace, nbytes, device):
+    if workspace is None:
+        return torch.empty(nbytes, dtype=torch.uint8, device=device)
+    assert workspace.numel() * workspace.element_size() >= nbytes
+    return workspace
+
+
+def project_logprobs(hidden, W, row_idx=None, rows=None, sel=None, row_k=None, k_max=0,
+                     logits_out=None, workspace=None, dev_status=None, out=None, stream=None):
+    """Selective head projection + per-row lse / selected logprob / top-k.
+
+    hidden: bf16 [T, H] (rows may be strided); W: bf16 [V, H] (lm_head.weight);
+    row_idx: int32 [rows] device tensor or None (rows 0..rows-1).
+    Returns a dict with lse, sel_logprob (or None), topk_ids, topk_logprobs.
+    """
+    assert hidden.is_cuda and hidden.dtype == torch.bfloat16 and hidden.dim() == 2
+    assert hidden.stride(1) == 1
+    assert W.is_cuda and W.dtype == torch.bfloat16 and W.dim() == 2 and W.is_contiguous()
+    T, H = hidden.shape
+    V = W.shape[0]
+    assert W.shape[1] == H
+    dev = hidden.device
+    if row_idx is not None:
+        rows = row_idx.numel() if rows is None else rows
+        assert row_idx.dtype == torch.int32 and row_idx.is_cuda
+    elif rows is None:
+        rows = T
+    sel_t = _dev_i32(sel, dev, rows, "sel")
+    rk_t = _dev_i32(row_k, dev, rows, "row_k")
+    o = out if out is not None else _outputs(rows, k_max, sel_t is not None, dev)
+    ws = _workspace(workspace, workspace_bytes(rows, H, V, k_max, PATH_PROJECT), dev)
+    st = load().lmh_project_logprobs(
+        _p(hidden), hidden.stride(0) if T > 1 else H, T, _p(row_idx), int(rows), H, _p(W), W_VH, V,
+        _p(sel_t), _p(rk_t), int(k_max), _p(o["lse"]), _p(o["sel_logprob"]), _p(o["topk_ids"]),
+        _p(o["topk_logprobs"]), _p(logits_out), _p(ws), ws.numel() * ws.element_size(), _p(dev_status),
+        _stream(stream))
+    _check(st, "lmh_project_logprobs")
+    return o
+
+
+_DTYPES = {torch.bfloat16: BF16, torch.float16: F16, torch.float32: F32}
+
+
+def logprobs_from_logits(logits, sel=None, row_k=None, k_max=0, workspace=None, dev_status=None,
+                         out=None, stream=None):
+    """Per-row lse / selected logprob / top-k of given logits [rows, V] (bf16, f16 or f32)."""
+    assert logits.is_cuda and logits.dim() == 2 and logits.stride(1) == 1
+    rows, V = logits.shape
+    dev = logits.device
+    sel_t = _dev_i32(sel, dev, rows, "sel")
+    rk_t = _dev_i32(row_k, dev, rows, "row_k")
+    o = out if out is not None else _outputs(rows, k_max, sel_t is not None, dev)
+    ws = _workspace(workspace, workspace_bytes(rows, 0, V, k_max, PATH_FROM_LOGITS), dev)
+    stride = logits.stride(0) if rows > 1 else V
+    st = load().lmh_logprobs_from_logits(
+        _p(logits), _DTYPES[logits.dtype], rows, V, stride, _p(sel_t), _p(rk_t), int(k_max),
+        _p(o["lse"]), _p(o["sel_logprob"]), _p(o["topk_ids"]), _p(o["topk_logprobs"]), _p(ws),
+        ws.numel() * ws.element_size(), _p(dev_status), _stream(stream))
+    _check(st, "lmh_logprobs_from_logits")
+    return o
+
+
+# ---------------------------------------------------------------------------
+# kernel trace
+# ---------------------------------------------------------------------------
+
+TRACE_KERNELS = ("select_rows", "gather_rows", "head_logprobs", "logits_reduce", "merge_partials")
+
+
+def trace_enable(on=True):
+    _check(load().lmh_trace_enable(1 if on else 0), "lmh_trace_enable")
+
+
+def trace_reset():
+    load().lmh_trace_reset()
+
+
+def trace_read(kernel):
+    """(launches, total_ms) of a kernel since the last reset (waits for its events)."""
+    n = ctypes.c_int64(0)
+    ms = ctypes.c_double(0.0)
+    _check(load().lmh_trace_read(kernel.encode(), ctypes.byref(n), ctypes.byref(ms)), "lmh_trace_read")
+    return int(n.value), float(ms.value)
