@@ -119,10 +119,13 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
     __syncthreads();
     for (int i = threadIdx.x; i < n_items; i += kMergeThreads) {
       uint64_t key = 0;
-      if (in_set(i, &key) && key >= T64) cand[atomicAdd(&misc[0], 1u)] = key;
+      if (in_set(i, &key) && key >= T64) {
+        const uint32_t pos = atomicAdd(&misc[0], 1u);  // exactly k of them
+        if (pos < kMergeCap) cand[pos] = key;
+      }
     }
     __syncthreads();
-    nsort = k;
+    nsort = min(k, static_cast<int>(misc[0]));
   }
   const int n2 = next_pow2(nsort);
   for (int i = nsort + threadIdx.x; i < n2; i += kMergeThreads) cand[i] = 0ull;
