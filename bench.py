@@ -1,0 +1,511 @@
+"""Benchmark of the LM-head logprob path: rows/s and the head kernel's roofline.
+
+One step = one pass of the whole hot path over one batch: lmh_select_rows on
+the batch's cu_seqlens, then lmh_project_logprobs on the selected rows (row
+gather, tcgen05 head GEMM with the fused lse / selected-logprob / top-k
+epilogue, partial merge).  The default workload is the decode batch (32 rows,
+H 2560, V 151936, K 5; synthetic seeded inputs, see workloads.py).  The
+2560 x 151936 bf16 head (778 MB) is larger than L2, so every step streams it
+from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode_batch]
+    python bench.py --impl reference ...   # the CPU oracle on the same workload
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its
+own batch (rows are independent: weak scaling, no collective on the data
+path); the value is all ranks' rows over the slowest rank's time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "logprob rows/sec (head+lse+top-K) and % of HBM / bf16 tensor roofline"
+UNIT = "rows/s"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "dram_traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=8000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="decode_batch",
+                   choices=["decode_batch", "decode_batch_k1", "prefill_batch", "prefill_full", "mixed_batch",
+                            "logits_chunk"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=None)
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+def make_workload(name, rank=0):
+    import workloads
+    seed_shift = 1000 * rank  # every rank gets its own batch
+    if name in ("decode_batch", "decode_batch_k1"):
+        b = workloads.decode_batch(seed=1 + seed_shift, k=1 if name.endswith("k1") else 5)
+    elif name in ("prefill_batch", "prefill_full"):
+        b = workloads.prefill_batch(seed=2 + seed_shift)
+        if name == "prefill_full":  # every packed row through the head (the materializing 'before' arm)
+            b = dict(b, name="prefill_full", num_decode=0, all_rows_mask=None,
+                     full=True, n_sel=b["hidden"].shape[0], sel=b["sel_all"])
+    elif name == "mixed_batch":
+        b = workloads.mixed_batch(seed=4 + seed_shift)
+    else:
+        b = workloads.logits_chunk("normal", seed=3 + seed_shift)
+        b["k"] = 20
+    return b
+
+
+def workload_config(b):
+    if b["name"] == "logits_chunk":
+        return {"workload": "logits_chunk", "rows": b["rows"], "V": b["V"], "k": b["k"], "dtype_in": "bf16",
+                "l2": "inputs larger than L2 (a 127 MB chunk; 4 chunks rotated)"}
+    return {"workload": b["name"], "rows": int(b["n_sel"]), "tokens": int(b["hidden"].shape[0]),
+            "H": int(b["H"]), "V": int(b["V"]), "k": int(b["k"]),
+            "l2": "inputs larger than L2 (the %.0f MB head is streamed from HBM every step)"
+                  % (b["V"] * b["H"] * 2 / 1e6)}
+
+
+def algorithmic(b):
+    """(bound, per-launch algorithmic amount, unit, peak key) of the dominant kernel."""
+    if b["name"] == "logits_chunk":
+        return "hbm", b["rows"] * b["V"] * 2 + b["rows"] * (2 + 2 * b["k"]) * 4, "GB/s"
+    rows, H, V = int(b["n_sel"]), int(b["H"]), int(b["V"])
+    if rows >= 256:  # the projection is tensor-bound from a few hundred rows on
+        return "tensor", 2.0 * rows * H * V, "TFLOP/s"
+    return "hbm", V * H * 2 + rows * H * 2, "GB/s"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, smax, reasons, power = [], None, set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def rejected(clocks):
+    if not clocks:
+        return False
+    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+    if bad & set(clocks["reasons"]):
+        return True
+    return clocks["sm_max_mhz"] and clocks["sm_mhz"] < 0.5 * clocks["sm_max_mhz"] and not clocks["reasons"]
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+class Step:
+    """Device-resident inputs, preallocated outputs/workspace and one step of the path."""
+
+    def __init__(self, lmh, b, device):
+        import torch
+        self.lmh, self.b, self.dev = lmh, b, device
+        self.chunk = b["name"] == "logits_chunk"
+        if self.chunk:
+            # rotate 4 copies so consecutive steps do not hit in L2 (a chunk is about the size of L2)
+            self.logits = [b["logits"].to(device) for _ in range(4)]
+            self.sel = b["sel"].to(device)
+            self.k = b["k"]
+            self.rows = b["rows"]
+            self.ws = torch.empty(lmh.workspace_bytes(self.rows, 0, b["V"], self.k, lmh.PATH_FROM_LOGITS),
+                                  dtype=torch.uint8, device=device)
+            self.out = self._outputs(self.rows, self.k, True)
+            self.i = 0
+            return
+        self.full = b.get("full", False)
+        self.hidden = b["hidden"].to(device)
+        self.W = b["W"].to(device)
+        self.cu = b["cu_seqlens"].to(device)
+        self.mask = None if b["all_rows_mask"] is None else b["all_rows_mask"].to(device)
+        self.sel = b["sel"].to(device)
+        self.row_k = None if b["row_k"] is None else b["row_k"].to(device)
+        self.k = int(b["k"])
+        self.rows = int(b["n_sel"])
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.ws = torch.empty(lmh.workspace_bytes(self.rows, b["H"], b["V"], self.k, lmh.PATH_PROJECT),
+                              dtype=torch.uint8, device=device)
+        self.out = self._outputs(self.rows, self.k, True)
+
+    def _outputs(self, rows, k, with_sel):
+        import torch
+        d = self.dev
+        return {"lse": torch.empty(rows, dtype=torch.float32, device=d),
+                "sel_logprob": torch.empty(rows, dtype=torch.float32, device=d) if with_sel else None,
+                "topk_ids": torch.empty((rows, k), dtype=torch.int32, device=d),
+                "topk_logprobs": torch.empty((rows, k), dtype=torch.float32, device=d)}
+
+    def launches_per_step(self):
+        if self.chunk:
+            return 2
+        return 2 if self.full else 4
+
+    def run(self):
+        lmh = self.lmh
+        if self.chunk:
+            x = self.logits[self.i & 3]
+            self.i += 1
+            return lmh.logprobs_from_logits(x, sel=self.sel, k_max=self.k, workspace=self.ws, out=self.out)
+        if self.full:
+            return lmh.project_logprobs(self.hidden, self.W, sel=self.sel, row_k=self.row_k, k_max=self.k,
+                                        workspace=self.ws, out=self.out, dev_status=self.status)
+        ri, _ = lmh.select_rows(self.cu, self.b["num_decode"], self.mask, max_out_rows=self.rows,
+                                dev_status=self.status)
+        return lmh.project_logprobs(self.hidden, self.W, row_idx=ri, sel=self.sel, row_k=self.row_k,
+                                    k_max=self.k, workspace=self.ws, out=self.out, dev_status=self.status)
+
+
+def timed_region(step, steps, dist, world):
+    import torch
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        step.run()
+    stop.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(stop)
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms
+
+
+def e2e_leg(lmh, b, device, steps):
+    """Same metric through the public API with inputs in pinned host memory.
+
+    Every step copies its inputs host->device (hidden rows, cu_seqlens,
+    selected ids; the head weight stays resident like model weights), runs
+    the path, copies the compact result device->host and waits for it.
+    """
+    import torch
+    if b["name"] == "logits_chunk":
+        h_in = {"logits": b["logits"].pin_memory(), "sel": b["sel"].pin_memory()}
+    else:
+        h_in = {"hidden": b["hidden"].pin_memory(), "cu": b["cu_seqlens"].pin_memory(),
+                "sel": b["sel"].pin_memory()}
+        W = b["W"].to(device)
+        mask = None if b["all_rows_mask"] is None else b["all_rows_mask"].to(device)
+        row_k = None if b["row_k"] is None else b["row_k"].to(device)
+    d_in = {k: torch.empty_like(v, device=device) for k, v in h_in.items()}
+    rows = b["rows"] if b["name"] == "logits_chunk" else int(b["n_sel"])
+    k = int(b["k"])
+    h_out = {"lse": torch.empty(rows, dtype=torch.float32).pin_memory(),
+             "sel_logprob": torch.empty(rows, dtype=torch.float32).pin_memory(),
+             "topk_ids": torch.empty((rows, k), dtype=torch.int32).pin_memory(),
+             "topk_logprobs": torch.empty((rows, k), dtype=torch.float32).pin_memory()}
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+
+    def one():
+        for key, v in h_in.items():
+            d_in[key].copy_(v, non_blocking=True)
+        if b["name"] == "logits_chunk":
+            o = lmh.logprobs_from_logits(d_in["logits"], sel=d_in["sel"], k_max=k)
+        else:
+            ri, _ = lmh.select_rows(d_in["cu"], b["num_decode"], mask, max_out_rows=rows)
+            o = lmh.project_logprobs(d_in["hidden"], W, row_idx=ri, sel=d_in["sel"], row_k=row_k, k_max=k)
+        for key, v in h_out.items():
+            v.copy_(o[key], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(5):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = time.perf_counter() - t0
+    return {"value": rows * steps / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": 1e3 * dt / steps}
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_hash(kernel):
+    src = {"head_logprobs": "head_gemm.cu", "logits_reduce": "logits_reduce.cu"}[kernel]
+    h = hashlib.sha256()
+    for name in (src, "device_common.cuh"):
+        with open(os.path.join(ROOT, "top_reduction_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu capture, if the kernel is unchanged since."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    r = rec.get("%s/%s" % (kernel, workload))
+    if not r or r.get("source_sha256_16") != kernel_source_hash(kernel):
+        return None
+    return r.get("dram_bytes_per_launch")
+
+
+class OracleStep:
+    """One step of the oracle, as it stands, on the same workload.
+
+    A step is one batch of selected rows (as many as there are host cores, so
+    the oracle's threads are all busy): row selection, f64 projection and the
+    full-vocabulary f64 log-softmax + full sort.  Rows cycle through the
+    workload's selected rows.
+    """
+
+    def __init__(self, b):
+        import numpy as np
+        import oracle
+        import workloads
+        self.oracle, self.b = oracle, b
+        self.cores = oracle.cores()
+        if b["name"] == "logits_chunk":
+            self.x = workloads.bits(b["logits"])
+            self.n = b["rows"]
+        else:
+            mask = None if b["all_rows_mask"] is None else b["all_rows_mask"].numpy()
+            self.ri, _ = oracle.select_rows(b["cu_seqlens"].numpy(), b["num_decode"], mask)
+            if b.get("full"):
+                self.ri = np.arange(b["hidden"].shape[0], dtype=np.int32)
+            self.hid, self.W = workloads.bits(b["hidden"]), workloads.bits(b["W"])
+            self.n = len(self.ri)
+        self.per = max(1, min(self.n, self.cores))
+        self.pos = 0
+        self.threads = self.cores
+
+    def run(self):
+        import numpy as np
+        b, o = self.b, self.oracle
+        idx = (self.pos + np.arange(self.per)) % self.n
+        self.pos = (self.pos + self.per) % self.n
+        sel = b["sel"].numpy()[idx]
+        if b["name"] == "logits_chunk":
+            r = o.logprobs(self.x[idx], dtype=o.BF16, sel=sel, k_max=b["k"], return_threads=True)
+            self.threads = r["threads"]
+        else:
+            rk = None if b["row_k"] is None else b["row_k"].numpy()[idx]
+            z, self.threads = o.project(self.hid, self.W, row_idx=self.ri[idx], return_threads=True)
+            o.logprobs(z, sel=sel, row_k=rk, k_max=b["k"])
+        return self.per
+
+    def describe(self):
+        what = ("rows of the logits chunk (full-vocabulary f64 log-softmax + full sort)"
+                if self.b["name"] == "logits_chunk" else
+                "selected rows (row selection + f64 projection + full-vocabulary f64 log-softmax + full sort)")
+        return "%d %s of %s per step" % (self.per, what, self.b["name"])
+
+
+def cpu_baseline(b, budget_s=12.0):
+    """The oracle on a bounded sample of the workload (about budget_s seconds of work)."""
+    st = OracleStep(b)
+    t0 = time.perf_counter()
+    rows, steps = 0, 0
+    while steps == 0 or time.perf_counter() - t0 < budget_s:
+        rows += st.run()
+        steps += 1
+    dt = time.perf_counter() - t0
+    return {"value": rows / dt, "unit": UNIT, "cores": int(st.threads), "kind": "oracle",
+            "sample": "%d steps of %s (%.1f s)" % (steps, st.describe(), dt)}
+
+
+def run_ours(args):
+    import torch
+    import top_reduction_gb300 as lmh
+    from top_reduction_gb300 import _build
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    _build.build()
+    b = make_workload(args.workload, rank)
+    step = Step(lmh, b, device)
+    for _ in range(max(args.warmup, 3)):
+        step.run()
+    torch.cuda.synchronize()
+
+    bound, amount, unit = algorithmic(b)
+    kernel = "logits_reduce" if step.chunk else "head_logprobs"
+    result = None
+    for attempt in range(2):
+        lmh.trace_reset()
+        lmh.trace_enable(True)
+        with ClockSampler(local) as cs:
+            ms = timed_region(step, args.steps, dist, world)
+        lmh.trace_enable(False)
+        clocks = cs.summary()
+        launches, kms = 0, 0.0
+        per_kernel = {}
+        for kname in lmh.lmh.TRACE_KERNELS:
+            n, t = lmh.trace_read(kname)
+            launches += n
+            if n:
+                per_kernel[kname] = {"launches": n, "avg_us": 1e3 * t / n}
+        result = (ms, clocks, launches, per_kernel)
+        if not rejected(clocks):
+            break
+    ms, clocks, launches, per_kernel = result
+    status = int(step.status.item()) if hasattr(step, "status") else 0
+    if status:
+        raise RuntimeError("device status %#x during the benchmark" % status)
+
+    rows_total = step.rows * args.steps * world
+    value = rows_total / (ms / 1e3)
+    peaks, peak_src = load_peaks()
+    avg_us = per_kernel.get(kernel, {}).get("avg_us")
+    if bound == "hbm":
+        peak = peaks["hbm_gbs"]
+        achieved = amount / (avg_us * 1e-6) / 1e9 if avg_us else None
+    else:
+        peak = peaks["bf16_tflops_sustained" if args.steps * (avg_us or 0) > 1e6 else "bf16_tflops"]
+        achieved = amount / (avg_us * 1e-6) / 1e12 if avg_us else None
+    roof = {"kernel": kernel, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": (achieved / peak) if achieved else None, "peak_source": peak_src,
+            "algorithmic_per_launch": amount, "avg_launch_us": avg_us,
+            "traffic": recorded_traffic(kernel, b["name"])}
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(b), "roofline": roof, "kernels": per_kernel,
+            "gpu_launches": launches, "clocks": clocks}
+    if rank == 0:
+        line["e2e"] = e2e_leg(lmh, b, device, args.e2e_steps or max(200, min(args.steps, 2000)))
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(b)
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The CPU oracle, as it stands, on our arm's workload and metric, on the host cores.
+
+    W warm-up steps, then up to K timed steps; the run stops early once its
+    time budget is spent (the line says how many steps ran).
+    """
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    b = make_workload(args.workload)
+    st = OracleStep(b)
+    budget = 150.0
+    for _ in range(min(args.warmup, 1)):
+        st.run()
+    t0 = time.perf_counter()
+    rows, steps = 0, 0
+    while steps < args.steps and (steps == 0 or time.perf_counter() - t0 < budget):
+        rows += st.run()
+        steps += 1
+    dt = time.perf_counter() - t0
+    value = rows / dt
+    sample = "%d of %d requested steps within a %.0f s budget; %s" % (steps, args.steps, budget, st.describe())
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(b),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": int(st.threads), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -188,9 +188,10 @@ lmh_status lmh_project_logprobs(const void* hidden, int64_t hidden_row_stride, i
  * survivors and the scored token; exact ties by ascending id) and openinfer
  * issue #719 (reusable for decode rows and batches of prompt positions).
  *
- *   logits            device [rows x V] of dtype, row stride row_stride (>= V);
- *                     base 16-byte aligned and row_stride * sizeof(dtype) a
- *                     multiple of 16.
+ *   logits            device [rows x V] of dtype, row stride row_stride (>= V),
+ *                     base aligned to sizeof(dtype).  Rows whose start is
+ *                     16-byte aligned are staged with one bulk copy, others
+ *                     with plain loads.
  *   sel_ids, row_k, k_max, lse, sel_logprob, topk_ids, topk_logprobs:
  *                     as for lmh_project_logprobs (logit = the given value
  *                     widened exactly to fp32).

@@ -128,8 +128,8 @@ def test_from_logits_argument_checks(lib):
     assert call(logits=0) == lmh.ERR_INVALID_ARG
     assert call(k_max=200) == lmh.ERR_UNSUPPORTED
     assert call(k_max=300, V=256) == lmh.ERR_UNSUPPORTED
-    assert call(logits=0x1002) == lmh.ERR_UNSUPPORTED                # not 16-byte aligned
-    assert call(stride=260) == lmh.ERR_UNSUPPORTED                   # 520-byte pitch
+    assert call(logits=0x1001) == lmh.ERR_UNSUPPORTED                # not element aligned
+    assert call(logits=0x1002, dtype=2) == lmh.ERR_UNSUPPORTED       # fp32 on a 2-byte boundary
     assert call(rows=0) == lmh.OK
 
 

@@ -265,7 +265,7 @@ lmh_status lmh_logprobs_from_logits(const void* logits, lmh_dtype dtype, int32_t
   if (!logits || !lse || (sel_ids && !sel_logprob) || (k_max > 0 && (!topk_ids || !topk_logprobs)))
     return LMH_ERR_INVALID_ARG;
   const int64_t elem = dtype == LMH_F32 ? 4 : 2;
-  if (!aligned(logits, 16) || ((row_stride * elem) % 16) != 0) return LMH_ERR_UNSUPPORTED;
+  if (!aligned(logits, static_cast<size_t>(elem))) return LMH_ERR_UNSUPPORTED;
   if (rows == 0) return LMH_OK;
   int sms = 0;
   if (device_setup(&sms) != cudaSuccess) return LMH_ERR_CUDA;

@@ -129,29 +129,38 @@ __global__ void __launch_bounds__(kReduceThreads) logits_reduce_kernel(const Red
   const uint32_t bytes = static_cast<uint32_t>(ne) * sizeof(T);
   const uint32_t bulk = bytes & ~15u;
 
+  // rows whose start is 16-byte aligned arrive by one bulk copy; any other
+  // row pitch is copied by the whole CTA with plain element loads
+  const bool use_bulk = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
   if (threadIdx.x == 0) {
     mbar_init(bar, 1);
     mbar_init_fence();
     misc[0] = 0;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    if (bulk > 0) {
-      mbar_arrive_expect_tx(bar, bulk);
-      bulk_load(chunk, src, bulk, bar);
-    } else {
-      mbar_arrive(bar);
+  if (use_bulk) {
+    if (threadIdx.x == 0) {
+      if (bulk > 0) {
+        mbar_arrive_expect_tx(bar, bulk);
+        bulk_load(chunk, src, bulk, bar);
+      } else {
+        mbar_arrive(bar);
+      }
+      // ragged tail (< 16 bytes) with plain loads
+      for (uint32_t o = bulk; o < bytes; o += sizeof(T))
+        *reinterpret_cast<T*>(reinterpret_cast<char*>(chunk) + o) = *reinterpret_cast<const T*>(src + o);
     }
-    // ragged tail (< 16 bytes) with plain loads
-    for (uint32_t o = bulk; o < bytes; o += sizeof(T))
-      *reinterpret_cast<T*>(reinterpret_cast<char*>(chunk) + o) = *reinterpret_cast<const T*>(src + o);
+  } else {
+    if (threadIdx.x == 0) mbar_arrive(bar);
+    const T* s = reinterpret_cast<const T*>(src);
+    for (int i = threadIdx.x; i < ne; i += kReduceThreads) chunk[i] = s[i];
   }
   const bool ok = mbar_wait(bar, 0);
   if (!ok) {
     if (threadIdx.x == 0) set_status(a.dev_status, LMH_DS_TIMEOUT);
     return;
   }
-  __syncthreads();  // the tail written by thread 0
+  __syncthreads();  // the plain-load parts
 
   // ---- pass A: block maxima and the chunk maximum ----
   const int nvec = nb * VPB;
