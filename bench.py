@@ -47,6 +47,7 @@ def parse_args():
                             "logits_chunk"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     return p.parse_args()
 
 
@@ -457,7 +458,8 @@ def run_ours(args):
             "config": workload_config(b), "roofline": roof, "kernels": per_kernel,
             "gpu_launches": launches, "clocks": clocks}
     if rank == 0:
-        line["e2e"] = e2e_leg(lmh, b, device, args.e2e_steps or max(200, min(args.steps, 2000)))
+        if not args.no_e2e:
+            line["e2e"] = e2e_leg(lmh, b, device, args.e2e_steps or max(200, min(args.steps, 2000)))
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(b)
         print(json.dumps(line), flush=True)
