@@ -208,6 +208,41 @@ lmh_status lmh_logprobs_from_logits(const void* logits, lmh_dtype dtype, int32_t
                                     void* workspace, size_t workspace_bytes, uint32_t* dev_status,
                                     cudaStream_t stream);
 
+/*
+ * lmh_logprobs_from_logits_static -- lmh_logprobs_from_logits without a
+ * caller workspace.
+ *
+ * The pages have no counterpart for this entry point.  It serves callers
+ * that cannot allocate device memory when they need the reduction:
+ * - an engine that gave all free HBM to its KV-cache pool at start-up;
+ * - plain C code without access to the framework's allocator;
+ * - a latency-critical loop where cudaMalloc/cudaFree would synchronise the
+ *   device.
+ * It runs the same kernels and returns the same results as
+ * lmh_logprobs_from_logits. Instead of a caller workspace, it keeps its
+ * partials in a fixed 8 MiB array in the library's own device memory, which
+ * every GPU that loads the library holds until the process exits.  The call
+ * allocates nothing.
+ *
+ * Arguments, results and errors are those of lmh_logprobs_from_logits,
+ * minus workspace/workspace_bytes, with two differences:
+ * - sizes whose partials need more than the 8 MiB are rejected with
+ *   LMH_ERR_WORKSPACE_TOO_SMALL, and nothing is launched.  For example,
+ *   256 rows x 248320 at k_max 128 needs about 4.2 MB and fits.
+ * - the first call on each device does a one-time set-up with that device
+ *   current: kernel attributes, and the array's device address via
+ *   cudaGetSymbolAddress.  Make that first call before any stream capture.
+ * Every call shares the one array, which keeps the previous call's contents.
+ * Nothing in it needs to start at zero, but calls that overlap on the GPU
+ * race on it: serialise them, on one stream or with events.
+ */
+lmh_status lmh_logprobs_from_logits_static(const void* logits, lmh_dtype dtype, int32_t rows,
+                                           int32_t V, int64_t row_stride, const int32_t* sel_ids,
+                                           const int32_t* row_k, int32_t k_max, float* lse,
+                                           float* sel_logprob, int32_t* topk_ids,
+                                           float* topk_logprobs, uint32_t* dev_status,
+                                           cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* lmh_status_string(lmh_status status);
 
