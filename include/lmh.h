@@ -228,7 +228,7 @@ lmh_status lmh_logprobs_from_logits(const void* logits, lmh_dtype dtype, int32_t
  * minus workspace/workspace_bytes, with two differences:
  * - sizes whose partials need more than the 8 MiB are rejected with
  *   LMH_ERR_WORKSPACE_TOO_SMALL, and nothing is launched.  For example,
- *   256 rows x 248320 at k_max 128 needs about 4.2 MB and fits.
+ *   256 rows x 248320 at k_max 128 needs about 0.8 MB and fits.
  * - the first call on each device does a one-time set-up with that device
  *   current: kernel attributes, and the array's device address via
  *   cudaGetSymbolAddress.  Make that first call before any stream capture.

@@ -46,10 +46,16 @@ constexpr int kTmemCols = 512;
 constexpr uint32_t kStageBytesA = kBM * kBK * 2;  // 16 KB
 constexpr uint32_t kStageBytesB = kBN * kBK * 2;  // 32 KB
 
+// KCAP: per-row candidate capacity.  KCAP <= 32 keeps each row's top-k list
+// in registers and uses the shared region to stage candidate blocks (4 warps x
+// 64 columns x 32 lanes x 4 bytes); KCAP 128 keeps the lists themselves in
+// shared memory (slot-major) and has room for only 2 pipeline stages.
 template <int KCAP>
 struct HeadCfg {
-  static constexpr int kStages = KCAP <= 32 ? 4 : 2;
-  static constexpr size_t kListBytes = static_cast<size_t>(kBM) * KCAP * 8;
+  static constexpr bool kRegList = KCAP <= 32;
+  static constexpr int kStages = kRegList ? 4 : 2;
+  static constexpr size_t kListBytes = kRegList ? static_cast<size_t>(4) * 64 * 32 * 4
+                                                : static_cast<size_t>(kBM) * KCAP * 8;
   static constexpr size_t kSmem = 1024 /*alignment slack*/ + kStages * (kStageBytesA + kStageBytesB) +
                                   kListBytes + (2 * kStages + 4) * 8 + 16;
 };
@@ -181,6 +187,46 @@ __device__ __noinline__ ListState list_insert(uint64_t* list, int r, ListState s
   st.tau = (st.cnt == k) ? key_value(list[(k - 1) * kBM + r]) : -INFINITY;
   return st;
 }
+
+// ---------------------------------------------------------------------------
+// per-row top-k list in registers (KCAP <= 32)
+// ---------------------------------------------------------------------------
+// L[0..k) holds the row's best keys sorted descending (0 = empty); slots
+// k..KC stay empty.  Insertion is a branchless compare-exchange sweep over the
+// first k slots: the new key settles at its rank and the smallest falls off.
+// tau is the value of the k-th key once k keys are held (else -inf): only
+// entries strictly above tau can still rank, because ids ascend within a
+// CTA's vocabulary range.  Slot k-1 is picked up during the sweep with a
+// predicated select (a plain select by a runtime index would move L to
+// local memory).
+template <int KC>
+struct RegTopK {
+  uint64_t L[KC];
+  float tau;
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int i = 0; i < KC; ++i) L[i] = 0ull;
+    tau = -INFINITY;
+  }
+
+  __device__ __forceinline__ void insert(uint64_t x, int k) {
+    uint64_t kth = 0ull;
+#pragma unroll
+    for (int i = 0; i < KC; ++i) {
+      const bool gt = (i < k) && x > L[i];
+      const uint64_t lo = gt ? L[i] : x;
+      L[i] = gt ? x : L[i];
+      x = lo;
+      // kth = (i == k - 1) ? L[i] : kth, as a predicated select the compiler
+      // cannot turn into a load from a runtime index
+      asm("{\n\t.reg .pred p;\n\tsetp.eq.s32 p, %2, %3;\n\tselp.b64 %0, %1, %0, p;\n\t}"
+          : "+l"(kth)
+          : "l"(L[i]), "r"(i), "r"(k - 1));
+    }
+    tau = kth ? key_value(kth) : -INFINITY;
+  }
+};
 
 // ---------------------------------------------------------------------------
 // the fused kernel
@@ -317,9 +363,11 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
       }
       float m = -INFINITY, ssum = 0.0f, sel_val = 0.0f;
       bool has_sel = false;
-      ListState st;
+      ListState st;  // shared-memory list (KCAP 128)
       st.tau = -INFINITY;
       st.cnt = 0;
+      RegTopK<Cfg::kRegList ? KCAP : 1> rt;  // register list (KCAP <= 32)
+      rt.reset();
       for (int n = n_begin; n < n_end; ++n, ++t) {
         const uint32_t b = t & 1u, aph = (t >> 1) & 1u;
         if (!wait_or_abort(&acc_full[b], aph, abort_flag, a.dev_status)) {
@@ -342,6 +390,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
               for (int j = 0; j < kBlock; ++j)
                 if (j >= nvalid) v[j] = -INFINITY;
             }
+            const unsigned valid_mask = __ballot_sync(0xffffffffu, valid);  // whole warp converged here
             if (!valid) continue;
             if (kMaterialize) {
               float* dst = a.logits_out + static_cast<int64_t>(row) * a.V + col0;
@@ -378,10 +427,36 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
               sel_val = sv;
               has_sel = true;
             }
-            if (k_row > 0 && bm > st.tau) {
+            if constexpr (Cfg::kRegList) {
+              // Stage the block for the lanes that have candidates; each lane then walks only its
+              // own candidate mask, so the warp pays the largest per-lane count, not their union.
+              const bool want = k_row > 0 && bm > rt.tau;
+              if (__any_sync(valid_mask, want)) {
+                float* stg = reinterpret_cast<float*>(lists) + q * (kBlock * 32);
+                uint32_t mlo = 0, mhi = 0;
 #pragma unroll
-              for (int j = 0; j < kBlock; ++j)
-                if (v[j] > st.tau) st = list_insert(lists, r_local, st, k_row, make_key(v[j], col0 + j));
+                for (int j = 0; j < 32; ++j) {
+                  stg[j * 32 + lane] = v[j];
+                  stg[(j + 32) * 32 + lane] = v[j + 32];
+                  mlo |= (v[j] > rt.tau ? 1u : 0u) << j;
+                  mhi |= (v[j + 32] > rt.tau ? 1u : 0u) << j;
+                }
+                __syncwarp(valid_mask);
+                uint64_t cm = want ? ((static_cast<uint64_t>(mhi) << 32) | mlo) : 0ull;
+                while (cm) {
+                  const int j = __ffsll(static_cast<long long>(cm)) - 1;
+                  cm &= cm - 1;
+                  const float x = stg[j * 32 + lane];
+                  if (x > rt.tau) rt.insert(make_key(x, col0 + j), k_row);
+                }
+                __syncwarp(valid_mask);
+              }
+            } else {
+              if (k_row > 0 && bm > st.tau) {
+#pragma unroll
+                for (int j = 0; j < kBlock; ++j)
+                  if (v[j] > st.tau) st = list_insert(lists, r_local, st, k_row, make_key(v[j], col0 + j));
+              }
             }
           }
         }
@@ -393,7 +468,13 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         const int64_t pidx = static_cast<int64_t>(row) * a.splits + split;
         a.parts.part_ms[pidx] = make_float2(m, ssum);
         unsigned long long* out = a.parts.part_keys + pidx * a.k_max;
-        for (int j = 0; j < k_row; ++j) out[j] = (j < st.cnt) ? lists[j * kBM + r_local] : 0ull;
+        if constexpr (Cfg::kRegList) {
+#pragma unroll
+          for (int j = 0; j < (Cfg::kRegList ? KCAP : 1); ++j)
+            if (j < k_row) out[j] = rt.L[j];
+        } else {
+          for (int j = 0; j < k_row; ++j) out[j] = (j < st.cnt) ? lists[j * kBM + r_local] : 0ull;
+        }
         if (has_sel) a.parts.sel_logit[row] = sel_val;
       }
     }
@@ -447,7 +528,7 @@ HeadPlan head_plan(int rows, int H, int V, int k_max, int num_sms) {
   HeadPlan p;
   p.m_tiles = (rows + kBM - 1) / kBM;
   p.n_tiles = (V + kBN - 1) / kBN;
-  p.kcap = k_max <= 32 ? 32 : 128;
+  p.kcap = k_max <= 4 ? 4 : k_max <= 8 ? 8 : k_max <= 16 ? 16 : k_max <= 24 ? 24 : k_max <= 32 ? 32 : 128;
   const int G = num_sms > 0 ? num_sms : 1;
   // choose the vocabulary split that minimises the busiest CTA's tile count
   // (plus a small cost per unit for its flush and pipeline refill)
@@ -509,10 +590,17 @@ static cudaError_t set_head_attr() {
 }
 
 cudaError_t head_setup() {
-  cudaError_t e = set_head_attr<32, false>();
-  if (e == cudaSuccess) e = set_head_attr<32, true>();
-  if (e == cudaSuccess) e = set_head_attr<128, false>();
-  if (e == cudaSuccess) e = set_head_attr<128, true>();
+  cudaError_t e = cudaSuccess;
+#define LMH_HEAD_ATTR(KC)                                            \
+  if (e == cudaSuccess) e = set_head_attr<KC, false>();              \
+  if (e == cudaSuccess) e = set_head_attr<KC, true>();
+  LMH_HEAD_ATTR(4)
+  LMH_HEAD_ATTR(8)
+  LMH_HEAD_ATTR(16)
+  LMH_HEAD_ATTR(24)
+  LMH_HEAD_ATTR(32)
+  LMH_HEAD_ATTR(128)
+#undef LMH_HEAD_ATTR
   return e;
 }
 
@@ -541,16 +629,23 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   a.logits_out = logits_out;
   a.dev_status = dev_status;
   const dim3 grid(plan.grid), block(kHeadThreads);
-  if (plan.kcap == 32) {
-    if (logits_out)
-      head_logprobs_kernel<32, true><<<grid, block, HeadCfg<32>::kSmem, stream>>>(ta, tb, a);
-    else
-      head_logprobs_kernel<32, false><<<grid, block, HeadCfg<32>::kSmem, stream>>>(ta, tb, a);
-  } else {
-    if (logits_out)
-      head_logprobs_kernel<128, true><<<grid, block, HeadCfg<128>::kSmem, stream>>>(ta, tb, a);
-    else
-      head_logprobs_kernel<128, false><<<grid, block, HeadCfg<128>::kSmem, stream>>>(ta, tb, a);
+  switch (plan.kcap) {
+#define LMH_HEAD_CASE(KC)                                                                     \
+  case KC:                                                                                    \
+    if (logits_out)                                                                           \
+      head_logprobs_kernel<KC, true><<<grid, block, HeadCfg<KC>::kSmem, stream>>>(ta, tb, a);  \
+    else                                                                                      \
+      head_logprobs_kernel<KC, false><<<grid, block, HeadCfg<KC>::kSmem, stream>>>(ta, tb, a); \
+    break;
+    LMH_HEAD_CASE(4)
+    LMH_HEAD_CASE(8)
+    LMH_HEAD_CASE(16)
+    LMH_HEAD_CASE(24)
+    LMH_HEAD_CASE(32)
+    LMH_HEAD_CASE(128)
+#undef LMH_HEAD_CASE
+    default:
+      return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
 }

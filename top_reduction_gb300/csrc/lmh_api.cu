@@ -198,7 +198,7 @@ size_t lmh_workspace_bytes(int32_t rows, int32_t hidden, int32_t vocab, int32_t 
            partials_bytes(rows, p.splits, k_max);
   }
   if (path == LMH_PATH_FROM_LOGITS) {
-    const VocabSplit vs = logits_reduce_split(rows, vocab, sms);
+    const VocabSplit vs = logits_reduce_split(rows, vocab, k_max, sms);
     return partials_bytes(rows, vs.splits, k_max);
   }
   return 0;
@@ -269,7 +269,7 @@ lmh_status lmh_logprobs_from_logits(const void* logits, lmh_dtype dtype, int32_t
   if (rows == 0) return LMH_OK;
   int sms = 0;
   if (device_setup(&sms) != cudaSuccess) return LMH_ERR_CUDA;
-  const VocabSplit vs = logits_reduce_split(rows, V, sms);
+  const VocabSplit vs = logits_reduce_split(rows, V, k_max, sms);
   if (static_cast<int64_t>(rows) * vs.splits > INT32_MAX) return LMH_ERR_UNSUPPORTED;
   const size_t need = partials_bytes(rows, vs.splits, k_max);
   if (!workspace || !aligned(workspace, 256)) return LMH_ERR_INVALID_ARG;
@@ -284,7 +284,7 @@ lmh_status lmh_logprobs_from_logits(const void* logits, lmh_dtype dtype, int32_t
   if (e == cudaSuccess) {
     Traced tr(kTraceMerge, stream);
     e = launch_merge(rows, vs.splits, V, k_max, parts, sel_ids, row_k, lse, sel_logprob, topk_ids, topk_logprobs,
-                     dev_status, stream);
+                     dev_status, stream, vs.per, vs.nblk);
   }
   return from_cuda(e);
 }

@@ -13,10 +13,16 @@ namespace lmh {
 
 constexpr int kBlock = 64;  // logits per prefilter block (MTPLX PR #532, "Change")
 
-// Split of one row's vocabulary into per-CTA chunks of whole 64-blocks.
+// Work split of the standalone reduction: the flattened (row, 64-block) space
+// is cut into n_ranges equal ranges of `per` blocks; a row meets at most
+// `splits` ranges, which is the number of partial slots per row.  The ranges
+// a row meets are [(row*nblk)/per, (row*nblk + nblk - 1)/per].
 struct VocabSplit {
-  int splits;            // chunks per row
-  int blocks_per_split;  // 64-blocks per chunk (the last chunk may have fewer)
+  int splits;    // partial slots per row
+  int per;       // 64-blocks per range
+  int n_ranges;  // ranges in total
+  int grid;      // persistent CTAs
+  int nblk;      // 64-blocks per row
 };
 
 // Per-(row, split) partial results, laid out in the caller's workspace:
@@ -37,7 +43,7 @@ cudaError_t logits_reduce_setup();
 cudaError_t merge_setup();
 cudaError_t head_setup();
 
-VocabSplit logits_reduce_split(int rows, int V, int num_sms);
+VocabSplit logits_reduce_split(int rows, int V, int k_max, int num_sms);
 
 cudaError_t launch_select_rows(const int32_t* cu, int num_seqs, int num_decode, const uint8_t* mask,
                                int max_out, int32_t* row_idx, int32_t* logits_cu, uint32_t* dev_status,
@@ -47,9 +53,13 @@ cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t ro
                                  VocabSplit split, const int32_t* sel, const int32_t* row_k, int k_max,
                                  Partials parts, uint32_t* dev_status, cudaStream_t stream);
 
+// Merges the partial slots of every row.  flat_per == 0: every one of the
+// `splits` slots is filled (head path); flat_per > 0: row r fills the slots of
+// the ranges it meets in a VocabSplit with per = flat_per, nblk = flat_nblk.
 cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts, const int32_t* sel,
                          const int32_t* row_k, float* lse, float* sel_logprob, int32_t* topk_ids,
-                         float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream);
+                         float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream, int flat_per = 0,
+                         int flat_nblk = 0);
 
 // ---- head projection (head_gemm.cu) ----
 
@@ -60,7 +70,7 @@ struct HeadPlan {
   int splits;           // vocabulary ranges per row (units = m_tiles * splits)
   int tiles_per_split;  // n-tiles per range
   int grid;             // persistent CTAs
-  int kcap;             // per-row candidate capacity variant (32 or 128)
+  int kcap;             // per-row candidate capacity variant (4, 8, 16, 24, 32 or 128)
 };
 
 HeadPlan head_plan(int rows, int H, int V, int k_max, int num_sms);

@@ -5,19 +5,23 @@
 // largest maxima, followed by an exact top-k among their entries; exact ties
 // by ascending token id.
 //
-// GB300 design: one CTA per (row, chunk) where a chunk is a run of whole
-// 64-blocks of the row.  A single bulk copy (TMA engine) brings the chunk into
-// shared memory; the CTA then makes its passes there:
-//   A. block maxima (16-byte vectors, the 8 or 16 lanes of a block combine
-//      with shuffles) and the chunk maximum m;
-//   B. s = sum exp(x - m) with ex2 on the SFU;
-//   C. the k-th largest block maximum tau (radix select on the block maxima);
-//   D. candidates = entries >= tau inside blocks whose max >= tau (the true
-//      top-k of the chunk lies among them: the k kept blocks each hold an
-//      entry >= tau), then an exact top-k of the candidates by key.
-// The chunk's (m, s), its sorted top-k keys and, if the chunk holds it, the
-// selected token's logit go to the workspace; merge_partials.cu combines the
-// chunks of a row.
+// GB300 design: a persistent grid (two CTAs per SM) splits the flattened
+// (row, 64-block) space of the whole chunk into equal contiguous ranges, so
+// every CTA streams the same number of bytes whatever the row length.  A CTA
+// streams its range through a 4-stage ring of 16 KB bulk copies (TMA engine)
+// and, per 16-byte vector, folds the data into
+//   * the maxima of the 64-blocks (the 8 or 16 lanes of a block combine by
+//     shuffles) -- kept in shared memory for the current row piece;
+//   * a per-thread running max m and sum exp(x - m) (online rescaling).
+// When its range leaves a row (at most a few times per CTA) it finalizes that
+// row piece:
+//   1. (m, s) of the piece by a CTA reduction;
+//   2. tau = the k-th largest block maximum (radix select);
+//   3. candidates = entries >= tau of the blocks whose maximum is >= tau,
+//      re-read from L2; the true top-k of the piece lies among them, because
+//      the k blocks ranked first each hold an entry >= tau;
+//   4. the exact top-k of the candidates by key (value desc, id asc), by rank.
+// merge_partials.cu then combines the few pieces of each row.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -26,9 +30,13 @@
 
 namespace lmh {
 
-constexpr int kReduceThreads = 256;
-constexpr int kReduceCandCap = 512;  // candidate keys held in shared memory
-constexpr int kReduceMaxBlocksPerSplit = 256;
+constexpr int kRThreads = 256;
+constexpr int kRStages = 4;
+constexpr int kRStageBytes = 16384;
+constexpr int kRMaxPer = 4096;  // blocks per range: bounds the block-max buffer
+constexpr int kRMinPer = 32;    // >= 2048 logits per range
+constexpr int kRCandCap = 512;
+constexpr int kRCtasPerSm = 2;
 
 template <typename T>
 struct Vec16;  // 16-byte vector of T widened to fp32
@@ -46,7 +54,7 @@ struct Vec16<__nv_bfloat16> {
       x[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
     }
   }
-  __device__ __forceinline__ static float at(const void* base, int i) {
+  __device__ __forceinline__ static float at(const void* base, int64_t i) {
     const uint16_t b = reinterpret_cast<const uint16_t*>(base)[i];
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
   }
@@ -66,7 +74,7 @@ struct Vec16<__half> {
       x[2 * i + 1] = f.y;
     }
   }
-  __device__ __forceinline__ static float at(const void* base, int i) {
+  __device__ __forceinline__ static float at(const void* base, int64_t i) {
     return __half2float(reinterpret_cast<const __half*>(base)[i]);
   }
 };
@@ -82,7 +90,7 @@ struct Vec16<float> {
     x[2] = w.z;
     x[3] = w.w;
   }
-  __device__ __forceinline__ static float at(const void* base, int i) {
+  __device__ __forceinline__ static float at(const void* base, int64_t i) {
     return reinterpret_cast<const float*>(base)[i];
   }
 };
@@ -90,7 +98,11 @@ struct Vec16<float> {
 struct ReduceArgs {
   const char* logits;
   int64_t row_stride;  // elements
-  int rows, V, splits, bps;
+  int rows, V, nblk;   // nblk = 64-blocks per row
+  int64_t nb_total;    // rows * nblk
+  int per;             // blocks per range
+  int n_ranges;
+  int P;               // partial slots per row
   const int32_t* sel;
   const int32_t* row_k;
   int k_max;
@@ -98,225 +110,309 @@ struct ReduceArgs {
   uint32_t* dev_status;
 };
 
+// One chunk of a CTA's work: up to CH blocks of one row inside one range.
+struct Chunk {
+  int row, lb, nbk;  // row, first block in the row, blocks
+  int range;
+  bool valid;
+};
+
+// Walks the chunks of the ranges blockIdx.x, blockIdx.x + gridDim.x, ...
+template <int CH>
+struct ChunkIter {
+  int64_t b, end;
+  int range;
+  bool done;
+  __device__ void init(const ReduceArgs& a) {
+    range = blockIdx.x;
+    done = range >= a.n_ranges;
+    b = static_cast<int64_t>(range) * a.per;
+    end = min(b + a.per, a.nb_total);
+  }
+  __device__ Chunk next(const ReduceArgs& a) {
+    Chunk c;
+    c.valid = false;
+    c.row = c.lb = c.nbk = c.range = 0;
+    if (done) return c;
+    if (b >= end) {
+      range += gridDim.x;
+      if (range >= a.n_ranges) {
+        done = true;
+        return c;
+      }
+      b = static_cast<int64_t>(range) * a.per;
+      end = min(b + a.per, a.nb_total);
+    }
+    c.row = static_cast<int>(b / a.nblk);
+    c.lb = static_cast<int>(b - static_cast<int64_t>(c.row) * a.nblk);
+    c.nbk = static_cast<int>(min(static_cast<int64_t>(CH), min(end - b, static_cast<int64_t>(a.nblk - c.lb))));
+    c.range = range;
+    c.valid = true;
+    b += c.nbk;
+    return c;
+  }
+};
+
 template <typename T>
-__global__ void __launch_bounds__(kReduceThreads) logits_reduce_kernel(const ReduceArgs a) {
-  using VT = Vec16<T>;
-  constexpr int EPV = VT::N;                // elements per 16-byte vector
-  constexpr int VPB = kBlock / EPV;         // vectors per 64-block
-  constexpr int kValueBits = VT::kKeyBits;  // key bits that order the values exactly
-
-  extern __shared__ __align__(128) unsigned char smem[];
-  const int row = blockIdx.x / a.splits;
-  const int split = blockIdx.x % a.splits;
-  const int nblk_row = (a.V + kBlock - 1) / kBlock;
-  const int b0 = split * a.bps;
-  const int nb = min(a.bps, nblk_row - b0);
-  const int e0 = b0 * kBlock;
-  const int ne = min(nb * kBlock, a.V - e0);
-
-  // shared layout: chunk | bmax[bps] | cand[cap] | hist[256] | misc[4] | red[32] | barrier
-  const int chunk_bytes = ((a.bps * kBlock * static_cast<int>(sizeof(T))) + 15) & ~15;
-  T* chunk = reinterpret_cast<T*>(smem);
-  float* bmax = reinterpret_cast<float*>(smem + chunk_bytes);
-  uint64_t* cand = reinterpret_cast<uint64_t*>(smem + chunk_bytes + ((a.bps * 4 + 15) & ~15));
-  uint32_t* hist = reinterpret_cast<uint32_t*>(cand + kReduceCandCap);
-  uint32_t* misc = hist + 256;                            // [0] candidate count, [1..2] select broadcast
-  float* red = reinterpret_cast<float*>(misc + 4);        // 32 floats
-  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 32);  // 16-byte aligned offset
-
-  const char* src =
-      a.logits + (static_cast<int64_t>(row) * a.row_stride + e0) * static_cast<int64_t>(sizeof(T));
-  const uint32_t bytes = static_cast<uint32_t>(ne) * sizeof(T);
-  const uint32_t bulk = bytes & ~15u;
-
-  // rows whose start is 16-byte aligned arrive by one bulk copy; any other
-  // row pitch is copied by the whole CTA with plain element loads
-  const bool use_bulk = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
-  if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
-    mbar_init_fence();
-    misc[0] = 0;
-  }
-  __syncthreads();
-  if (use_bulk) {
-    if (threadIdx.x == 0) {
-      if (bulk > 0) {
-        mbar_arrive_expect_tx(bar, bulk);
-        bulk_load(chunk, src, bulk, bar);
-      } else {
-        mbar_arrive(bar);
-      }
-      // ragged tail (< 16 bytes) with plain loads
-      for (uint32_t o = bulk; o < bytes; o += sizeof(T))
-        *reinterpret_cast<T*>(reinterpret_cast<char*>(chunk) + o) = *reinterpret_cast<const T*>(src + o);
-    }
-  } else {
-    if (threadIdx.x == 0) mbar_arrive(bar);
-    const T* s = reinterpret_cast<const T*>(src);
-    for (int i = threadIdx.x; i < ne; i += kReduceThreads) chunk[i] = s[i];
-  }
-  const bool ok = mbar_wait(bar, 0);
-  if (!ok) {
-    if (threadIdx.x == 0) set_status(a.dev_status, LMH_DS_TIMEOUT);
-    return;
-  }
-  __syncthreads();  // the plain-load parts
-
-  // ---- pass A: block maxima and the chunk maximum ----
-  const int nvec = nb * VPB;
-  float tmax = -INFINITY;
-  for (int base = 0; base < nvec; base += kReduceThreads) {
-    const int v = base + threadIdx.x;
-    float x[EPV];
-    float vm = -INFINITY;
-    if (v < nvec) {
-      VT::load(reinterpret_cast<const char*>(chunk) + v * 16, x);
-      const int first = v * EPV;
-      if (first + EPV <= ne) {
-#pragma unroll
-        for (int j = 0; j < EPV; ++j) vm = fmaxf(vm, x[j]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < EPV; ++j)
-          if (first + j < ne) vm = fmaxf(vm, x[j]);
-      }
-    }
-    tmax = fmaxf(tmax, vm);
-#pragma unroll
-    for (int o = VPB / 2; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
-    if (v < nvec && (threadIdx.x % VPB) == 0) bmax[v / VPB] = vm;
-  }
-  const float m = block_max(tmax, red);
-
-  // ---- pass B: s = sum exp(x - m) ----
-  float tsum = 0.0f;
-  if (m != -INFINITY) {
-    const float mL = m * kLog2e;
-    for (int v = threadIdx.x; v < nvec; v += kReduceThreads) {
-      float x[EPV];
-      VT::load(reinterpret_cast<const char*>(chunk) + v * 16, x);
-      const int first = v * EPV;
-      if (first + EPV <= ne) {
-#pragma unroll
-        for (int j = 0; j < EPV; ++j) tsum += ex2_approx(fmaf(x[j], kLog2e, -mL));
-      } else {
-#pragma unroll
-        for (int j = 0; j < EPV; ++j)
-          if (first + j < ne) tsum += ex2_approx(fmaf(x[j], kLog2e, -mL));
-      }
-    }
-  }
-  const float s = block_sum(tsum, red);
-
-  const int64_t pidx = static_cast<int64_t>(row) * a.splits + split;
-  if (threadIdx.x == 0) {
-    a.parts.part_ms[pidx] = make_float2(m, s);
-    const int t = a.sel ? a.sel[row] : -1;
-    if (t >= e0 && t < e0 + ne) a.parts.sel_logit[row] = VT::at(chunk, t - e0);
-  }
-
-  int k = a.k_max;
-  if (a.row_k) k = min(max(a.row_k[row], 0), a.k_max);
-  if (k == 0) return;
-
-  // ---- pass C: tau = the k-th largest block maximum ----
-  uint32_t thr = 0;  // ord(tau) restricted to the top kValueBits bits; 0 keeps every entry
-  constexpr uint32_t kMask = kValueBits >= 32 ? 0xFFFFFFFFu : (0xFFFFFFFFu << (32 - kValueBits));
-  if (nb > k) {
-    int above;
-    const uint64_t T64 = cta_radix_select(
-        [&](int i, uint64_t* key) {
-          *key = static_cast<uint64_t>(f32_ord(bmax[i])) << 32;
-          return true;
-        },
-        nb, k, kValueBits, hist, misc + 1, &above);
-    thr = static_cast<uint32_t>(T64 >> 32);
-  }
-
-  // ---- pass D: candidates, then the exact top-k among them ----
-  auto in_set = [&](int i, uint64_t* key) -> bool {
-    const int b = i / kBlock;
-    if ((f32_ord(bmax[b]) & kMask) < thr) return false;
-    if (i >= ne) return false;
-    const float x = VT::at(chunk, i);
-    if ((f32_ord(x) & kMask) < thr) return false;
-    *key = make_key(x, e0 + i);
-    return true;
-  };
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int b = warp; b < nb; b += kReduceThreads / 32) {
-    if ((f32_ord(bmax[b]) & kMask) < thr) continue;  // warp-uniform: block pruned
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int i = b * kBlock + h * 32 + lane;
-      uint64_t key = 0;
-      const bool in = in_set(i, &key);
-      const unsigned bal = __ballot_sync(0xffffffffu, in);
-      uint32_t basepos = 0;
-      if (lane == 0 && bal) basepos = atomicAdd(&misc[0], __popc(bal));
-      basepos = __shfl_sync(0xffffffffu, basepos, 0);
-      if (in) {
-        const uint32_t pos = basepos + __popc(bal & ((1u << lane) - 1u));
-        if (pos < kReduceCandCap) cand[pos] = key;
-      }
-    }
-  }
-  __syncthreads();
-  const int cnt = static_cast<int>(misc[0]);
-  int nsort = cnt;
-  if (cnt > kReduceCandCap) {
-    // many exact ties at tau: exact radix select over the whole candidate set
-    int above;
-    const uint64_t T64 = cta_radix_select(in_set, nb * kBlock, k, 64, hist, misc + 1, &above);
-    __syncthreads();
-    if (threadIdx.x == 0) misc[0] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < nb * kBlock; i += kReduceThreads) {
-      uint64_t key = 0;
-      if (in_set(i, &key) && key >= T64) {
-        const uint32_t pos = atomicAdd(&misc[0], 1u);  // exactly k of them
-        if (pos < kReduceCandCap) cand[pos] = key;
-      }
-    }
-    __syncthreads();
-    nsort = min(k, static_cast<int>(misc[0]));
-  }
-  const int n2 = next_pow2(nsort);
-  for (int i = nsort + threadIdx.x; i < n2; i += kReduceThreads) cand[i] = 0ull;
-  cta_bitonic_sort_desc(cand, n2);
-  unsigned long long* out = a.parts.part_keys + pidx * a.k_max;
-  for (int j = threadIdx.x; j < k; j += kReduceThreads) out[j] = (j < nsort) ? cand[j] : 0ull;
+__device__ __forceinline__ const char* chunk_src(const ReduceArgs& a, const Chunk& c) {
+  return a.logits + (static_cast<int64_t>(c.row) * a.row_stride + static_cast<int64_t>(c.lb) * kBlock) *
+                        static_cast<int64_t>(sizeof(T));
 }
 
-VocabSplit logits_reduce_split(int rows, int V, int num_sms) {
-  const int nblk = (V + kBlock - 1) / kBlock;
-  const int lo = (nblk + kReduceMaxBlocksPerSplit - 1) / kReduceMaxBlocksPerSplit;  // shared-memory bound
-  const int want = (4 * num_sms + rows - 1) / (rows > 0 ? rows : 1);                // enough CTAs
-  const int hi = nblk / 16 > lo ? nblk / 16 : lo;                                   // >= 1024 logits each
-  int splits = want < lo ? lo : (want > hi ? hi : want);
-  if (splits < 1) splits = 1;
-  const int bps = (nblk + splits - 1) / splits;
+template <typename T>
+__device__ __forceinline__ int chunk_elems(const ReduceArgs& a, const Chunk& c) {
+  return min(c.nbk * kBlock, a.V - c.lb * kBlock);
+}
+
+// Thread 0: start the copy of chunk c into `stage`.  A chunk whose start is
+// not 16-byte aligned only arrives on the barrier: the CTA copies it itself.
+template <typename T>
+__device__ __forceinline__ void issue_chunk(const ReduceArgs& a, const Chunk& c, unsigned char* stage,
+                                            uint64_t* bar) {
+  const char* src = chunk_src<T>(a, c);
+  const uint32_t bytes = static_cast<uint32_t>(chunk_elems<T>(a, c)) * sizeof(T);
+  if ((reinterpret_cast<uintptr_t>(src) & 15u) != 0) {
+    mbar_arrive(bar);
+    return;
+  }
+  const uint32_t bulk = bytes & ~15u;
+  for (uint32_t o = bulk; o < bytes; o += sizeof(T))  // ragged tail (< 16 bytes), before the arrive
+    *reinterpret_cast<T*>(stage + o) = *reinterpret_cast<const T*>(src + o);
+  if (bulk > 0) {
+    mbar_arrive_expect_tx(bar, bulk);
+    bulk_load(stage, src, bulk, bar);
+  } else {
+    mbar_arrive(bar);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRThreads) logits_reduce_kernel(const ReduceArgs a) {
+  using VT = Vec16<T>;
+  constexpr int EPV = VT::N;                                                  // elements per 16-byte vector
+  constexpr int VPB = kBlock / EPV;                                           // vectors per 64-block
+  constexpr int CH = kRStageBytes / (kBlock * static_cast<int>(sizeof(T)));  // blocks per chunk
+  constexpr int kValueBits = VT::kKeyBits;
+  constexpr uint32_t kMask = kValueBits >= 32 ? 0xFFFFFFFFu : (0xFFFFFFFFu << (32 - kValueBits));
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* ring = smem;
+  float* bmax = reinterpret_cast<float*>(smem + kRStages * kRStageBytes);
+  uint64_t* cand = reinterpret_cast<uint64_t*>(bmax + kRMaxPer);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(cand + kRCandCap);
+  uint32_t* misc = hist + 256;  // [0] candidate count, [1..2] select broadcast
+  float* red = reinterpret_cast<float*>(misc + 8);
+  uint64_t* red64 = reinterpret_cast<uint64_t*>(red + 32);
+  uint64_t* full = red64 + 32;  // kRStages mbarriers
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRStages; ++s) mbar_init(&full[s], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  ChunkIter<CH> prod, cons;
+  if (threadIdx.x == 0) {
+    prod.init(a);
+    for (int s = 0; s < kRStages; ++s) {
+      const Chunk c = prod.next(a);
+      if (!c.valid) break;
+      issue_chunk<T>(a, c, ring + s * kRStageBytes, &full[s]);
+    }
+  }
+  cons.init(a);
+  Chunk cur = cons.next(a);
+
+  const float L = kLog2e;
+  float tm = -INFINITY, ts = 0.0f;  // this thread's running max / sum over the current piece
+  int piece_blocks = 0, piece_lb = 0;
+  for (uint32_t i = 0; cur.valid; ++i) {
+    const int s = static_cast<int>(i % kRStages);
+    unsigned char* stage = ring + s * kRStageBytes;
+    const Chunk nxt = cons.next(a);
+    if (piece_blocks == 0) piece_lb = cur.lb;
+    if (!mbar_wait(&full[s], (i / kRStages) & 1u)) {
+      if (threadIdx.x == 0) set_status(a.dev_status, LMH_DS_TIMEOUT);
+      return;
+    }
+    const char* src = chunk_src<T>(a, cur);
+    const int ne = chunk_elems<T>(a, cur);
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) != 0) {  // unaligned row start: copy it here
+      for (int e = threadIdx.x; e < ne; e += kRThreads)
+        reinterpret_cast<T*>(stage)[e] = reinterpret_cast<const T*>(src)[e];
+      __syncthreads();
+    }
+
+    // ---- block maxima + online (m, s) ----
+    const int nvec = cur.nbk * VPB;
+    for (int base = 0; base < nvec; base += kRThreads) {
+      const int v = base + threadIdx.x;
+      float x[EPV];
+      float vm = -INFINITY;
+      if (v < nvec) {
+        VT::load(stage + v * 16, x);
+        const int first = v * EPV;
+        if (first + EPV > ne) {
+#pragma unroll
+          for (int j = 0; j < EPV; ++j)
+            if (first + j >= ne) x[j] = -INFINITY;
+        }
+#pragma unroll
+        for (int j = 0; j < EPV; ++j) vm = fmaxf(vm, x[j]);
+        if (vm > tm) {
+          ts = (tm == -INFINITY) ? 0.0f : ts * ex2_approx((tm - vm) * L);
+          tm = vm;
+        }
+        if (tm != -INFINITY) {
+          const float mL = tm * L;
+#pragma unroll
+          for (int j = 0; j < EPV; ++j) ts += ex2_approx(fmaf(x[j], L, -mL));
+        }
+      }
+#pragma unroll
+      for (int o = VPB / 2; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+      if (v < nvec && (threadIdx.x % VPB) == 0) bmax[piece_blocks + v / VPB] = vm;
+    }
+    if (threadIdx.x == 0 && a.sel) {
+      const int t = a.sel[cur.row] - cur.lb * kBlock;
+      if (t >= 0 && t < ne) a.parts.sel_logit[cur.row] = VT::at(stage, t);
+    }
+    piece_blocks += cur.nbk;
+    __syncthreads();  // stage s is free; this chunk's block maxima are in place
+    if (threadIdx.x == 0) {
+      const Chunk c = prod.next(a);
+      if (c.valid) issue_chunk<T>(a, c, stage, &full[s]);
+    }
+
+    const bool piece_end = !nxt.valid || nxt.row != cur.row || nxt.range != cur.range;
+    if (piece_end) {
+      // ---- finalize the row piece [piece_lb, piece_lb + piece_blocks) of row cur.row ----
+      const int row = cur.row;
+      const int slot = cur.range - static_cast<int>((static_cast<int64_t>(row) * a.nblk) / a.per);
+      const int64_t pidx = static_cast<int64_t>(row) * a.P + slot;
+      const float M = block_max(tm, red);
+      const float S = block_sum((tm == -INFINITY) ? 0.0f : ts * expf(tm - M), red);
+      if (threadIdx.x == 0) {
+        a.parts.part_ms[pidx] = make_float2(M, M == -INFINITY ? 0.0f : S);
+        misc[0] = 0;
+      }
+      int k = a.k_max;
+      if (a.row_k) k = min(max(a.row_k[row], 0), a.k_max);
+      if (k > 0) {
+        const int nbp = piece_blocks;
+        const int e_lo = piece_lb * kBlock;                    // first element of the piece
+        const int e_hi = min((piece_lb + nbp) * kBlock, a.V);  // one past its last element
+        const char* rowp =
+            a.logits + static_cast<int64_t>(row) * a.row_stride * static_cast<int64_t>(sizeof(T));
+        uint32_t thr = 0;  // ord(tau) restricted to the top kValueBits bits; 0 keeps every entry
+        if (nbp > k) {
+          int above;
+          const uint64_t T64 = cta_radix_select(
+              [&](int b, uint64_t* key) {
+                *key = static_cast<uint64_t>(f32_ord(bmax[b])) << 32;
+                return true;
+              },
+              nbp, k, kValueBits, hist, misc + 1, &above);
+          thr = static_cast<uint32_t>(T64 >> 32);
+        }
+        auto in_set = [&](int i, uint64_t* key) -> bool {
+          const int b = i / kBlock;
+          if ((f32_ord(bmax[b]) & kMask) < thr) return false;
+          const int e = e_lo + i;
+          if (e >= e_hi) return false;
+          const float x = VT::at(rowp, e);
+          if ((f32_ord(x) & kMask) < thr) return false;
+          *key = make_key(x, e);
+          return true;
+        };
+        __syncthreads();
+        // candidates: one warp per kept block, its entries re-read (from L2)
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        for (int b = warp; b < nbp; b += kRThreads / 32) {
+          if ((f32_ord(bmax[b]) & kMask) < thr) continue;  // warp-uniform: block pruned
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint64_t key = 0;
+            const bool in = in_set(b * kBlock + h * 32 + lane, &key);
+            const unsigned bal = __ballot_sync(0xffffffffu, in);
+            uint32_t basepos = 0;
+            if (lane == 0 && bal) basepos = atomicAdd(&misc[0], __popc(bal));
+            basepos = __shfl_sync(0xffffffffu, basepos, 0);
+            if (in) {
+              const uint32_t pos = basepos + __popc(bal & ((1u << lane) - 1u));
+              if (pos < kRCandCap) cand[pos] = key;
+            }
+          }
+        }
+        __syncthreads();
+        int cnt = static_cast<int>(misc[0]);
+        if (cnt > kRCandCap) {
+          // many exact ties at tau: exact radix select over the candidate set, then keep the k best
+          int above;
+          const uint64_t T64 = cta_radix_select(in_set, nbp * kBlock, k, 64, hist, misc + 1, &above);
+          __syncthreads();
+          if (threadIdx.x == 0) misc[0] = 0;
+          __syncthreads();
+          for (int i = threadIdx.x; i < nbp * kBlock; i += kRThreads) {
+            uint64_t key = 0;
+            if (in_set(i, &key) && key >= T64) {
+              const uint32_t pos = atomicAdd(&misc[0], 1u);
+              if (pos < kRCandCap) cand[pos] = key;
+            }
+          }
+          __syncthreads();
+          cnt = min(k, static_cast<int>(misc[0]));
+        }
+        // exact order by rank (keys are unique)
+        unsigned long long* out = a.parts.part_keys + pidx * a.k_max;
+        for (int t = threadIdx.x; t < cnt; t += kRThreads) {
+          const uint64_t key = cand[t];
+          int rank = 0;
+          for (int j = 0; j < cnt; ++j) rank += cand[j] > key;
+          if (rank < k) out[rank] = key;
+        }
+        for (int j = cnt + threadIdx.x; j < k; j += kRThreads) out[j] = 0ull;
+      }
+      __syncthreads();  // cand / misc / bmax are reused by the next piece
+      tm = -INFINITY;
+      ts = 0.0f;
+      piece_blocks = 0;
+    }
+    cur = nxt;
+  }
+}
+
+VocabSplit logits_reduce_split(int rows, int V, int k_max, int num_sms) {
   VocabSplit vs;
-  vs.blocks_per_split = bps;
-  vs.splits = (nblk + bps - 1) / bps;
+  const int nblk = (V + kBlock - 1) / kBlock;
+  const int64_t nb_total = static_cast<int64_t>(rows) * nblk;
+  const int64_t G = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * kRCtasPerSm;
+  int64_t per = (nb_total + G - 1) / G;
+  // a range of more than 2k blocks lets the block-max threshold prune (<= k blocks keep everything)
+  const int64_t min_per = 2 * k_max > kRMinPer ? 2 * k_max : kRMinPer;
+  if (per < min_per) per = min_per;
+  if (per > kRMaxPer) per = kRMaxPer;
+  vs.per = static_cast<int>(per);
+  vs.n_ranges = static_cast<int>((nb_total + per - 1) / per);
+  vs.grid = static_cast<int>(vs.n_ranges < G ? vs.n_ranges : G);
+  vs.splits = static_cast<int>((nblk + per - 1) / per) + 1;  // row pieces per row, at most
+  vs.nblk = nblk;
   return vs;
 }
 
-static size_t reduce_smem_bytes(int bps, int elem) {
-  size_t chunk = ((static_cast<size_t>(bps) * kBlock * elem) + 15) & ~static_cast<size_t>(15);
-  size_t b = ((static_cast<size_t>(bps) * 4) + 15) & ~static_cast<size_t>(15);
-  return chunk + b + kReduceCandCap * 8 + 256 * 4 + 4 * 4 + 32 * 4 + 16;
+static size_t reduce_smem_bytes() {
+  return static_cast<size_t>(kRStages) * kRStageBytes + kRMaxPer * 4 + kRCandCap * 8 + 256 * 4 + 8 * 4 + 32 * 4 +
+         32 * 8 + kRStages * 8;
 }
 
 cudaError_t logits_reduce_setup() {
-  const int max2 = static_cast<int>(reduce_smem_bytes(kReduceMaxBlocksPerSplit, 2));
-  const int max4 = static_cast<int>(reduce_smem_bytes(kReduceMaxBlocksPerSplit, 4));
+  const int bytes = static_cast<int>(reduce_smem_bytes());
   cudaError_t e = cudaFuncSetAttribute(logits_reduce_kernel<__nv_bfloat16>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, max2);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(logits_reduce_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, max2);
+    e = cudaFuncSetAttribute(logits_reduce_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(logits_reduce_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, max4);
+    e = cudaFuncSetAttribute(logits_reduce_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   return e;
 }
 
@@ -328,23 +424,27 @@ cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t ro
   a.row_stride = row_stride;
   a.rows = rows;
   a.V = V;
-  a.splits = split.splits;
-  a.bps = split.blocks_per_split;
+  a.nblk = split.nblk;
+  a.nb_total = static_cast<int64_t>(rows) * split.nblk;
+  a.per = split.per;
+  a.n_ranges = split.n_ranges;
+  a.P = split.splits;
   a.sel = sel;
   a.row_k = row_k;
   a.k_max = k_max;
   a.parts = parts;
   a.dev_status = dev_status;
-  const dim3 grid(static_cast<unsigned>(rows) * static_cast<unsigned>(split.splits));
+  const dim3 grid(static_cast<unsigned>(split.grid));
+  const size_t smem = reduce_smem_bytes();
   switch (dtype) {
     case LMH_BF16:
-      logits_reduce_kernel<__nv_bfloat16><<<grid, kReduceThreads, reduce_smem_bytes(a.bps, 2), stream>>>(a);
+      logits_reduce_kernel<__nv_bfloat16><<<grid, kRThreads, smem, stream>>>(a);
       break;
     case LMH_F16:
-      logits_reduce_kernel<__half><<<grid, kReduceThreads, reduce_smem_bytes(a.bps, 2), stream>>>(a);
+      logits_reduce_kernel<__half><<<grid, kRThreads, smem, stream>>>(a);
       break;
     default:
-      logits_reduce_kernel<float><<<grid, kReduceThreads, reduce_smem_bytes(a.bps, 4), stream>>>(a);
+      logits_reduce_kernel<float><<<grid, kRThreads, smem, stream>>>(a);
       break;
   }
   return cudaGetLastError();

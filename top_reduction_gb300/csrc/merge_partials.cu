@@ -24,6 +24,7 @@ constexpr int kMergeCap = 1024;
 
 struct MergeArgs {
   int rows, splits, V, k_max;
+  int flat_per, flat_nblk;  // flat_per > 0: the slots a row fills follow the range layout
   Partials parts;
   const int32_t* sel;
   const int32_t* row_k;
@@ -43,10 +44,15 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
 
   const int row = blockIdx.x;
   const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.splits;
+  int nslots = a.splits;
+  if (a.flat_per > 0) {
+    const int64_t b0 = static_cast<int64_t>(row) * a.flat_nblk;
+    nslots = static_cast<int>((b0 + a.flat_nblk - 1) / a.flat_per - b0 / a.flat_per) + 1;
+  }
 
   // ---- lse ----
   float tm = -INFINITY, ts = 0.0f;
-  for (int j = threadIdx.x; j < a.splits; j += kMergeThreads) {
+  for (int j = threadIdx.x; j < nslots; j += kMergeThreads) {
     const float2 p = ms[j];
     if (p.x > tm) {
       ts = (tm == -INFINITY) ? 0.0f : ts * expf(tm - p.x);
@@ -86,13 +92,13 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
   const unsigned long long* keys = a.parts.part_keys + static_cast<int64_t>(row) * a.splits * a.k_max;
   // lower bound of the row's k-th key
   uint64_t lb = 0;
-  for (int j = threadIdx.x; j < a.splits; j += kMergeThreads) {
+  for (int j = threadIdx.x; j < nslots; j += kMergeThreads) {
     const uint64_t kk = keys[static_cast<int64_t>(j) * a.k_max + (k - 1)];
     lb = kk > lb ? kk : lb;
   }
   lb = block_max_u64(lb, red64);
 
-  const int n_items = a.splits * k;
+  const int n_items = nslots * k;
   auto in_set = [&](int i, uint64_t* key) -> bool {
     const int j = i / k, r = i - j * k;
     const uint64_t kk = keys[static_cast<int64_t>(j) * a.k_max + r];
@@ -146,8 +152,11 @@ cudaError_t merge_setup() { return cudaSuccess; }
 
 cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts, const int32_t* sel,
                          const int32_t* row_k, float* lse, float* sel_logprob, int32_t* topk_ids,
-                         float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream) {
+                         float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream, int flat_per,
+                         int flat_nblk) {
   MergeArgs a;
+  a.flat_per = flat_per;
+  a.flat_nblk = flat_nblk;
   a.rows = rows;
   a.splits = splits;
   a.V = V;

@@ -92,7 +92,7 @@ extern "C" lmh_status lmh_logprobs_from_logits_static(const void* logits, lmh_dt
   void* scratch = nullptr;
   int sms = 0;
   if (static_setup(&scratch, &sms) != cudaSuccess) return LMH_ERR_CUDA;
-  const VocabSplit vs = logits_reduce_split(rows, V, sms);
+  const VocabSplit vs = logits_reduce_split(rows, V, k_max, sms);
   if (static_cast<int64_t>(rows) * vs.splits > INT32_MAX) return LMH_ERR_UNSUPPORTED;
   if (partials_bytes(rows, vs.splits, k_max) > kStaticScratchBytes) return LMH_ERR_WORKSPACE_TOO_SMALL;
   const Partials parts = carve_partials(scratch, rows, vs.splits, k_max);
@@ -100,6 +100,6 @@ extern "C" lmh_status lmh_logprobs_from_logits_static(const void* logits, lmh_dt
                                        dev_status, stream);
   if (e == cudaSuccess)
     e = launch_merge(rows, vs.splits, V, k_max, parts, sel_ids, row_k, lse, sel_logprob, topk_ids, topk_logprobs,
-                     dev_status, stream);
+                     dev_status, stream, vs.per, vs.nblk);
   return e == cudaSuccess ? LMH_OK : LMH_ERR_CUDA;
 }
