@@ -125,6 +125,17 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, 
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// A kernel launched with the programmatic-serialization attribute may start
+// while its predecessor in the stream is still running; pdl_wait() blocks
+// until the predecessor has completed and its writes are visible (a no-op
+// without such a predecessor).  pdl_launch_dependents() lets the successor be
+// scheduled once every CTA of this grid has executed it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// ---------------------------------------------------------------------------
 // reductions
 // ---------------------------------------------------------------------------
 

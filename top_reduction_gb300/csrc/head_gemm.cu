@@ -275,31 +275,66 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_launch_dependents();  // the merge may be scheduled; it waits for this grid's partials
 
   if (warp == 0) {
     // ------------------------- TMA producer -------------------------
+    // The (unit, n-tile, k-block) sequence of this CTA.  W does not depend on
+    // the kernel launched before this one (the row gather), so the first S
+    // stages get their W slices before the grid-dependency wait; their A
+    // slices (the gathered rows) follow it.
     if (lane == 0) {
       prefetch_tmap(&tmap_a);
       prefetch_tmap(&tmap_b);
-      uint32_t it = 0;
-      bool live = true;
-      for (int u = blockIdx.x; u < a.num_units && live; u += gridDim.x) {
-        const int m_tile = u % a.m_tiles, split = u / a.m_tiles;
-        const int n_begin = split * a.tiles_per_split;
-        const int n_end = min(n_begin + a.tiles_per_split, a.n_tiles);
-        for (int n = n_begin; n < n_end && live; ++n) {
-          for (int kb = 0; kb < k_blocks; ++kb, ++it) {
-            const int s = it % S;
-            const uint32_t ph = (it / S) & 1u;
-            if (!wait_or_abort(&empty[s], ph ^ 1u, abort_flag, a.dev_status)) {
-              live = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&full[s], kStageBytesA + kStageBytesB);
-            tma_load_2d(sA + s * kStageBytesA, &tmap_a, kb * kBK, m_tile * kBM, &full[s]);
-            tma_load_2d(sB + s * kStageBytesB, &tmap_b, kb * kBK, n * kBN, &full[s]);
+      int u = blockIdx.x, m_tile = 0, n = 0, n_end = 0, kb = 0;
+      bool valid = false;
+      auto start_unit = [&]() {
+        valid = false;
+        for (; u < a.num_units; u += gridDim.x) {
+          m_tile = u % a.m_tiles;
+          n = (u / a.m_tiles) * a.tiles_per_split;
+          n_end = min(n + a.tiles_per_split, a.n_tiles);
+          if (n < n_end) {
+            valid = true;
+            return;
           }
         }
+      };
+      auto advance = [&]() {
+        if (++kb == k_blocks) {
+          kb = 0;
+          if (++n == n_end) {
+            u += gridDim.x;
+            start_unit();
+          }
+        }
+      };
+      start_unit();
+      int pm[S], pk[S];
+      int np = 0;
+#pragma unroll
+      for (int j = 0; j < S; ++j) {
+        if (valid) {  // a fresh ring: the empty barriers need no wait yet
+          pm[j] = m_tile;
+          pk[j] = kb;
+          mbar_arrive_expect_tx(&full[j], kStageBytesA + kStageBytesB);
+          tma_load_2d(sB + j * kStageBytesB, &tmap_b, kb * kBK, n * kBN, &full[j]);
+          advance();
+          np = j + 1;
+        }
+      }
+      pdl_wait();  // the gathered rows are written by the preceding kernel
+#pragma unroll
+      for (int j = 0; j < S; ++j)
+        if (j < np) tma_load_2d(sA + j * kStageBytesA, &tmap_a, pk[j] * kBK, pm[j] * kBM, &full[j]);
+      for (uint32_t it = np; valid; ++it) {
+        const int s = it % S;
+        const uint32_t ph = (it / S) & 1u;
+        if (!wait_or_abort(&empty[s], ph ^ 1u, abort_flag, a.dev_status)) break;
+        mbar_arrive_expect_tx(&full[s], kStageBytesA + kStageBytesB);
+        tma_load_2d(sA + s * kStageBytesA, &tmap_a, kb * kBK, m_tile * kBM, &full[s]);
+        tma_load_2d(sB + s * kStageBytesB, &tmap_b, kb * kBK, n * kBN, &full[s]);
+        advance();
       }
     }
   } else if (warp == 1) {
@@ -496,6 +531,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ hidden, int64_t stride,
                                                           int num_tokens, const int32_t* __restrict__ row_idx,
                                                           int H, uint16_t* __restrict__ out, uint32_t* dev_status) {
+  pdl_launch_dependents();  // the head kernel may start and stream W meanwhile
   const int i = blockIdx.x;
   const int src = row_idx ? row_idx[i] : i;
   const bool ok = src >= 0 && src < num_tokens;
@@ -606,7 +642,7 @@ cudaError_t head_setup() {
 
 cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const void* W, int V, const HeadPlan& plan,
                         const int32_t* sel, const int32_t* row_k, int k_max, Partials parts, float* logits_out,
-                        uint32_t* dev_status, cudaStream_t stream) {
+                        uint32_t* dev_status, cudaStream_t stream, bool pdl) {
   CUtensorMap ta, tb;
   cudaError_t e = make_tmap(&ta, A, static_cast<uint64_t>(H), static_cast<uint64_t>(rows),
                             static_cast<uint64_t>(a_stride), kBK, kBM);
@@ -630,12 +666,12 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   a.dev_status = dev_status;
   const dim3 grid(plan.grid), block(kHeadThreads);
   switch (plan.kcap) {
-#define LMH_HEAD_CASE(KC)                                                                     \
-  case KC:                                                                                    \
-    if (logits_out)                                                                           \
-      head_logprobs_kernel<KC, true><<<grid, block, HeadCfg<KC>::kSmem, stream>>>(ta, tb, a);  \
-    else                                                                                      \
-      head_logprobs_kernel<KC, false><<<grid, block, HeadCfg<KC>::kSmem, stream>>>(ta, tb, a); \
+#define LMH_HEAD_CASE(KC)                                                                               \
+  case KC:                                                                                              \
+    e = logits_out ? launch_kernel(head_logprobs_kernel<KC, true>, grid, block, HeadCfg<KC>::kSmem, stream, \
+                                   pdl, ta, tb, a)                                                       \
+                   : launch_kernel(head_logprobs_kernel<KC, false>, grid, block, HeadCfg<KC>::kSmem,       \
+                                   stream, pdl, ta, tb, a);                                              \
     break;
     LMH_HEAD_CASE(4)
     LMH_HEAD_CASE(8)
@@ -647,7 +683,7 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
     default:
       return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace lmh

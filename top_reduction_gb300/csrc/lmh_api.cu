@@ -244,12 +244,13 @@ lmh_status lmh_project_logprobs(const void* hidden, int64_t hidden_row_stride, i
   }
   if (e == cudaSuccess) {
     Traced tr(kTraceHead, stream);
-    e = launch_head(A, a_stride, rows, H, W, V, plan, sel_ids, row_k, k_max, parts, logits_out, dev_status, stream);
+    e = launch_head(A, a_stride, rows, H, W, V, plan, sel_ids, row_k, k_max, parts, logits_out, dev_status, stream,
+                    /*pdl=*/gather);
   }
   if (e == cudaSuccess) {
     Traced tr(kTraceMerge, stream);
     e = launch_merge(rows, plan.splits, V, k_max, parts, sel_ids, row_k, lse, sel_logprob, topk_ids, topk_logprobs,
-                     dev_status, stream);
+                     dev_status, stream, 0, 0, /*pdl=*/true);
   }
   return from_cuda(e);
 }
@@ -284,7 +285,7 @@ lmh_status lmh_logprobs_from_logits(const void* logits, lmh_dtype dtype, int32_t
   if (e == cudaSuccess) {
     Traced tr(kTraceMerge, stream);
     e = launch_merge(rows, vs.splits, V, k_max, parts, sel_ids, row_k, lse, sel_logprob, topk_ids, topk_logprobs,
-                     dev_status, stream, vs.per, vs.nblk);
+                     dev_status, stream, vs.per, vs.nblk, /*pdl=*/true);
   }
   return from_cuda(e);
 }

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include <cuda_runtime.h>
 
@@ -59,7 +60,7 @@ cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t ro
 cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts, const int32_t* sel,
                          const int32_t* row_k, float* lse, float* sel_logprob, int32_t* topk_ids,
                          float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream, int flat_per = 0,
-                         int flat_nblk = 0);
+                         int flat_nblk = 0, bool pdl = false);
 
 // ---- head projection (head_gemm.cu) ----
 
@@ -81,7 +82,28 @@ cudaError_t launch_gather_rows(const void* hidden, int64_t hidden_stride, int nu
 
 cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const void* W, int V,
                         const HeadPlan& plan, const int32_t* sel, const int32_t* row_k, int k_max,
-                        Partials parts, float* logits_out, uint32_t* dev_status, cudaStream_t stream);
+                        Partials parts, float* logits_out, uint32_t* dev_status, cudaStream_t stream,
+                        bool pdl = false);
+
+// Launch `kernel` on `stream`; with pdl = true it carries the programmatic
+// stream serialization attribute, so it may start while its predecessor in the
+// stream finishes (the kernel calls pdl_wait() before reading that
+// predecessor's output).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- tracing (lmh_api.cu) ----
 enum TraceKernel { kTraceSelect = 0, kTraceGather, kTraceHead, kTraceReduce, kTraceMerge, kTraceCount };

@@ -8,8 +8,9 @@
 // GB300 design: a persistent grid (two CTAs per SM) splits the flattened
 // (row, 64-block) space of the whole chunk into equal contiguous ranges, so
 // every CTA streams the same number of bytes whatever the row length.  A CTA
-// streams its range through a 4-stage ring of 16 KB bulk copies (TMA engine)
-// and, per 16-byte vector, folds the data into
+// streams its range in chunks of 2048 coalesced 16-byte vectors (eight per
+// thread), issuing the next chunk's loads before it works on the current
+// one, and folds every vector into
 //   * the maxima of the 64-blocks (the 8 or 16 lanes of a block combine by
 //     shuffles) -- kept in shared memory for the current row piece;
 //   * a per-thread running max m and sum exp(x - m) (online rescaling).
@@ -31,10 +32,9 @@
 namespace lmh {
 
 constexpr int kRThreads = 256;
-constexpr int kRStages = 4;
-constexpr int kRStageBytes = 16384;
-constexpr int kRMaxPer = 4096;  // blocks per range: bounds the block-max buffer
-constexpr int kRMinPer = 32;    // >= 2048 logits per range
+constexpr int kRVecPerThread = 8;  // 16-byte vectors per thread per chunk
+constexpr int kRMaxPer = 4096;     // blocks per range: bounds the block-max buffer
+constexpr int kRMinPer = 32;       // >= 2048 logits per range
 constexpr int kRCandCap = 512;
 constexpr int kRCtasPerSm = 2;
 
@@ -95,6 +95,21 @@ struct Vec16<float> {
   }
 };
 
+template <typename T>
+__device__ __forceinline__ T neg_inf();
+template <>
+__device__ __forceinline__ __nv_bfloat16 neg_inf<__nv_bfloat16>() {
+  return __ushort_as_bfloat16(static_cast<unsigned short>(0xFF80u));
+}
+template <>
+__device__ __forceinline__ __half neg_inf<__half>() {
+  return __ushort_as_half(static_cast<unsigned short>(0xFC00u));
+}
+template <>
+__device__ __forceinline__ float neg_inf<float>() {
+  return -INFINITY;
+}
+
 struct ReduceArgs {
   const char* logits;
   int64_t row_stride;  // elements
@@ -118,174 +133,153 @@ struct Chunk {
 };
 
 // Walks the chunks of the ranges blockIdx.x, blockIdx.x + gridDim.x, ...
+// (row and block advance incrementally; one division per range).
 template <int CH>
 struct ChunkIter {
-  int64_t b, end;
-  int range;
+  int64_t left;  // blocks left in the current range
+  int row, lb, range;
   bool done;
+  __device__ void start(const ReduceArgs& a) {
+    if (range >= a.n_ranges) {
+      done = true;
+      return;
+    }
+    const int64_t b = static_cast<int64_t>(range) * a.per;
+    left = min(static_cast<int64_t>(a.per), a.nb_total - b);
+    row = static_cast<int>(b / a.nblk);
+    lb = static_cast<int>(b - static_cast<int64_t>(row) * a.nblk);
+  }
   __device__ void init(const ReduceArgs& a) {
     range = blockIdx.x;
-    done = range >= a.n_ranges;
-    b = static_cast<int64_t>(range) * a.per;
-    end = min(b + a.per, a.nb_total);
+    done = false;
+    start(a);
   }
   __device__ Chunk next(const ReduceArgs& a) {
     Chunk c;
     c.valid = false;
     c.row = c.lb = c.nbk = c.range = 0;
     if (done) return c;
-    if (b >= end) {
+    if (left == 0) {
       range += gridDim.x;
-      if (range >= a.n_ranges) {
-        done = true;
-        return c;
-      }
-      b = static_cast<int64_t>(range) * a.per;
-      end = min(b + a.per, a.nb_total);
+      start(a);
+      if (done) return c;
     }
-    c.row = static_cast<int>(b / a.nblk);
-    c.lb = static_cast<int>(b - static_cast<int64_t>(c.row) * a.nblk);
-    c.nbk = static_cast<int>(min(static_cast<int64_t>(CH), min(end - b, static_cast<int64_t>(a.nblk - c.lb))));
+    c.row = row;
+    c.lb = lb;
+    c.nbk = static_cast<int>(min(static_cast<int64_t>(CH), min(left, static_cast<int64_t>(a.nblk - lb))));
     c.range = range;
     c.valid = true;
-    b += c.nbk;
+    left -= c.nbk;
+    lb += c.nbk;
+    if (lb == a.nblk) {
+      lb = 0;
+      ++row;
+    }
     return c;
   }
 };
 
+// The chunk's vectors v = threadIdx.x + j * kRThreads (j < kRVecPerThread)
+// held in registers; `ne` logits of the chunk are real, the rest read as -inf.
 template <typename T>
-__device__ __forceinline__ const char* chunk_src(const ReduceArgs& a, const Chunk& c) {
-  return a.logits + (static_cast<int64_t>(c.row) * a.row_stride + static_cast<int64_t>(c.lb) * kBlock) *
-                        static_cast<int64_t>(sizeof(T));
-}
+struct ChunkRegs {
+  uint4 w[kRVecPerThread];
+  int ne;
 
-template <typename T>
-__device__ __forceinline__ int chunk_elems(const ReduceArgs& a, const Chunk& c) {
-  return min(c.nbk * kBlock, a.V - c.lb * kBlock);
-}
-
-// Thread 0: start the copy of chunk c into `stage`.  A chunk whose start is
-// not 16-byte aligned only arrives on the barrier: the CTA copies it itself.
-template <typename T>
-__device__ __forceinline__ void issue_chunk(const ReduceArgs& a, const Chunk& c, unsigned char* stage,
-                                            uint64_t* bar) {
-  const char* src = chunk_src<T>(a, c);
-  const uint32_t bytes = static_cast<uint32_t>(chunk_elems<T>(a, c)) * sizeof(T);
-  if ((reinterpret_cast<uintptr_t>(src) & 15u) != 0) {
-    mbar_arrive(bar);
-    return;
+  __device__ __forceinline__ void load(const ReduceArgs& a, const Chunk& c) {
+    constexpr int EPV = Vec16<T>::N;
+    const T* src = reinterpret_cast<const T*>(a.logits) + static_cast<int64_t>(c.row) * a.row_stride +
+                   static_cast<int64_t>(c.lb) * kBlock;
+    ne = min(c.nbk * kBlock, a.V - c.lb * kBlock);
+    const bool vec_ok = (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+#pragma unroll
+    for (int j = 0; j < kRVecPerThread; ++j) {
+      const int v = threadIdx.x + j * kRThreads;
+      const int first = v * EPV;
+      if (vec_ok && first + EPV <= ne) {
+        w[j] = __ldcs(reinterpret_cast<const uint4*>(src) + v);  // streamed once: evict-first
+      } else {
+        // ragged tail or unaligned row: element loads, -inf beyond the row
+        alignas(16) T t[EPV];
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) t[e] = (first + e < ne) ? src[first + e] : neg_inf<T>();
+        w[j] = *reinterpret_cast<uint4*>(t);
+      }
+    }
   }
-  const uint32_t bulk = bytes & ~15u;
-  for (uint32_t o = bulk; o < bytes; o += sizeof(T))  // ragged tail (< 16 bytes), before the arrive
-    *reinterpret_cast<T*>(stage + o) = *reinterpret_cast<const T*>(src + o);
-  if (bulk > 0) {
-    mbar_arrive_expect_tx(bar, bulk);
-    bulk_load(stage, src, bulk, bar);
-  } else {
-    mbar_arrive(bar);
-  }
-}
+};
 
 template <typename T>
-__global__ void __launch_bounds__(kRThreads) logits_reduce_kernel(const ReduceArgs a) {
+__global__ void __launch_bounds__(kRThreads, kRCtasPerSm) logits_reduce_kernel(const ReduceArgs a) {
   using VT = Vec16<T>;
-  constexpr int EPV = VT::N;                                                  // elements per 16-byte vector
-  constexpr int VPB = kBlock / EPV;                                           // vectors per 64-block
-  constexpr int CH = kRStageBytes / (kBlock * static_cast<int>(sizeof(T)));  // blocks per chunk
+  constexpr int EPV = VT::N;                                        // elements per 16-byte vector
+  constexpr int VPB = kBlock / EPV;                                 // vectors per 64-block
+  constexpr int CH = kRVecPerThread * kRThreads / VPB;              // blocks per chunk
   constexpr int kValueBits = VT::kKeyBits;
   constexpr uint32_t kMask = kValueBits >= 32 ? 0xFFFFFFFFu : (0xFFFFFFFFu << (32 - kValueBits));
 
   extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char* ring = smem;
-  float* bmax = reinterpret_cast<float*>(smem + kRStages * kRStageBytes);
+  float* bmax = reinterpret_cast<float*>(smem);
   uint64_t* cand = reinterpret_cast<uint64_t*>(bmax + kRMaxPer);
   uint32_t* hist = reinterpret_cast<uint32_t*>(cand + kRCandCap);
   uint32_t* misc = hist + 256;  // [0] candidate count, [1..2] select broadcast
   float* red = reinterpret_cast<float*>(misc + 8);
-  uint64_t* red64 = reinterpret_cast<uint64_t*>(red + 32);
-  uint64_t* full = red64 + 32;  // kRStages mbarriers
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kRStages; ++s) mbar_init(&full[s], 1);
-    mbar_init_fence();
-  }
-  __syncthreads();
+  pdl_launch_dependents();  // the merge may be scheduled now; it waits for this grid's results
 
-  ChunkIter<CH> prod, cons;
-  if (threadIdx.x == 0) {
-    prod.init(a);
-    for (int s = 0; s < kRStages; ++s) {
-      const Chunk c = prod.next(a);
-      if (!c.valid) break;
-      issue_chunk<T>(a, c, ring + s * kRStageBytes, &full[s]);
-    }
-  }
-  cons.init(a);
-  Chunk cur = cons.next(a);
+  ChunkIter<CH> it;
+  it.init(a);
+  Chunk cur = it.next(a);
+  ChunkRegs<T> buf0, buf1;  // two register buffers with fixed roles per half of the unrolled loop
+  if (cur.valid) buf0.load(a, cur);
 
   const float L = kLog2e;
   float tm = -INFINITY, ts = 0.0f;  // this thread's running max / sum over the current piece
-  int piece_blocks = 0, piece_lb = 0;
-  for (uint32_t i = 0; cur.valid; ++i) {
-    const int s = static_cast<int>(i % kRStages);
-    unsigned char* stage = ring + s * kRStageBytes;
-    const Chunk nxt = cons.next(a);
-    if (piece_blocks == 0) piece_lb = cur.lb;
-    if (!mbar_wait(&full[s], (i / kRStages) & 1u)) {
-      if (threadIdx.x == 0) set_status(a.dev_status, LMH_DS_TIMEOUT);
-      return;
+  int piece_blocks = 0, piece_lb = 0, sel_rel = -1;
+  auto step = [&](ChunkRegs<T>& cb, ChunkRegs<T>& nb) {
+    const Chunk nxt = it.next(a);
+    if (nxt.valid) nb.load(a, nxt);  // in flight while this chunk is worked on
+    if (piece_blocks == 0) {
+      piece_lb = cur.lb;
+      sel_rel = a.sel ? a.sel[cur.row] : -1;
     }
-    const char* src = chunk_src<T>(a, cur);
-    const int ne = chunk_elems<T>(a, cur);
-    if ((reinterpret_cast<uintptr_t>(src) & 15u) != 0) {  // unaligned row start: copy it here
-      for (int e = threadIdx.x; e < ne; e += kRThreads)
-        reinterpret_cast<T*>(stage)[e] = reinterpret_cast<const T*>(src)[e];
-      __syncthreads();
-    }
+    const int ne = cb.ne;
+    const int rel0 = sel_rel - cur.lb * kBlock;  // selected token relative to this chunk
 
     // ---- block maxima + online (m, s) ----
-    const int nvec = cur.nbk * VPB;
-    for (int base = 0; base < nvec; base += kRThreads) {
-      const int v = base + threadIdx.x;
+#pragma unroll
+    for (int j = 0; j < kRVecPerThread; ++j) {
+      const int v = threadIdx.x + j * kRThreads;
       float x[EPV];
-      float vm = -INFINITY;
-      if (v < nvec) {
-        VT::load(stage + v * 16, x);
-        const int first = v * EPV;
-        if (first + EPV > ne) {
+      VT::load(&cb.w[j], x);
+      float vm = x[0];
 #pragma unroll
-          for (int j = 0; j < EPV; ++j)
-            if (first + j >= ne) x[j] = -INFINITY;
-        }
+      for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, x[e]);
+      if (vm > tm) {
+        ts = (tm == -INFINITY) ? 0.0f : ts * ex2_approx((tm - vm) * L);
+        tm = vm;
+      }
+      if (tm != -INFINITY) {
+        const float mL = tm * L;
 #pragma unroll
-        for (int j = 0; j < EPV; ++j) vm = fmaxf(vm, x[j]);
-        if (vm > tm) {
-          ts = (tm == -INFINITY) ? 0.0f : ts * ex2_approx((tm - vm) * L);
-          tm = vm;
-        }
-        if (tm != -INFINITY) {
-          const float mL = tm * L;
+        for (int e = 0; e < EPV; ++e) ts += ex2_approx(fmaf(x[e], L, -mL));
+      }
+      const unsigned r = static_cast<unsigned>(rel0 - v * EPV);
+      if (r < static_cast<unsigned>(EPV) && rel0 < ne) {  // the token is one of this chunk's real logits
+        float sv = 0.0f;
 #pragma unroll
-          for (int j = 0; j < EPV; ++j) ts += ex2_approx(fmaf(x[j], L, -mL));
-        }
+        for (int e = 0; e < EPV; ++e) sv = (static_cast<unsigned>(e) == r) ? x[e] : sv;
+        a.parts.sel_logit[cur.row] = sv;
       }
 #pragma unroll
       for (int o = VPB / 2; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
-      if (v < nvec && (threadIdx.x % VPB) == 0) bmax[piece_blocks + v / VPB] = vm;
-    }
-    if (threadIdx.x == 0 && a.sel) {
-      const int t = a.sel[cur.row] - cur.lb * kBlock;
-      if (t >= 0 && t < ne) a.parts.sel_logit[cur.row] = VT::at(stage, t);
+      if (v * EPV < cur.nbk * kBlock && (threadIdx.x % VPB) == 0) bmax[piece_blocks + v / VPB] = vm;
     }
     piece_blocks += cur.nbk;
-    __syncthreads();  // stage s is free; this chunk's block maxima are in place
-    if (threadIdx.x == 0) {
-      const Chunk c = prod.next(a);
-      if (c.valid) issue_chunk<T>(a, c, stage, &full[s]);
-    }
 
     const bool piece_end = !nxt.valid || nxt.row != cur.row || nxt.range != cur.range;
     if (piece_end) {
+      __syncthreads();  // every block maximum of the piece is in place
       // ---- finalize the row piece [piece_lb, piece_lb + piece_blocks) of row cur.row ----
       const int row = cur.row;
       const int slot = cur.range - static_cast<int>((static_cast<int64_t>(row) * a.nblk) / a.per);
@@ -379,6 +373,11 @@ __global__ void __launch_bounds__(kRThreads) logits_reduce_kernel(const ReduceAr
       piece_blocks = 0;
     }
     cur = nxt;
+  };
+  while (cur.valid) {
+    step(buf0, buf1);
+    if (!cur.valid) break;
+    step(buf1, buf0);
   }
 }
 
@@ -401,8 +400,7 @@ VocabSplit logits_reduce_split(int rows, int V, int k_max, int num_sms) {
 }
 
 static size_t reduce_smem_bytes() {
-  return static_cast<size_t>(kRStages) * kRStageBytes + kRMaxPer * 4 + kRCandCap * 8 + 256 * 4 + 8 * 4 + 32 * 4 +
-         32 * 8 + kRStages * 8;
+  return static_cast<size_t>(kRMaxPer) * 4 + kRCandCap * 8 + 256 * 4 + 8 * 4 + 32 * 4;
 }
 
 cudaError_t logits_reduce_setup() {
