@@ -257,7 +257,9 @@ int32_t lmh_version(void);
  * lmh_trace_enable(1) starts recording, lmh_trace_enable(0) stops.
  * lmh_trace_read waits for the recorded events, then reports the launches
  * and total milliseconds of the named kernel ("select_rows", "gather_rows",
- * "head_logprobs", "logits_reduce", "merge_partials") since the last reset.
+ * "head_logprobs", "merge_partials", "logits_reduce" (the streaming pass of
+ * lmh_logprobs_from_logits), "logits_select" (its per-row selection)) since
+ * the last reset.
  * lmh_trace_reset clears the totals.
  */
 lmh_status lmh_trace_enable(int32_t enable);

@@ -61,6 +61,7 @@ struct HeadCfg {
 };
 
 struct HeadArgs {
+  uint32_t a_bytes;  // bytes one A box brings per stage (rows of the box x 128)
   int rows, H, V, k_max;
   int m_tiles, n_tiles, splits, tiles_per_split, num_units;
   const int32_t* sel;
@@ -317,7 +318,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         if (valid) {  // a fresh ring: the empty barriers need no wait yet
           pm[j] = m_tile;
           pk[j] = kb;
-          mbar_arrive_expect_tx(&full[j], kStageBytesA + kStageBytesB);
+          mbar_arrive_expect_tx(&full[j], a.a_bytes + kStageBytesB);
           tma_load_2d(sB + j * kStageBytesB, &tmap_b, kb * kBK, n * kBN, &full[j]);
           advance();
           np = j + 1;
@@ -331,7 +332,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         const int s = it % S;
         const uint32_t ph = (it / S) & 1u;
         if (!wait_or_abort(&empty[s], ph ^ 1u, abort_flag, a.dev_status)) break;
-        mbar_arrive_expect_tx(&full[s], kStageBytesA + kStageBytesB);
+        mbar_arrive_expect_tx(&full[s], a.a_bytes + kStageBytesB);
         tma_load_2d(sA + s * kStageBytesA, &tmap_a, kb * kBK, m_tile * kBM, &full[s]);
         tma_load_2d(sB + s * kStageBytesB, &tmap_b, kb * kBK, n * kBN, &full[s]);
         advance();
@@ -644,12 +645,17 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
                         const int32_t* sel, const int32_t* row_k, int k_max, Partials parts, float* logits_out,
                         uint32_t* dev_status, cudaStream_t stream, bool pdl) {
   CUtensorMap ta, tb;
+  // With fewer than 128 rows (one row tile) the A box covers only the real
+  // rows (rounded up to 8); the stage's other rows keep stale data that only
+  // reaches accumulator rows the epilogue never reads.
+  const uint32_t a_box = rows < kBM ? static_cast<uint32_t>((rows + 7) / 8 * 8) : static_cast<uint32_t>(kBM);
   cudaError_t e = make_tmap(&ta, A, static_cast<uint64_t>(H), static_cast<uint64_t>(rows),
-                            static_cast<uint64_t>(a_stride), kBK, kBM);
+                            static_cast<uint64_t>(a_stride), kBK, a_box);
   if (e != cudaSuccess) return e;
   e = make_tmap(&tb, W, static_cast<uint64_t>(H), static_cast<uint64_t>(V), static_cast<uint64_t>(H), kBK, kBN);
   if (e != cudaSuccess) return e;
   HeadArgs a;
+  a.a_bytes = a_box * kBK * 2;
   a.rows = rows;
   a.H = H;
   a.V = V;

@@ -62,8 +62,8 @@ Partials carve_partials(void* base, int rows, int splits, int k_max) {
 // ---------------------------------------------------------------------------
 // kernel trace
 // ---------------------------------------------------------------------------
-static const char* const kTraceNames[kTraceCount] = {"select_rows", "gather_rows", "head_logprobs",
-                                                     "logits_reduce", "merge_partials"};
+static const char* const kTraceNames[kTraceCount] = {"select_rows",   "gather_rows",    "head_logprobs",
+                                                     "logits_reduce", "merge_partials", "logits_select"};
 
 struct TraceRecord {
   int kernel;
@@ -199,7 +199,7 @@ size_t lmh_workspace_bytes(int32_t rows, int32_t hidden, int32_t vocab, int32_t 
   }
   if (path == LMH_PATH_FROM_LOGITS) {
     const VocabSplit vs = logits_reduce_split(rows, vocab, k_max, sms);
-    return partials_bytes(rows, vs.splits, k_max);
+    return stream_partials_bytes(rows, vs);
   }
   return 0;
 }
@@ -272,21 +272,12 @@ lmh_status lmh_logprobs_from_logits(const void* logits, lmh_dtype dtype, int32_t
   if (device_setup(&sms) != cudaSuccess) return LMH_ERR_CUDA;
   const VocabSplit vs = logits_reduce_split(rows, V, k_max, sms);
   if (static_cast<int64_t>(rows) * vs.splits > INT32_MAX) return LMH_ERR_UNSUPPORTED;
-  const size_t need = partials_bytes(rows, vs.splits, k_max);
+  const size_t need = stream_partials_bytes(rows, vs);
   if (!workspace || !aligned(workspace, 256)) return LMH_ERR_INVALID_ARG;
   if (workspace_bytes < need) return LMH_ERR_WORKSPACE_TOO_SMALL;
-  const Partials parts = carve_partials(workspace, rows, vs.splits, k_max);
-  cudaError_t e;
-  {
-    Traced tr(kTraceReduce, stream);
-    e = launch_logits_reduce(logits, dtype, row_stride, rows, V, vs, sel_ids, row_k, k_max, parts, dev_status,
-                             stream);
-  }
-  if (e == cudaSuccess) {
-    Traced tr(kTraceMerge, stream);
-    e = launch_merge(rows, vs.splits, V, k_max, parts, sel_ids, row_k, lse, sel_logprob, topk_ids, topk_logprobs,
-                     dev_status, stream, vs.per, vs.nblk, /*pdl=*/true);
-  }
+  const Partials parts = carve_stream_partials(workspace, rows, vs);
+  const cudaError_t e = launch_logits_reduce(logits, dtype, row_stride, rows, V, vs, sel_ids, row_k, k_max, parts,
+                                             lse, sel_logprob, topk_ids, topk_logprobs, dev_status, stream);
   return from_cuda(e);
 }
 

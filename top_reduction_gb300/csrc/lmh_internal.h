@@ -34,6 +34,7 @@ struct Partials {
   float2* part_ms;
   unsigned long long* part_keys;
   float* sel_logit;
+  float* bmax;  // standalone reduction: block maxima [rows * nblk] (else unused)
 };
 
 size_t partials_bytes(int rows, int splits, int k_max);
@@ -50,9 +51,16 @@ cudaError_t launch_select_rows(const int32_t* cu, int num_seqs, int num_decode, 
                                int max_out, int32_t* row_idx, int32_t* logits_cu, uint32_t* dev_status,
                                cudaStream_t stream);
 
+// Workspace of the standalone reduction: part_ms [rows * splits], sel_logit
+// [rows], bmax [rows * nblk].
+size_t stream_partials_bytes(int rows, const VocabSplit& vs);
+Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs);
+
+// Stream kernel then per-row select kernel (the results go straight to the outputs).
 cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t row_stride, int rows, int V,
                                  VocabSplit split, const int32_t* sel, const int32_t* row_k, int k_max,
-                                 Partials parts, uint32_t* dev_status, cudaStream_t stream);
+                                 Partials parts, float* lse, float* sel_logprob, int32_t* topk_ids,
+                                 float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream);
 
 // Merges the partial slots of every row.  flat_per == 0: every one of the
 // `splits` slots is filled (head path); flat_per > 0: row r fills the slots of
@@ -106,7 +114,15 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 }
 
 // ---- tracing (lmh_api.cu) ----
-enum TraceKernel { kTraceSelect = 0, kTraceGather, kTraceHead, kTraceReduce, kTraceMerge, kTraceCount };
+enum TraceKernel {
+  kTraceSelect = 0,
+  kTraceGather,
+  kTraceHead,
+  kTraceReduce,
+  kTraceMerge,
+  kTraceLogitsSelect,
+  kTraceCount
+};
 void trace_begin(TraceKernel k, cudaStream_t s);
 void trace_end(TraceKernel k, cudaStream_t s);
 

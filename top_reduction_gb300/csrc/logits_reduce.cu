@@ -5,24 +5,23 @@
 // largest maxima, followed by an exact top-k among their entries; exact ties
 // by ascending token id.
 //
-// GB300 design: a persistent grid (two CTAs per SM) splits the flattened
-// (row, 64-block) space of the whole chunk into equal contiguous ranges, so
-// every CTA streams the same number of bytes whatever the row length.  A CTA
-// streams its range in chunks of 2048 coalesced 16-byte vectors (eight per
-// thread), issuing the next chunk's loads before it works on the current
-// one, and folds every vector into
-//   * the maxima of the 64-blocks (the 8 or 16 lanes of a block combine by
-//     shuffles) -- kept in shared memory for the current row piece;
-//   * a per-thread running max m and sum exp(x - m) (online rescaling).
-// When its range leaves a row (at most a few times per CTA) it finalizes that
-// row piece:
-//   1. (m, s) of the piece by a CTA reduction;
-//   2. tau = the k-th largest block maximum (radix select);
-//   3. candidates = entries >= tau of the blocks whose maximum is >= tau,
-//      re-read from L2; the true top-k of the piece lies among them, because
-//      the k blocks ranked first each hold an entry >= tau;
-//   4. the exact top-k of the candidates by key (value desc, id asc), by rank.
-// merge_partials.cu then combines the few pieces of each row.
+// GB300 design, two kernels:
+//   * logits_stream_kernel -- a persistent grid (two CTAs per SM) splits the
+//     flattened (row, 64-block) space of the whole chunk into equal
+//     contiguous ranges, so every CTA streams the same number of bytes
+//     whatever the row length.  A CTA streams its range in chunks of 2048
+//     coalesced 16-byte vectors (eight per thread), issuing the next chunk's
+//     loads before it works on the current one, and folds every vector into
+//     the maxima of the 64-blocks (the 8 or 16 lanes of a block combine by
+//     shuffles; written to the workspace) and a per-thread running max m and
+//     sum exp(x - m) (online rescaling; one (m, s) per row piece after a CTA
+//     reduction).  It also picks up the selected token's logit.
+//   * logits_select_kernel -- one CTA per row: lse from the row pieces'
+//     (m, s); tau = the k-th largest block maximum of the row (radix
+//     select); candidates = entries >= tau of the blocks whose maximum is
+//     >= tau, re-read from L2/HBM (the true top-k lies among them, because
+//     the k blocks ranked first each hold an entry >= tau); the exact top-k
+//     of the candidates by key (value desc, id asc), ordered by rank.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -210,7 +209,7 @@ struct ChunkRegs {
 };
 
 template <typename T>
-__global__ void __launch_bounds__(kRThreads, kRCtasPerSm) logits_reduce_kernel(const ReduceArgs a) {
+__global__ void __launch_bounds__(kRThreads, kRCtasPerSm) logits_stream_kernel(const ReduceArgs a) {
   using VT = Vec16<T>;
   constexpr int EPV = VT::N;                                        // elements per 16-byte vector
   constexpr int VPB = kBlock / EPV;                                 // vectors per 64-block
@@ -218,14 +217,8 @@ __global__ void __launch_bounds__(kRThreads, kRCtasPerSm) logits_reduce_kernel(c
   constexpr int kValueBits = VT::kKeyBits;
   constexpr uint32_t kMask = kValueBits >= 32 ? 0xFFFFFFFFu : (0xFFFFFFFFu << (32 - kValueBits));
 
-  extern __shared__ __align__(128) unsigned char smem[];
-  float* bmax = reinterpret_cast<float*>(smem);
-  uint64_t* cand = reinterpret_cast<uint64_t*>(bmax + kRMaxPer);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(cand + kRCandCap);
-  uint32_t* misc = hist + 256;  // [0] candidate count, [1..2] select broadcast
-  float* red = reinterpret_cast<float*>(misc + 8);
-
-  pdl_launch_dependents();  // the merge may be scheduled now; it waits for this grid's results
+  __shared__ float red[32];
+  pdl_launch_dependents();  // the select kernel may be scheduled now; it waits for this grid's results
 
   ChunkIter<CH> it;
   it.init(a);
@@ -235,14 +228,11 @@ __global__ void __launch_bounds__(kRThreads, kRCtasPerSm) logits_reduce_kernel(c
 
   const float L = kLog2e;
   float tm = -INFINITY, ts = 0.0f;  // this thread's running max / sum over the current piece
-  int piece_blocks = 0, piece_lb = 0, sel_rel = -1;
+  int piece_blocks = 0, sel_rel = -1;
   auto step = [&](ChunkRegs<T>& cb, ChunkRegs<T>& nb) {
     const Chunk nxt = it.next(a);
     if (nxt.valid) nb.load(a, nxt);  // in flight while this chunk is worked on
-    if (piece_blocks == 0) {
-      piece_lb = cur.lb;
-      sel_rel = a.sel ? a.sel[cur.row] : -1;
-    }
+    if (piece_blocks == 0) sel_rel = a.sel ? a.sel[cur.row] : -1;
     const int ne = cb.ne;
     const int rel0 = sel_rel - cur.lb * kBlock;  // selected token relative to this chunk
 
@@ -273,101 +263,18 @@ __global__ void __launch_bounds__(kRThreads, kRCtasPerSm) logits_reduce_kernel(c
       }
 #pragma unroll
       for (int o = VPB / 2; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
-      if (v * EPV < cur.nbk * kBlock && (threadIdx.x % VPB) == 0) bmax[piece_blocks + v / VPB] = vm;
+      if (v * EPV < cur.nbk * kBlock && (threadIdx.x % VPB) == 0)
+        a.parts.bmax[static_cast<int64_t>(cur.row) * a.nblk + cur.lb + v / VPB] = vm;
     }
     piece_blocks += cur.nbk;
 
     const bool piece_end = !nxt.valid || nxt.row != cur.row || nxt.range != cur.range;
     if (piece_end) {
-      __syncthreads();  // every block maximum of the piece is in place
-      // ---- finalize the row piece [piece_lb, piece_lb + piece_blocks) of row cur.row ----
       const int row = cur.row;
       const int slot = cur.range - static_cast<int>((static_cast<int64_t>(row) * a.nblk) / a.per);
-      const int64_t pidx = static_cast<int64_t>(row) * a.P + slot;
       const float M = block_max(tm, red);
       const float S = block_sum((tm == -INFINITY) ? 0.0f : ts * expf(tm - M), red);
-      if (threadIdx.x == 0) {
-        a.parts.part_ms[pidx] = make_float2(M, M == -INFINITY ? 0.0f : S);
-        misc[0] = 0;
-      }
-      int k = a.k_max;
-      if (a.row_k) k = min(max(a.row_k[row], 0), a.k_max);
-      if (k > 0) {
-        const int nbp = piece_blocks;
-        const int e_lo = piece_lb * kBlock;                    // first element of the piece
-        const int e_hi = min((piece_lb + nbp) * kBlock, a.V);  // one past its last element
-        const char* rowp =
-            a.logits + static_cast<int64_t>(row) * a.row_stride * static_cast<int64_t>(sizeof(T));
-        uint32_t thr = 0;  // ord(tau) restricted to the top kValueBits bits; 0 keeps every entry
-        if (nbp > k) {
-          int above;
-          const uint64_t T64 = cta_radix_select(
-              [&](int b, uint64_t* key) {
-                *key = static_cast<uint64_t>(f32_ord(bmax[b])) << 32;
-                return true;
-              },
-              nbp, k, kValueBits, hist, misc + 1, &above);
-          thr = static_cast<uint32_t>(T64 >> 32);
-        }
-        auto in_set = [&](int i, uint64_t* key) -> bool {
-          const int b = i / kBlock;
-          if ((f32_ord(bmax[b]) & kMask) < thr) return false;
-          const int e = e_lo + i;
-          if (e >= e_hi) return false;
-          const float x = VT::at(rowp, e);
-          if ((f32_ord(x) & kMask) < thr) return false;
-          *key = make_key(x, e);
-          return true;
-        };
-        __syncthreads();
-        // candidates: one warp per kept block, its entries re-read (from L2)
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        for (int b = warp; b < nbp; b += kRThreads / 32) {
-          if ((f32_ord(bmax[b]) & kMask) < thr) continue;  // warp-uniform: block pruned
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint64_t key = 0;
-            const bool in = in_set(b * kBlock + h * 32 + lane, &key);
-            const unsigned bal = __ballot_sync(0xffffffffu, in);
-            uint32_t basepos = 0;
-            if (lane == 0 && bal) basepos = atomicAdd(&misc[0], __popc(bal));
-            basepos = __shfl_sync(0xffffffffu, basepos, 0);
-            if (in) {
-              const uint32_t pos = basepos + __popc(bal & ((1u << lane) - 1u));
-              if (pos < kRCandCap) cand[pos] = key;
-            }
-          }
-        }
-        __syncthreads();
-        int cnt = static_cast<int>(misc[0]);
-        if (cnt > kRCandCap) {
-          // many exact ties at tau: exact radix select over the candidate set, then keep the k best
-          int above;
-          const uint64_t T64 = cta_radix_select(in_set, nbp * kBlock, k, 64, hist, misc + 1, &above);
-          __syncthreads();
-          if (threadIdx.x == 0) misc[0] = 0;
-          __syncthreads();
-          for (int i = threadIdx.x; i < nbp * kBlock; i += kRThreads) {
-            uint64_t key = 0;
-            if (in_set(i, &key) && key >= T64) {
-              const uint32_t pos = atomicAdd(&misc[0], 1u);
-              if (pos < kRCandCap) cand[pos] = key;
-            }
-          }
-          __syncthreads();
-          cnt = min(k, static_cast<int>(misc[0]));
-        }
-        // exact order by rank (keys are unique)
-        unsigned long long* out = a.parts.part_keys + pidx * a.k_max;
-        for (int t = threadIdx.x; t < cnt; t += kRThreads) {
-          const uint64_t key = cand[t];
-          int rank = 0;
-          for (int j = 0; j < cnt; ++j) rank += cand[j] > key;
-          if (rank < k) out[rank] = key;
-        }
-        for (int j = cnt + threadIdx.x; j < k; j += kRThreads) out[j] = 0ull;
-      }
-      __syncthreads();  // cand / misc / bmax are reused by the next piece
+      if (threadIdx.x == 0) a.parts.part_ms[static_cast<int64_t>(row) * a.P + slot] = make_float2(M, M == -INFINITY ? 0.0f : S);
       tm = -INFINITY;
       ts = 0.0f;
       piece_blocks = 0;
@@ -378,6 +285,162 @@ __global__ void __launch_bounds__(kRThreads, kRCtasPerSm) logits_reduce_kernel(c
     step(buf0, buf1);
     if (!cur.valid) break;
     step(buf1, buf0);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// per-row selection
+// ---------------------------------------------------------------------------
+constexpr int kSThreads = 256;
+constexpr int kSKeptCap = 1024;  // kept blocks held in shared memory
+constexpr int kSCandCap = 512;   // candidate keys held in shared memory
+constexpr int kSStageBlocks = 16384;  // block maxima staged in shared memory (V <= 1,048,576)
+
+template <typename T>
+__global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceArgs a, float* lse_out,
+                                                                  float* sel_logprob, int32_t* topk_ids,
+                                                                  float* topk_logprobs) {
+  using VT = Vec16<T>;
+  constexpr int kValueBits = VT::kKeyBits;
+  constexpr uint32_t kMask = kValueBits >= 32 ? 0xFFFFFFFFu : (0xFFFFFFFFu << (32 - kValueBits));
+  __shared__ uint64_t cand[kSCandCap];
+  __shared__ int kept[kSKeptCap];
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t misc[4];  // [0] candidates, [1..2] select broadcast, [3] kept blocks
+  __shared__ float red[32];
+  pdl_wait();  // the block maxima and (m, s) come from the stream kernel just before
+
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x;
+  // ---- lse over the row's pieces ----
+  const int64_t b0 = static_cast<int64_t>(row) * a.nblk;
+  const int nslots = static_cast<int>((b0 + a.nblk - 1) / a.per - b0 / a.per) + 1;
+  const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.P;
+  float tm = -INFINITY, ts = 0.0f;
+  for (int j = tid; j < nslots; j += kSThreads) {
+    const float2 p = ms[j];
+    if (p.x > tm) {
+      ts = (tm == -INFINITY) ? 0.0f : ts * expf(tm - p.x);
+      tm = p.x;
+    }
+    if (p.x != -INFINITY) ts += p.y * expf(p.x - tm);
+  }
+  const float M = block_max(tm, red);
+  const float S = block_sum((tm == -INFINITY) ? 0.0f : ts * expf(tm - M), red);
+  const float lse = (M == -INFINITY) ? -INFINITY : M + logf(S);
+  if (tid == 0) {
+    lse_out[row] = lse;
+    if (a.sel) {
+      const int t = a.sel[row];
+      float v = __int_as_float(0x7fc00000);  // NaN: no selected token / out of range
+      if (t >= 0 && t < a.V)
+        v = a.parts.sel_logit[row] - lse;
+      else if (t != -1)
+        set_status(a.dev_status, LMH_DS_SEL_OUT_OF_RANGE);
+      sel_logprob[row] = v;
+    }
+    misc[0] = 0;
+    misc[3] = 0;
+  }
+  if (a.k_max == 0) return;
+  int k = a.k_max;
+  if (a.row_k) k = min(max(a.row_k[row], 0), a.k_max);
+  int32_t* out_ids = topk_ids + static_cast<int64_t>(row) * a.k_max;
+  float* out_lp = topk_logprobs + static_cast<int64_t>(row) * a.k_max;
+  if (k == 0) {
+    for (int r = tid; r < a.k_max; r += kSThreads) {
+      out_ids[r] = -1;
+      out_lp[r] = -INFINITY;
+    }
+    return;
+  }
+
+  // ---- tau: the k-th largest block maximum of the row ----
+  // The row's block maxima are staged in shared memory (one coalesced round)
+  // when they fit; otherwise they are read from global memory (L2).
+  extern __shared__ float sbm[];
+  const int nb = a.nblk;
+  const float* bm = a.parts.bmax + b0;
+  if (nb <= kSStageBlocks) {
+    for (int b = tid; b < nb; b += kSThreads) sbm[b] = bm[b];
+    __syncthreads();
+    bm = sbm;
+  }
+  uint32_t thr = 0;  // ord(tau) restricted to the top kValueBits bits; 0 keeps every entry
+  if (nb > k) {
+    int above;
+    const uint64_t T64 = cta_radix_select(
+        [&](int b, uint64_t* key) {
+          *key = static_cast<uint64_t>(f32_ord(bm[b])) << 32;
+          return true;
+        },
+        nb, k, kValueBits, hist, misc + 1, &above);
+    thr = static_cast<uint32_t>(T64 >> 32);
+  }
+  __syncthreads();
+  // ---- kept blocks (order is irrelevant: candidates are ranked below) ----
+  for (int b = tid; b < nb; b += kSThreads)
+    if ((f32_ord(bm[b]) & kMask) >= thr) {
+      const uint32_t pos = atomicAdd(&misc[3], 1u);
+      if (pos < kSKeptCap) kept[pos] = b;
+    }
+  __syncthreads();
+  const int nkept = static_cast<int>(misc[3]);
+  const T* rowp = reinterpret_cast<const T*>(a.logits) + static_cast<int64_t>(row) * a.row_stride;
+  auto in_set = [&](int i, uint64_t* key) -> bool {  // i over the whole row (fallback)
+    if ((f32_ord(bm[i / kBlock]) & kMask) < thr || i >= a.V) return false;
+    const float x = VT::at(rowp, i);
+    if ((f32_ord(x) & kMask) < thr) return false;
+    *key = make_key(x, i);
+    return true;
+  };
+  int cnt;
+  if (nkept <= kSKeptCap) {
+    // gather the kept blocks' entries >= tau: every load of the CTA in one round
+    const int n_el = nkept * kBlock;
+    for (int i = tid; i < n_el; i += kSThreads) {
+      const int e = kept[i / kBlock] * kBlock + (i % kBlock);
+      if (e >= a.V) continue;
+      const float x = VT::at(rowp, e);
+      if ((f32_ord(x) & kMask) < thr) continue;
+      const uint32_t pos = atomicAdd(&misc[0], 1u);
+      if (pos < kSCandCap) cand[pos] = make_key(x, e);
+    }
+    __syncthreads();
+    cnt = static_cast<int>(misc[0]);
+  } else {
+    cnt = kSCandCap + 1;  // too many ties at tau for the lists: take the exact path
+  }
+  if (cnt > kSCandCap) {
+    int above;
+    const int n_items = nb * kBlock;
+    const uint64_t T64 = cta_radix_select(in_set, n_items, k, 64, hist, misc + 1, &above);
+    __syncthreads();
+    if (tid == 0) misc[0] = 0;
+    __syncthreads();
+    for (int i = tid; i < n_items; i += kSThreads) {
+      uint64_t key = 0;
+      if (in_set(i, &key) && key >= T64) {
+        const uint32_t pos = atomicAdd(&misc[0], 1u);  // exactly k of them
+        if (pos < kSCandCap) cand[pos] = key;
+      }
+    }
+    __syncthreads();
+    cnt = min(k, static_cast<int>(misc[0]));
+  }
+  // ---- exact order by rank (keys are unique) ----
+  for (int t = tid; t < cnt; t += kSThreads) {
+    const uint64_t key = cand[t];
+    int rank = 0;
+    for (int j = 0; j < cnt; ++j) rank += cand[j] > key;
+    if (rank < k) {
+      out_ids[rank] = key_id(key);
+      out_lp[rank] = key_value(key) - lse;
+    }
+  }
+  for (int r = min(cnt, k) + tid; r < a.k_max; r += kSThreads) {  // ranks without a candidate, and ranks >= k
+    out_ids[r] = -1;
+    out_lp[r] = -INFINITY;
   }
 }
 
@@ -399,24 +462,58 @@ VocabSplit logits_reduce_split(int rows, int V, int k_max, int num_sms) {
   return vs;
 }
 
-static size_t reduce_smem_bytes() {
-  return static_cast<size_t>(kRMaxPer) * 4 + kRCandCap * 8 + 256 * 4 + 8 * 4 + 32 * 4;
+cudaError_t logits_reduce_setup() {
+  const int bytes = kSStageBlocks * static_cast<int>(sizeof(float));
+  cudaError_t e =
+      cudaFuncSetAttribute(logits_select_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(logits_select_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(logits_select_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return e;
 }
 
-cudaError_t logits_reduce_setup() {
-  const int bytes = static_cast<int>(reduce_smem_bytes());
-  cudaError_t e = cudaFuncSetAttribute(logits_reduce_kernel<__nv_bfloat16>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(logits_reduce_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(logits_reduce_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+size_t stream_partials_bytes(int rows, const VocabSplit& vs) {
+  auto al = [](size_t n) { return (n + 255) & ~static_cast<size_t>(255); };
+  return al(static_cast<size_t>(rows) * vs.splits * 8) + al(static_cast<size_t>(rows) * 4) +
+         al(static_cast<size_t>(rows) * vs.nblk * 4);
+}
+
+Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs) {
+  auto al = [](size_t n) { return (n + 255) & ~static_cast<size_t>(255); };
+  char* p = static_cast<char*>(base);
+  Partials out;
+  out.part_ms = reinterpret_cast<float2*>(p);
+  p += al(static_cast<size_t>(rows) * vs.splits * 8);
+  out.sel_logit = reinterpret_cast<float*>(p);
+  p += al(static_cast<size_t>(rows) * 4);
+  out.bmax = reinterpret_cast<float*>(p);
+  out.part_keys = nullptr;
+  return out;
+}
+
+template <typename T>
+static cudaError_t launch_both(const ReduceArgs& a, const VocabSplit& split, float* lse, float* sel_logprob,
+                               int32_t* topk_ids, float* topk_logprobs, cudaStream_t stream, TraceKernel tk_select) {
+  cudaError_t e;
+  {
+    trace_begin(kTraceReduce, stream);
+    e = launch_kernel(logits_stream_kernel<T>, dim3(split.grid), dim3(kRThreads), 0, stream, false, a);
+    trace_end(kTraceReduce, stream);
+  }
+  if (e != cudaSuccess) return e;
+  trace_begin(tk_select, stream);
+  const size_t smem = static_cast<size_t>(min(a.nblk, kSStageBlocks)) * sizeof(float);
+  e = launch_kernel(logits_select_kernel<T>, dim3(a.rows), dim3(kSThreads), smem, stream, true, a, lse, sel_logprob,
+                    topk_ids, topk_logprobs);
+  trace_end(tk_select, stream);
   return e;
 }
 
 cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t row_stride, int rows, int V,
                                  VocabSplit split, const int32_t* sel, const int32_t* row_k, int k_max,
-                                 Partials parts, uint32_t* dev_status, cudaStream_t stream) {
+                                 Partials parts, float* lse, float* sel_logprob, int32_t* topk_ids,
+                                 float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream) {
   ReduceArgs a;
   a.logits = static_cast<const char*>(logits);
   a.row_stride = row_stride;
@@ -432,20 +529,14 @@ cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t ro
   a.k_max = k_max;
   a.parts = parts;
   a.dev_status = dev_status;
-  const dim3 grid(static_cast<unsigned>(split.grid));
-  const size_t smem = reduce_smem_bytes();
   switch (dtype) {
     case LMH_BF16:
-      logits_reduce_kernel<__nv_bfloat16><<<grid, kRThreads, smem, stream>>>(a);
-      break;
+      return launch_both<__nv_bfloat16>(a, split, lse, sel_logprob, topk_ids, topk_logprobs, stream, kTraceLogitsSelect);
     case LMH_F16:
-      logits_reduce_kernel<__half><<<grid, kRThreads, smem, stream>>>(a);
-      break;
+      return launch_both<__half>(a, split, lse, sel_logprob, topk_ids, topk_logprobs, stream, kTraceLogitsSelect);
     default:
-      logits_reduce_kernel<float><<<grid, kRThreads, smem, stream>>>(a);
-      break;
+      return launch_both<float>(a, split, lse, sel_logprob, topk_ids, topk_logprobs, stream, kTraceLogitsSelect);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace lmh

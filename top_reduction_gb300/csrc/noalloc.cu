@@ -10,7 +10,7 @@
 //   * latency-critical loops where cudaMalloc / cudaFree would synchronise
 //     the device.
 // This variant runs the same two kernels as lmh_logprobs_from_logits
-// (logits_reduce + merge_partials) but keeps their per-chunk partials in a
+// (logits stream + per-row select) but keeps their intermediate results in a
 // fixed array in the library's own device memory, so the call allocates
 // nothing.
 //
@@ -57,7 +57,6 @@ cudaError_t static_setup(void** ptr, int* num_sms) {
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = logits_reduce_setup();
-    if (e == cudaSuccess) e = merge_setup();
     void* p = nullptr;
     if (e == cudaSuccess) e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess) return e;
@@ -94,12 +93,9 @@ extern "C" lmh_status lmh_logprobs_from_logits_static(const void* logits, lmh_dt
   if (static_setup(&scratch, &sms) != cudaSuccess) return LMH_ERR_CUDA;
   const VocabSplit vs = logits_reduce_split(rows, V, k_max, sms);
   if (static_cast<int64_t>(rows) * vs.splits > INT32_MAX) return LMH_ERR_UNSUPPORTED;
-  if (partials_bytes(rows, vs.splits, k_max) > kStaticScratchBytes) return LMH_ERR_WORKSPACE_TOO_SMALL;
-  const Partials parts = carve_partials(scratch, rows, vs.splits, k_max);
-  cudaError_t e = launch_logits_reduce(logits, dtype, row_stride, rows, V, vs, sel_ids, row_k, k_max, parts,
-                                       dev_status, stream);
-  if (e == cudaSuccess)
-    e = launch_merge(rows, vs.splits, V, k_max, parts, sel_ids, row_k, lse, sel_logprob, topk_ids, topk_logprobs,
-                     dev_status, stream, vs.per, vs.nblk);
+  if (stream_partials_bytes(rows, vs) > kStaticScratchBytes) return LMH_ERR_WORKSPACE_TOO_SMALL;
+  const Partials parts = carve_stream_partials(scratch, rows, vs);
+  const cudaError_t e = launch_logits_reduce(logits, dtype, row_stride, rows, V, vs, sel_ids, row_k, k_max, parts,
+                                             lse, sel_logprob, topk_ids, topk_logprobs, dev_status, stream);
   return e == cudaSuccess ? LMH_OK : LMH_ERR_CUDA;
 }

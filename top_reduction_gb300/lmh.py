@@ -220,7 +220,8 @@ def logprobs_from_logits(logits, sel=None, row_k=None, k_max=0, workspace=None, 
 # kernel trace
 # ---------------------------------------------------------------------------
 
-TRACE_KERNELS = ("select_rows", "gather_rows", "head_logprobs", "logits_reduce", "merge_partials")
+TRACE_KERNELS = ("select_rows", "gather_rows", "head_logprobs", "logits_reduce", "merge_partials",
+                 "logits_select")
 
 
 def trace_enable(on=True):
