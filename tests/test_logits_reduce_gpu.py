@@ -147,3 +147,24 @@ def test_no_selected_tokens(lmh):
     o, st = gpu_run(lmh, x.cuda(), None, 3)
     assert st == 0 and o["sel_logprob"] is None
     check_from_logits(o, oracle_ref(x, None, 3), 3)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+def test_layout_paths(lmh, dtype):
+    """Row lengths and offsets on both sides of the 16-byte alignment the bulk-copy path needs.
+
+    Rows whose start and length are multiples of 16 bytes are streamed through
+    shared memory; the others are read with vector or element loads.  Partial
+    last blocks, f32 blocks split over two threads and a start one element
+    past the alignment are all covered.
+    """
+    g = torch.Generator().manual_seed(11)
+    for V, offset in ((40, 0), (1000, 0), (1001, 0), (2056, 0), (3000, 1), (5000, 0)):
+        wide = (torch.randn(9, V + 24, generator=g) * 2).to(dtype)
+        wide[2, offset + 5:offset + 25] = wide[2, offset + 3]      # ties inside a block and across blocks
+        x = wide[:, offset:offset + V]
+        sel = torch.randint(-1, V, (9,), generator=g, dtype=torch.int32)
+        k = min(20, V)
+        o, st = gpu_run(lmh, wide.cuda()[:, offset:offset + V], sel, k)
+        assert st == 0
+        check_from_logits(o, oracle_ref(x.contiguous(), sel, k), k, what="%s V=%d offset=%d" % (dtype, V, offset))

@@ -114,6 +114,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
+// Wait on an mbarrier unless the CTA has aborted (another thread gave up
+// first); on a timeout, mark the abort and report LMH_DS_TIMEOUT.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              uint32_t* dev_status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      set_status(dev_status, LMH_DS_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
 // One-dimensional bulk copy global -> shared, completing on `bar`.
 // dst and src 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {

@@ -147,22 +147,6 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Wait on an mbarrier unless the CTA has aborted; on timeout mark the abort.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                              uint32_t* dev_status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      *abort_flag = 1;
-      set_status(dev_status, LMH_DS_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
-
 // ---------------------------------------------------------------------------
 // per-row sorted candidate list in shared memory (slot-major: list[j*128+r])
 // ---------------------------------------------------------------------------

@@ -19,11 +19,12 @@ constexpr int kBlock = 64;  // logits per prefilter block (MTPLX PR #532, "Chang
 // `splits` ranges, which is the number of partial slots per row.  The ranges
 // a row meets are [(row*nblk)/per, (row*nblk + nblk - 1)/per].
 struct VocabSplit {
-  int splits;    // partial slots per row
+  int splits;    // row pieces per row, at most
   int per;       // 64-blocks per range
   int n_ranges;  // ranges in total
-  int grid;      // persistent CTAs
+  int grid;      // persistent CTAs of the register-path stream kernel (two per SM)
   int nblk;      // 64-blocks per row
+  int sms;       // SMs of the device (persistent CTAs of the TMA-path stream kernel)
 };
 
 // Per-(row, split) partial results, laid out in the caller's workspace:
@@ -51,8 +52,9 @@ cudaError_t launch_select_rows(const int32_t* cu, int num_seqs, int num_decode, 
                                int max_out, int32_t* row_idx, int32_t* logits_cu, uint32_t* dev_status,
                                cudaStream_t stream);
 
-// Workspace of the standalone reduction: part_ms [rows * splits], sel_logit
-// [rows], bmax [rows * nblk].
+// Workspace of the standalone reduction: part_ms [rows * splits * 8] (one
+// (m, s) pair per consumer warp and row piece), sel_logit [rows], bmax
+// [rows * nblk].
 size_t stream_partials_bytes(int rows, const VocabSplit& vs);
 Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs);
 

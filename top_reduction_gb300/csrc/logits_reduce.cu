@@ -6,22 +6,28 @@
 // by ascending token id.
 //
 // GB300 design, two kernels:
-//   * logits_stream_kernel -- a persistent grid (two CTAs per SM) splits the
+//   * a stream kernel reads every logit once.  A persistent grid splits the
 //     flattened (row, 64-block) space of the whole chunk into equal
 //     contiguous ranges, so every CTA streams the same number of bytes
-//     whatever the row length.  A CTA streams its range in chunks of 2048
-//     coalesced 16-byte vectors (eight per thread), issuing the next chunk's
-//     loads before it works on the current one, and folds every vector into
-//     the maxima of the 64-blocks (the 8 or 16 lanes of a block combine by
-//     shuffles; written to the workspace) and a per-thread running max m and
-//     sum exp(x - m) (online rescaling; one (m, s) per row piece after a CTA
-//     reduction).  It also picks up the selected token's logit.
-//   * logits_select_kernel -- one CTA per row: lse from the row pieces'
-//     (m, s); tau = the k-th largest block maximum of the row (radix
-//     select); candidates = entries >= tau of the blocks whose maximum is
-//     >= tau, re-read from L2/HBM (the true top-k lies among them, because
-//     the k blocks ranked first each hold an entry >= tau); the exact top-k
-//     of the candidates by key (value desc, id asc), ordered by rank.
+//     whatever the row length.  For every 64-block it writes the block's
+//     maximum to the workspace, and it folds the logits into running
+//     (max m, sum exp(x - m)) pairs, one pair per warp and row piece.  It
+//     also picks up the selected token's logit.
+//       - logits_stream_tma_kernel (rows and the row length 16-byte
+//         aligned): one producer lane streams 32 KB chunks of one row into a
+//         ring of shared-memory stages with bulk copies (cp.async.bulk,
+//         completion on mbarriers); eight consumer warps read them, each
+//         thread owning 128 contiguous bytes (one bf16/f16 block, half an f32
+//         block), so a block's maximum needs no exchange between lanes.
+//       - logits_stream_regs_kernel (any element-aligned layout): every thread
+//         loads 16-byte vectors (or elements at unaligned rows) straight into
+//         registers, two chunks in flight; the lanes of a block combine their
+//         maxima by shuffles.
+//   * logits_select_kernel -- one CTA per row: lse from the row's (m, s)
+//     pairs; a lower bound t on the row's k-th largest logit from the block
+//     maxima; candidates = entries >= t of the blocks whose maximum is >= t,
+//     re-read from memory; their exact top-k by key (value desc, id asc),
+//     ordered by rank.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -30,12 +36,23 @@
 
 namespace lmh {
 
+// register-path stream kernel
 constexpr int kRThreads = 256;
 constexpr int kRVecPerThread = 8;  // 16-byte vectors per thread per chunk
-constexpr int kRMaxPer = 4096;     // blocks per range: bounds the block-max buffer
-constexpr int kRMinPer = 32;       // >= 2048 logits per range
-constexpr int kRCandCap = 512;
 constexpr int kRCtasPerSm = 2;
+// ranges
+constexpr int kRMaxPer = 4096;  // blocks per range, at most
+constexpr int kRMinPer = 32;    // >= 2048 logits per range
+// TMA-path stream kernel
+constexpr int kTConsumerWarps = 8;
+constexpr int kTConsumers = kTConsumerWarps * 32;
+constexpr int kTThreads = kTConsumers + 32;  // + one producer warp
+constexpr int kTChunkBytes = kTConsumers * 128;  // 128 contiguous bytes per consumer thread
+constexpr int kTStages = 6;
+constexpr int kTDescBytes = 32;
+constexpr int kTSmem = kTStages * kTChunkBytes + kTStages * kTDescBytes + 2 * kTStages * 8 + 16;
+// (m, s) slots reserved per row piece: one per consumer warp of the TMA path
+constexpr int kSlotsPerPiece = kTConsumerWarps;
 
 template <typename T>
 struct Vec16;  // 16-byte vector of T widened to fp32
@@ -43,15 +60,32 @@ struct Vec16;  // 16-byte vector of T widened to fp32
 template <>
 struct Vec16<__nv_bfloat16> {
   static constexpr int N = 8;
-  static constexpr int kKeyBits = 16;  // a bf16 value is exact in the top 16 bits of its fp32 key
-  __device__ __forceinline__ static void load(const void* p, float* x) {
-    const uint4 w = *reinterpret_cast<const uint4*>(p);
+  static constexpr uint32_t kNegInfWord = 0xFF80FF80u;  // two bf16 -inf
+  __device__ __forceinline__ static void load(const void* p, float* x) { unpack(*reinterpret_cast<const uint4*>(p), x); }
+  __device__ __forceinline__ static void unpack(const uint4 w, float* x) {
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       x[2 * i] = __uint_as_float(u[i] << 16);
       x[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
     }
+  }
+  // maximum of 8 vectors, pairwise on packed bf16x2 (exact)
+  __device__ __forceinline__ static float max8(const uint4* w) {
+    __nv_bfloat162 m[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t* a = reinterpret_cast<const uint32_t*>(&w[2 * i]);
+      const uint32_t* b = reinterpret_cast<const uint32_t*>(&w[2 * i + 1]);
+      __nv_bfloat162 t0 = __hmax2(as2(a[0]), as2(a[1])), t1 = __hmax2(as2(a[2]), as2(a[3]));
+      __nv_bfloat162 t2 = __hmax2(as2(b[0]), as2(b[1])), t3 = __hmax2(as2(b[2]), as2(b[3]));
+      m[i] = __hmax2(__hmax2(t0, t1), __hmax2(t2, t3));
+    }
+    const __nv_bfloat162 r = __hmax2(__hmax2(m[0], m[1]), __hmax2(m[2], m[3]));
+    return fmaxf(__low2float(r), __high2float(r));
+  }
+  __device__ __forceinline__ static __nv_bfloat162 as2(uint32_t u) {
+    return *reinterpret_cast<const __nv_bfloat162*>(&u);
   }
   __device__ __forceinline__ static float at(const void* base, int64_t i) {
     const uint16_t b = reinterpret_cast<const uint16_t*>(base)[i];
@@ -62,9 +96,9 @@ struct Vec16<__nv_bfloat16> {
 template <>
 struct Vec16<__half> {
   static constexpr int N = 8;
-  static constexpr int kKeyBits = 32;
-  __device__ __forceinline__ static void load(const void* p, float* x) {
-    const uint4 w = *reinterpret_cast<const uint4*>(p);
+  static constexpr uint32_t kNegInfWord = 0xFC00FC00u;  // two f16 -inf
+  __device__ __forceinline__ static void load(const void* p, float* x) { unpack(*reinterpret_cast<const uint4*>(p), x); }
+  __device__ __forceinline__ static void unpack(const uint4 w, float* x) {
     const __half2* h = reinterpret_cast<const __half2*>(&w);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -72,6 +106,18 @@ struct Vec16<__half> {
       x[2 * i] = f.x;
       x[2 * i + 1] = f.y;
     }
+  }
+  __device__ __forceinline__ static float max8(const uint4* w) {
+    const __half2* h = reinterpret_cast<const __half2*>(w);
+    __half2 m[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2* p = h + 8 * i;
+      m[i] = __hmax2(__hmax2(__hmax2(p[0], p[1]), __hmax2(p[2], p[3])),
+                     __hmax2(__hmax2(p[4], p[5]), __hmax2(p[6], p[7])));
+    }
+    const __half2 r = __hmax2(__hmax2(m[0], m[1]), __hmax2(m[2], m[3]));
+    return fmaxf(__low2float(r), __high2float(r));
   }
   __device__ __forceinline__ static float at(const void* base, int64_t i) {
     return __half2float(reinterpret_cast<const __half*>(base)[i]);
@@ -81,13 +127,23 @@ struct Vec16<__half> {
 template <>
 struct Vec16<float> {
   static constexpr int N = 4;
-  static constexpr int kKeyBits = 32;
-  __device__ __forceinline__ static void load(const void* p, float* x) {
-    const float4 w = *reinterpret_cast<const float4*>(p);
-    x[0] = w.x;
-    x[1] = w.y;
-    x[2] = w.z;
-    x[3] = w.w;
+  static constexpr uint32_t kNegInfWord = 0xFF800000u;
+  __device__ __forceinline__ static void load(const void* p, float* x) { unpack(*reinterpret_cast<const uint4*>(p), x); }
+  __device__ __forceinline__ static void unpack(const uint4 w, float* x) {
+    x[0] = __uint_as_float(w.x);
+    x[1] = __uint_as_float(w.y);
+    x[2] = __uint_as_float(w.z);
+    x[3] = __uint_as_float(w.w);
+  }
+  __device__ __forceinline__ static float max8(const uint4* w) {
+    float m[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 a = w[2 * i], b = w[2 * i + 1];
+      m[i] = fmaxf(fmaxf(fmaxf(__uint_as_float(a.x), __uint_as_float(a.y)), fmaxf(__uint_as_float(a.z), __uint_as_float(a.w))),
+                   fmaxf(fmaxf(__uint_as_float(b.x), __uint_as_float(b.y)), fmaxf(__uint_as_float(b.z), __uint_as_float(b.w))));
+    }
+    return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
   }
   __device__ __forceinline__ static float at(const void* base, int64_t i) {
     return reinterpret_cast<const float*>(base)[i];
@@ -116,7 +172,9 @@ struct ReduceArgs {
   int64_t nb_total;    // rows * nblk
   int per;             // blocks per range
   int n_ranges;
-  int P;               // partial slots per row
+  int P;               // (m, s) slots per row: kSlotsPerPiece per row piece
+  int W;               // slots a row piece fills: kTConsumerWarps (TMA path) or 1
+  bool vec_ok;         // rows and the row length are 16-byte aligned
   const int32_t* sel;
   const int32_t* row_k;
   int k_max;
@@ -176,7 +234,163 @@ struct ChunkIter {
     }
     return c;
   }
+  // The chunk just returned by next() was the last of its row piece.
+  __device__ bool piece_ended() const { return left == 0 || lb == 0; }
 };
+
+// Index of a row piece's first (m, s) slot: row * P + (range - first range of the row) * W.
+__device__ __forceinline__ int64_t piece_slot(const ReduceArgs& a, int row, int range) {
+  const int first = static_cast<int>((static_cast<int64_t>(row) * a.nblk) / a.per);
+  return static_cast<int64_t>(row) * a.P + static_cast<int64_t>(range - first) * a.W;
+}
+
+// ---------------------------------------------------------------------------
+// stream kernel, TMA path
+// ---------------------------------------------------------------------------
+struct StreamDesc {  // one per stage, written by the producer before the copy is issued
+  int row;           // < 0: no more chunks
+  int lb;            // first 64-block of the chunk within the row
+  int nbk;           // blocks in the chunk
+  int ne;            // real logits in the chunk (the copied ones)
+  int64_t slot;      // first (m, s) slot of the chunk's row piece
+  int sel_rel;       // selected token relative to the chunk's first logit
+  int piece_end;     // the chunk is the last of its row piece
+};
+static_assert(sizeof(StreamDesc) <= kTDescBytes, "descriptor slot");
+
+template <typename T>
+__global__ void __launch_bounds__(kTThreads, 1) logits_stream_tma_kernel(const ReduceArgs a) {
+  using VT = Vec16<T>;
+  constexpr int ES = static_cast<int>(sizeof(T));
+  constexpr int EPV = VT::N;         // elements per 16-byte vector
+  constexpr int EPT = 128 / ES;      // elements per consumer thread
+  constexpr int TPB = kBlock / EPT;  // consumer threads per 64-block (1, or 2 for f32)
+  constexpr int CH = kTConsumers / TPB;  // blocks per chunk
+  constexpr int S = kTStages;
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* stages = smem;
+  StreamDesc* desc = reinterpret_cast<StreamDesc*>(smem + S * kTChunkBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kTChunkBytes + S * kTDescBytes);
+  uint64_t* empty = full + S;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kTConsumerWarps);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+  pdl_launch_dependents();  // the select kernel may be scheduled; it waits for this grid's results
+
+  if (warp == kTConsumerWarps) {
+    // ------------------------------ producer ------------------------------
+    if (lane != 0) return;
+    ChunkIter<CH> it;
+    it.init(a);
+    uint32_t issued = 0;
+    int sel_row = -1, sel_id = -1;
+    for (;; ++issued) {
+      const int s = static_cast<int>(issued % S);
+      if (issued >= static_cast<uint32_t>(S) &&
+          !wait_or_abort(&empty[s], ((issued / S) & 1u) ^ 1u, abort_flag, a.dev_status))
+        break;
+      const Chunk c = it.next(a);
+      StreamDesc& d = desc[s];
+      if (!c.valid) {
+        d.row = -1;
+        mbar_arrive(&full[s]);  // end marker: completes with no bytes
+        ++issued;
+        break;
+      }
+      if (c.row != sel_row) {
+        sel_row = c.row;
+        sel_id = a.sel ? a.sel[c.row] : -1;
+      }
+      const int ne = min(c.nbk * kBlock, a.V - c.lb * kBlock);
+      d.row = c.row;
+      d.lb = c.lb;
+      d.nbk = c.nbk;
+      d.ne = ne;
+      d.slot = piece_slot(a, c.row, c.range);
+      d.sel_rel = sel_id - c.lb * kBlock;
+      d.piece_end = it.piece_ended() ? 1 : 0;
+      const char* src = a.logits + (static_cast<int64_t>(c.row) * a.row_stride + static_cast<int64_t>(c.lb) * kBlock) * ES;
+      mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(ne * ES));
+      bulk_load(stages + static_cast<size_t>(s) * kTChunkBytes, src, static_cast<uint32_t>(ne * ES), &full[s]);
+    }
+    // Copies still in flight (only after an abort) land before the CTA exits.
+    const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
+    for (uint32_t i = first; i < issued; ++i) mbar_wait(&full[i % S], (i / S) & 1u);
+    return;
+  }
+
+  // ------------------------------ consumers ------------------------------
+  const int c = tid;  // consumer thread 0..255: bytes [128c, 128c + 128) of a chunk
+  const int rot = c & 7;  // vector order rotated by lane: conflict-free 16-byte shared loads
+  const int bi = c / TPB;
+  const float L = kLog2e;
+  float tm = -INFINITY, ts = 0.0f;  // running max / sum of this thread over the current row piece
+  for (uint32_t i = 0;; ++i) {
+    const int s = static_cast<int>(i % S);
+    bool ok = wait_or_abort(&full[s], (i / S) & 1u, abort_flag, a.dev_status);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    const StreamDesc d = desc[s];
+    if (d.row < 0) break;
+    const unsigned char* stg = stages + static_cast<size_t>(s) * kTChunkBytes;
+    uint4 w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] = *reinterpret_cast<const uint4*>(stg + c * 128 + ((j + rot) & 7) * 16);
+    const bool sel_hit = static_cast<unsigned>(d.sel_rel - c * EPT) < static_cast<unsigned>(EPT) && d.sel_rel < d.ne;
+    float selv = 0.0f;
+    if (sel_hit) selv = VT::at(stg, d.sel_rel);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);  // the stage is in registers: release it
+    if (sel_hit) a.parts.sel_logit[d.row] = selv;
+
+    const int ne_t = d.ne - c * EPT;  // real logits among this thread's
+    if (ne_t < EPT) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (((j + rot) & 7) * EPV >= ne_t) w[j] = make_uint4(VT::kNegInfWord, VT::kNegInfWord, VT::kNegInfWord, VT::kNegInfWord);
+    }
+    const float vm = VT::max8(w);
+    float bmx = vm;
+    if (TPB == 2) bmx = fmaxf(bmx, __shfl_xor_sync(0xffffffffu, bmx, 1));
+    if ((c % TPB) == 0 && bi < d.nbk) a.parts.bmax[static_cast<int64_t>(d.row) * a.nblk + d.lb + bi] = bmx;
+    if (vm > -INFINITY) {
+      if (vm > tm) {
+        ts *= ex2_approx((tm - vm) * L);  // tm = -inf: ts is 0 and stays 0
+        tm = vm;
+      }
+      const float mL = tm * L;
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float x[EPV];
+        VT::unpack(w[j], x);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) acc[e & 3] += ex2_approx(fmaf(x[e], L, -mL));
+      }
+      ts += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    }
+    if (d.piece_end) {
+      const float M = warp_max(tm);
+      const float sc = warp_sum(tm == -INFINITY ? 0.0f : ts * ex2_approx((tm - M) * L));
+      if (lane == 0) a.parts.part_ms[d.slot + warp] = make_float2(M, M == -INFINITY ? 0.0f : sc);
+      tm = -INFINITY;
+      ts = 0.0f;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// stream kernel, register path (any element-aligned layout)
+// ---------------------------------------------------------------------------
 
 // The chunk's vectors v = threadIdx.x + j * kRThreads (j < kRVecPerThread)
 // held in registers; `ne` logits of the chunk are real, the rest read as -inf.
@@ -209,13 +423,11 @@ struct ChunkRegs {
 };
 
 template <typename T>
-__global__ void __launch_bounds__(kRThreads, kRCtasPerSm) logits_stream_kernel(const ReduceArgs a) {
+__global__ void __launch_bounds__(kRThreads, kRCtasPerSm) logits_stream_regs_kernel(const ReduceArgs a) {
   using VT = Vec16<T>;
-  constexpr int EPV = VT::N;                                        // elements per 16-byte vector
-  constexpr int VPB = kBlock / EPV;                                 // vectors per 64-block
-  constexpr int CH = kRVecPerThread * kRThreads / VPB;              // blocks per chunk
-  constexpr int kValueBits = VT::kKeyBits;
-  constexpr uint32_t kMask = kValueBits >= 32 ? 0xFFFFFFFFu : (0xFFFFFFFFu << (32 - kValueBits));
+  constexpr int EPV = VT::N;                            // elements per 16-byte vector
+  constexpr int VPB = kBlock / EPV;                     // vectors per 64-block
+  constexpr int CH = kRVecPerThread * kRThreads / VPB;  // blocks per chunk
 
   __shared__ float red[32];
   pdl_launch_dependents();  // the select kernel may be scheduled now; it waits for this grid's results
@@ -223,30 +435,36 @@ __global__ void __launch_bounds__(kRThreads, kRCtasPerSm) logits_stream_kernel(c
   ChunkIter<CH> it;
   it.init(a);
   Chunk cur = it.next(a);
+  bool cur_end = it.piece_ended();
   ChunkRegs<T> buf0, buf1;  // two register buffers with fixed roles per half of the unrolled loop
   if (cur.valid) buf0.load(a, cur);
 
   const float L = kLog2e;
   float tm = -INFINITY, ts = 0.0f;  // this thread's running max / sum over the current piece
-  int piece_blocks = 0, sel_rel = -1;
+  int sel_row = -1, sel_id = -1;
   auto step = [&](ChunkRegs<T>& cb, ChunkRegs<T>& nb) {
     const Chunk nxt = it.next(a);
+    const bool nxt_end = it.piece_ended();
     if (nxt.valid) nb.load(a, nxt);  // in flight while this chunk is worked on
-    if (piece_blocks == 0) sel_rel = a.sel ? a.sel[cur.row] : -1;
+    if (cur.row != sel_row) {
+      sel_row = cur.row;
+      sel_id = a.sel ? a.sel[cur.row] : -1;
+    }
     const int ne = cb.ne;
-    const int rel0 = sel_rel - cur.lb * kBlock;  // selected token relative to this chunk
+    const int rel0 = sel_id - cur.lb * kBlock;  // selected token relative to this chunk
+    const bool sel_here = rel0 >= 0 && rel0 < ne;
 
     // ---- block maxima + online (m, s) ----
 #pragma unroll
     for (int j = 0; j < kRVecPerThread; ++j) {
       const int v = threadIdx.x + j * kRThreads;
       float x[EPV];
-      VT::load(&cb.w[j], x);
+      VT::unpack(cb.w[j], x);
       float vm = x[0];
 #pragma unroll
       for (int e = 1; e < EPV; ++e) vm = fmaxf(vm, x[e]);
       if (vm > tm) {
-        ts = (tm == -INFINITY) ? 0.0f : ts * ex2_approx((tm - vm) * L);
+        ts *= ex2_approx((tm - vm) * L);  // tm = -inf: ts is 0 and stays 0
         tm = vm;
       }
       if (tm != -INFINITY) {
@@ -254,32 +472,30 @@ __global__ void __launch_bounds__(kRThreads, kRCtasPerSm) logits_stream_kernel(c
 #pragma unroll
         for (int e = 0; e < EPV; ++e) ts += ex2_approx(fmaf(x[e], L, -mL));
       }
-      const unsigned r = static_cast<unsigned>(rel0 - v * EPV);
-      if (r < static_cast<unsigned>(EPV) && rel0 < ne) {  // the token is one of this chunk's real logits
-        float sv = 0.0f;
+      if (sel_here) {
+        const unsigned r = static_cast<unsigned>(rel0 - v * EPV);
+        if (r < static_cast<unsigned>(EPV)) {
+          float sv = 0.0f;
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) sv = (static_cast<unsigned>(e) == r) ? x[e] : sv;
-        a.parts.sel_logit[cur.row] = sv;
+          for (int e = 0; e < EPV; ++e) sv = (static_cast<unsigned>(e) == r) ? x[e] : sv;
+          a.parts.sel_logit[cur.row] = sv;
+        }
       }
 #pragma unroll
       for (int o = VPB / 2; o > 0; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
       if (v * EPV < cur.nbk * kBlock && (threadIdx.x % VPB) == 0)
         a.parts.bmax[static_cast<int64_t>(cur.row) * a.nblk + cur.lb + v / VPB] = vm;
     }
-    piece_blocks += cur.nbk;
 
-    const bool piece_end = !nxt.valid || nxt.row != cur.row || nxt.range != cur.range;
-    if (piece_end) {
-      const int row = cur.row;
-      const int slot = cur.range - static_cast<int>((static_cast<int64_t>(row) * a.nblk) / a.per);
+    if (cur_end) {
       const float M = block_max(tm, red);
-      const float S = block_sum((tm == -INFINITY) ? 0.0f : ts * expf(tm - M), red);
-      if (threadIdx.x == 0) a.parts.part_ms[static_cast<int64_t>(row) * a.P + slot] = make_float2(M, M == -INFINITY ? 0.0f : S);
+      const float S = block_sum((tm == -INFINITY) ? 0.0f : ts * ex2_approx((tm - M) * L), red);
+      if (threadIdx.x == 0) a.parts.part_ms[piece_slot(a, cur.row, cur.range)] = make_float2(M, M == -INFINITY ? 0.0f : S);
       tm = -INFINITY;
       ts = 0.0f;
-      piece_blocks = 0;
     }
     cur = nxt;
+    cur_end = nxt_end;
   };
   while (cur.valid) {
     step(buf0, buf1);
@@ -292,29 +508,56 @@ __global__ void __launch_bounds__(kRThreads, kRCtasPerSm) logits_stream_kernel(c
 // per-row selection
 // ---------------------------------------------------------------------------
 constexpr int kSThreads = 256;
+constexpr int kSWarps = kSThreads / 32;
 constexpr int kSKeptCap = 1024;  // kept blocks held in shared memory
 constexpr int kSCandCap = 512;   // candidate keys held in shared memory
-constexpr int kSStageBlocks = 16384;  // block maxima staged in shared memory (V <= 1,048,576)
+
+// Lower bound on the k-th largest logit of a row from its block maxima.
+// Each thread takes the maximum of its share of the blocks; in every warp the
+// q-th largest of those (q = ceil(k / warps)) is a value that q blocks of the
+// warp reach, so the minimum t over the warps is reached by q * warps >= k
+// distinct blocks, each holding a logit >= t: the k-th largest logit is >= t,
+// every top-k logit is >= t and lies in a block whose maximum is >= t.
+__device__ __forceinline__ float topk_lower_bound(const float* bm, int nb, int k, float* wq) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float tmax = -INFINITY;  // never NaN: fmaxf drops NaN block maxima
+#pragma unroll 4
+  for (int b = tid; b < nb; b += kSThreads) tmax = fmaxf(tmax, bm[b]);
+  const int q = (k + kSWarps - 1) / kSWarps;
+  int rank = 0;  // position of (tmax, lane) in the warp, by value desc then lane asc
+#pragma unroll
+  for (int o = 0; o < 32; ++o) {
+    const float v = __shfl_sync(0xffffffffu, tmax, o);
+    rank += (v > tmax) | ((v == tmax) & (o < lane));
+  }
+  if (rank == q - 1) wq[warp] = tmax;
+  __syncthreads();
+  float t = wq[0];
+#pragma unroll
+  for (int w = 1; w < kSWarps; ++w) t = fminf(t, wq[w]);
+  return t;
+}
 
 template <typename T>
 __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceArgs a, float* lse_out,
                                                                   float* sel_logprob, int32_t* topk_ids,
                                                                   float* topk_logprobs) {
   using VT = Vec16<T>;
-  constexpr int kValueBits = VT::kKeyBits;
-  constexpr uint32_t kMask = kValueBits >= 32 ? 0xFFFFFFFFu : (0xFFFFFFFFu << (32 - kValueBits));
+  constexpr int EPV = VT::N;
+  constexpr int VPB = kBlock / EPV;
   __shared__ uint64_t cand[kSCandCap];
   __shared__ int kept[kSKeptCap];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t misc[4];  // [0] candidates, [1..2] select broadcast, [3] kept blocks
   __shared__ float red[32];
+  __shared__ float wq[kSWarps];
   pdl_wait();  // the block maxima and (m, s) come from the stream kernel just before
 
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
-  // ---- lse over the row's pieces ----
+  // ---- lse over the row's (m, s) slots ----
   const int64_t b0 = static_cast<int64_t>(row) * a.nblk;
-  const int nslots = static_cast<int>((b0 + a.nblk - 1) / a.per - b0 / a.per) + 1;
+  const int nslots = static_cast<int>((b0 + a.nblk - 1) / a.per - b0 / a.per + 1) * a.W;
   const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.P;
   float tm = -INFINITY, ts = 0.0f;
   for (int j = tid; j < nslots; j += kSThreads) {
@@ -355,63 +598,61 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
     return;
   }
 
-  // ---- tau: the k-th largest block maximum of the row ----
-  // The row's block maxima are staged in shared memory (one coalesced round)
-  // when they fit; otherwise they are read from global memory (L2).
-  extern __shared__ float sbm[];
+  // ---- t <= the k-th largest logit; kept blocks: maximum >= t ----
   const int nb = a.nblk;
   const float* bm = a.parts.bmax + b0;
-  if (nb <= kSStageBlocks) {
-    for (int b = tid; b < nb; b += kSThreads) sbm[b] = bm[b];
-    __syncthreads();
-    bm = sbm;
-  }
-  uint32_t thr = 0;  // ord(tau) restricted to the top kValueBits bits; 0 keeps every entry
-  if (nb > k) {
-    int above;
-    const uint64_t T64 = cta_radix_select(
-        [&](int b, uint64_t* key) {
-          *key = static_cast<uint64_t>(f32_ord(bm[b])) << 32;
-          return true;
-        },
-        nb, k, kValueBits, hist, misc + 1, &above);
-    thr = static_cast<uint32_t>(T64 >> 32);
-  }
-  __syncthreads();
-  // ---- kept blocks (order is irrelevant: candidates are ranked below) ----
+  const float t = topk_lower_bound(bm, nb, k, wq);
   for (int b = tid; b < nb; b += kSThreads)
-    if ((f32_ord(bm[b]) & kMask) >= thr) {
+    if (bm[b] >= t) {
       const uint32_t pos = atomicAdd(&misc[3], 1u);
       if (pos < kSKeptCap) kept[pos] = b;
     }
   __syncthreads();
   const int nkept = static_cast<int>(misc[3]);
   const T* rowp = reinterpret_cast<const T*>(a.logits) + static_cast<int64_t>(row) * a.row_stride;
-  auto in_set = [&](int i, uint64_t* key) -> bool {  // i over the whole row (fallback)
-    if ((f32_ord(bm[i / kBlock]) & kMask) < thr || i >= a.V) return false;
-    const float x = VT::at(rowp, i);
-    if ((f32_ord(x) & kMask) < thr) return false;
-    *key = make_key(x, i);
-    return true;
-  };
   int cnt;
   if (nkept <= kSKeptCap) {
-    // gather the kept blocks' entries >= tau: every load of the CTA in one round
-    const int n_el = nkept * kBlock;
-    for (int i = tid; i < n_el; i += kSThreads) {
-      const int e = kept[i / kBlock] * kBlock + (i % kBlock);
-      if (e >= a.V) continue;
-      const float x = VT::at(rowp, e);
-      if ((f32_ord(x) & kMask) < thr) continue;
-      const uint32_t pos = atomicAdd(&misc[0], 1u);
-      if (pos < kSCandCap) cand[pos] = make_key(x, e);
+    // the kept blocks' entries >= t: every load of the CTA in one round
+    if (a.vec_ok) {  // whole 16-byte vectors; none straddles the row end
+      const int n_vec = nkept * VPB;
+      for (int i = tid; i < n_vec; i += kSThreads) {
+        const int e0 = kept[i / VPB] * kBlock + (i % VPB) * EPV;
+        if (e0 >= a.V) continue;
+        float x[EPV];
+        VT::load(rowp + e0, x);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e)
+          if (x[e] >= t) {
+            const uint32_t pos = atomicAdd(&misc[0], 1u);
+            if (pos < kSCandCap) cand[pos] = make_key(x[e], e0 + e);
+          }
+      }
+    } else {
+      const int n_el = nkept * kBlock;
+      for (int i = tid; i < n_el; i += kSThreads) {
+        const int e = kept[i / kBlock] * kBlock + (i % kBlock);
+        if (e >= a.V) continue;
+        const float x = VT::at(rowp, e);
+        if (x >= t) {
+          const uint32_t pos = atomicAdd(&misc[0], 1u);
+          if (pos < kSCandCap) cand[pos] = make_key(x, e);
+        }
+      }
     }
     __syncthreads();
     cnt = static_cast<int>(misc[0]);
   } else {
-    cnt = kSCandCap + 1;  // too many ties at tau for the lists: take the exact path
+    cnt = kSCandCap + 1;  // too many blocks reach t (ties, -inf rows): take the exact path
   }
   if (cnt > kSCandCap) {
+    // exact k-th key over the entries >= t of blocks reaching t, then the k keys at or above it
+    auto in_set = [&](int i, uint64_t* key) -> bool {
+      if (i >= a.V || !(bm[i / kBlock] >= t)) return false;
+      const float x = VT::at(rowp, i);
+      if (!(x >= t)) return false;
+      *key = make_key(x, i);
+      return true;
+    };
     int above;
     const int n_items = nb * kBlock;
     const uint64_t T64 = cta_radix_select(in_set, n_items, k, 64, hist, misc + 1, &above);
@@ -429,8 +670,8 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
     cnt = min(k, static_cast<int>(misc[0]));
   }
   // ---- exact order by rank (keys are unique) ----
-  for (int t = tid; t < cnt; t += kSThreads) {
-    const uint64_t key = cand[t];
+  for (int i = tid; i < cnt; i += kSThreads) {
+    const uint64_t key = cand[i];
     int rank = 0;
     for (int j = 0; j < cnt; ++j) rank += cand[j] > key;
     if (rank < k) {
@@ -444,11 +685,16 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
   }
 }
 
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
 VocabSplit logits_reduce_split(int rows, int V, int k_max, int num_sms) {
   VocabSplit vs;
   const int nblk = (V + kBlock - 1) / kBlock;
   const int64_t nb_total = static_cast<int64_t>(rows) * nblk;
-  const int64_t G = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * kRCtasPerSm;
+  const int sms = num_sms > 0 ? num_sms : 1;
+  const int64_t G = static_cast<int64_t>(sms) * kRCtasPerSm;  // ranges aimed at: two per SM
   int64_t per = (nb_total + G - 1) / G;
   // a range of more than 2k blocks lets the block-max threshold prune (<= k blocks keep everything)
   const int64_t min_per = 2 * k_max > kRMinPer ? 2 * k_max : kRMinPer;
@@ -459,23 +705,23 @@ VocabSplit logits_reduce_split(int rows, int V, int k_max, int num_sms) {
   vs.grid = static_cast<int>(vs.n_ranges < G ? vs.n_ranges : G);
   vs.splits = static_cast<int>((nblk + per - 1) / per) + 1;  // row pieces per row, at most
   vs.nblk = nblk;
+  vs.sms = sms;
   return vs;
 }
 
 cudaError_t logits_reduce_setup() {
-  const int bytes = kSStageBlocks * static_cast<int>(sizeof(float));
-  cudaError_t e =
-      cudaFuncSetAttribute(logits_select_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaError_t e = cudaFuncSetAttribute(logits_stream_tma_kernel<__nv_bfloat16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(logits_select_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = cudaFuncSetAttribute(logits_stream_tma_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(logits_select_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    e = cudaFuncSetAttribute(logits_stream_tma_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
   return e;
 }
 
 size_t stream_partials_bytes(int rows, const VocabSplit& vs) {
   auto al = [](size_t n) { return (n + 255) & ~static_cast<size_t>(255); };
-  return al(static_cast<size_t>(rows) * vs.splits * 8) + al(static_cast<size_t>(rows) * 4) +
+  return al(static_cast<size_t>(rows) * vs.splits * kSlotsPerPiece * 8) + al(static_cast<size_t>(rows) * 4) +
          al(static_cast<size_t>(rows) * vs.nblk * 4);
 }
 
@@ -484,7 +730,7 @@ Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs) {
   char* p = static_cast<char*>(base);
   Partials out;
   out.part_ms = reinterpret_cast<float2*>(p);
-  p += al(static_cast<size_t>(rows) * vs.splits * 8);
+  p += al(static_cast<size_t>(rows) * vs.splits * kSlotsPerPiece * 8);
   out.sel_logit = reinterpret_cast<float*>(p);
   p += al(static_cast<size_t>(rows) * 4);
   out.bmax = reinterpret_cast<float*>(p);
@@ -493,20 +739,25 @@ Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs) {
 }
 
 template <typename T>
-static cudaError_t launch_both(const ReduceArgs& a, const VocabSplit& split, float* lse, float* sel_logprob,
-                               int32_t* topk_ids, float* topk_logprobs, cudaStream_t stream, TraceKernel tk_select) {
+static cudaError_t launch_both(ReduceArgs a, const VocabSplit& split, float* lse, float* sel_logprob,
+                               int32_t* topk_ids, float* topk_logprobs, cudaStream_t stream) {
   cudaError_t e;
-  {
-    trace_begin(kTraceReduce, stream);
-    e = launch_kernel(logits_stream_kernel<T>, dim3(split.grid), dim3(kRThreads), 0, stream, false, a);
-    trace_end(kTraceReduce, stream);
+  trace_begin(kTraceReduce, stream);
+  if (a.vec_ok) {
+    a.W = kTConsumerWarps;
+    const int grid = split.n_ranges < split.sms ? split.n_ranges : split.sms;
+    e = launch_kernel(logits_stream_tma_kernel<T>, dim3(grid), dim3(kTThreads), static_cast<size_t>(kTSmem), stream,
+                      false, a);
+  } else {
+    a.W = 1;
+    e = launch_kernel(logits_stream_regs_kernel<T>, dim3(split.grid), dim3(kRThreads), 0, stream, false, a);
   }
+  trace_end(kTraceReduce, stream);
   if (e != cudaSuccess) return e;
-  trace_begin(tk_select, stream);
-  const size_t smem = static_cast<size_t>(min(a.nblk, kSStageBlocks)) * sizeof(float);
-  e = launch_kernel(logits_select_kernel<T>, dim3(a.rows), dim3(kSThreads), smem, stream, true, a, lse, sel_logprob,
+  trace_begin(kTraceLogitsSelect, stream);
+  e = launch_kernel(logits_select_kernel<T>, dim3(a.rows), dim3(kSThreads), 0, stream, true, a, lse, sel_logprob,
                     topk_ids, topk_logprobs);
-  trace_end(tk_select, stream);
+  trace_end(kTraceLogitsSelect, stream);
   return e;
 }
 
@@ -514,6 +765,7 @@ cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t ro
                                  VocabSplit split, const int32_t* sel, const int32_t* row_k, int k_max,
                                  Partials parts, float* lse, float* sel_logprob, int32_t* topk_ids,
                                  float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream) {
+  const int64_t es = dtype == LMH_F32 ? 4 : 2;
   ReduceArgs a;
   a.logits = static_cast<const char*>(logits);
   a.row_stride = row_stride;
@@ -523,7 +775,10 @@ cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t ro
   a.nb_total = static_cast<int64_t>(rows) * split.nblk;
   a.per = split.per;
   a.n_ranges = split.n_ranges;
-  a.P = split.splits;
+  a.P = split.splits * kSlotsPerPiece;
+  a.W = 1;
+  a.vec_ok = (reinterpret_cast<uintptr_t>(logits) % 16) == 0 && ((row_stride * es) % 16) == 0 &&
+             ((static_cast<int64_t>(V) * es) % 16) == 0;
   a.sel = sel;
   a.row_k = row_k;
   a.k_max = k_max;
@@ -531,11 +786,11 @@ cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t ro
   a.dev_status = dev_status;
   switch (dtype) {
     case LMH_BF16:
-      return launch_both<__nv_bfloat16>(a, split, lse, sel_logprob, topk_ids, topk_logprobs, stream, kTraceLogitsSelect);
+      return launch_both<__nv_bfloat16>(a, split, lse, sel_logprob, topk_ids, topk_logprobs, stream);
     case LMH_F16:
-      return launch_both<__half>(a, split, lse, sel_logprob, topk_ids, topk_logprobs, stream, kTraceLogitsSelect);
+      return launch_both<__half>(a, split, lse, sel_logprob, topk_ids, topk_logprobs, stream);
     default:
-      return launch_both<float>(a, split, lse, sel_logprob, topk_ids, topk_logprobs, stream, kTraceLogitsSelect);
+      return launch_both<float>(a, split, lse, sel_logprob, topk_ids, topk_logprobs, stream);
   }
 }
 
