@@ -176,3 +176,28 @@ def test_row_idx_out_of_range_sets_status(lmh, tiny):
     o, st, logits = gpu_project(lmh, b["hidden"].cuda(), b["W"].cuda(), row_idx=ri, k=3, materialize=True)
     assert st & L.DS_ROW_IDX_OUT_OF_RANGE
     assert torch.count_nonzero(logits[1]) == 0
+
+
+@pytest.mark.parametrize("rows,H,V,k,gather", [(19400, 64, 512, 20, False), (10000, 128, 200, 128, True)])
+def test_single_split_plans(lmh, rows, H, V, k, gather):
+    """Plans with one vocabulary split: the head kernel writes lse, the selected
+    logprob and the top-k itself (no merge launch).  152 row tiles of one split
+    each, or a vocabulary of one column tile; per-row K includes 0 and ranks
+    past a row's K; sampled rows vs the oracle."""
+    g = torch.Generator().manual_seed(rows + V)
+    T = rows + (7 if gather else 0)
+    b = {"hidden": torch.randn(T, H, generator=g).to(torch.bfloat16),
+         "W": (torch.randn(V, H, generator=g) / H ** 0.5).to(torch.bfloat16)}
+    ri = torch.randperm(T, generator=g)[:rows].to(torch.int32) if gather else None
+    sel = torch.randint(-1, V, (rows,), generator=g, dtype=torch.int32)
+    row_k = torch.randint(0, k + 1, (rows,), generator=g, dtype=torch.int32)
+    o, st, _ = gpu_project(lmh, b["hidden"].cuda(), b["W"].cuda(), row_idx=None if ri is None else ri.cuda(),
+                           rows=rows, sel=sel, row_k=row_k, k=k)
+    assert st == 0
+    rng = np.random.default_rng(1)
+    sample = np.unique(np.concatenate([[0, 1, 127, 128, rows - 1], rng.choice(rows, 120, replace=False)]))
+    packed = sample if ri is None else ri.numpy()[sample]
+    rk = row_k.numpy()[sample]
+    z, orc, A = oracle_rows(b, packed, sel.numpy()[sample], k, row_k=rk)
+    sub = {key: v[torch.as_tensor(sample)] for key, v in o.items() if v is not None}
+    check_fused(sub, orc, z, A, b["W"], k, row_k=rk, what="one split %s" % ((rows, H, V, k),))

@@ -69,6 +69,8 @@ struct HeadArgs {
   Partials parts;
   float* logits_out;
   uint32_t* dev_status;
+  int final_out;   // one vocabulary split: write the final results (out), not partials
+  RowOutputs out;
 };
 
 // ---------------------------------------------------------------------------
@@ -484,7 +486,33 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         mbar_arrive(&acc_empty[b]);
       }
       if (!live) break;
-      if (valid) {
+      if (valid && a.final_out) {
+        // the whole row went through this thread: lse = m + log(sum), logprob = logit - lse
+        const float lse = (m == -INFINITY) ? -INFINITY : m + logf(ssum);
+        a.out.lse[row] = lse;
+        if (a.sel) {
+          float sv = __int_as_float(0x7fc00000);  // NaN: no selected token / out of range
+          if (sel_id >= 0 && sel_id < a.V)
+            sv = sel_val - lse;
+          else if (sel_id != -1)
+            set_status(a.dev_status, LMH_DS_SEL_OUT_OF_RANGE);
+          a.out.sel_logprob[row] = sv;
+        }
+        int32_t* ids = a.out.topk_ids + static_cast<int64_t>(row) * a.k_max;
+        float* lps = a.out.topk_logprobs + static_cast<int64_t>(row) * a.k_max;
+        auto put = [&](int j, uint64_t key) {  // key 0: fewer than k candidates
+          ids[j] = key ? key_id(key) : -1;
+          lps[j] = key ? key_value(key) - lse : -INFINITY;
+        };
+        if constexpr (Cfg::kRegList) {
+#pragma unroll
+          for (int j = 0; j < (Cfg::kRegList ? KCAP : 1); ++j)
+            if (j < k_row) put(j, rt.L[j]);
+        } else {
+          for (int j = 0; j < k_row; ++j) put(j, (j < st.cnt) ? lists[j * kBM + r_local] : 0ull);
+        }
+        for (int j = k_row; j < a.k_max; ++j) put(j, 0ull);
+      } else if (valid) {
         const int64_t pidx = static_cast<int64_t>(row) * a.splits + split;
         a.parts.part_ms[pidx] = make_float2(m, ssum);
         unsigned long long* out = a.parts.part_keys + pidx * a.k_max;
@@ -627,7 +655,8 @@ cudaError_t head_setup() {
 
 cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const void* W, int V, const HeadPlan& plan,
                         const int32_t* sel, const int32_t* row_k, int k_max, Partials parts, float* logits_out,
-                        uint32_t* dev_status, cudaStream_t stream, bool pdl) {
+                        uint32_t* dev_status, cudaStream_t stream, bool pdl, const RowOutputs* final_out) {
+  if (final_out && plan.splits != 1) return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
   // With fewer than 128 rows (one row tile) the A box covers only the real
   // rows (rounded up to 8); the stage's other rows keep stale data that only
@@ -654,6 +683,8 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   a.parts = parts;
   a.logits_out = logits_out;
   a.dev_status = dev_status;
+  a.final_out = final_out ? 1 : 0;
+  a.out = final_out ? *final_out : RowOutputs{nullptr, nullptr, nullptr, nullptr};
   const dim3 grid(plan.grid), block(kHeadThreads);
   switch (plan.kcap) {
 #define LMH_HEAD_CASE(KC)                                                                               \

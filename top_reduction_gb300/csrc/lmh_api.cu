@@ -242,12 +242,15 @@ lmh_status lmh_project_logprobs(const void* hidden, int64_t hidden_row_stride, i
     A = ws;
     a_stride = H;
   }
+  // One vocabulary split: the head kernel finishes every row itself.
+  const RowOutputs outs{lse, sel_logprob, topk_ids, topk_logprobs};
+  const bool one_split = plan.splits == 1;
   if (e == cudaSuccess) {
     Traced tr(kTraceHead, stream);
     e = launch_head(A, a_stride, rows, H, W, V, plan, sel_ids, row_k, k_max, parts, logits_out, dev_status, stream,
-                    /*pdl=*/gather);
+                    /*pdl=*/gather, one_split ? &outs : nullptr);
   }
-  if (e == cudaSuccess) {
+  if (e == cudaSuccess && !one_split) {
     Traced tr(kTraceMerge, stream);
     e = launch_merge(rows, plan.splits, V, k_max, parts, sel_ids, row_k, lse, sel_logprob, topk_ids, topk_logprobs,
                      dev_status, stream, 0, 0, /*pdl=*/true);

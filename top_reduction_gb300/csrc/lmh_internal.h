@@ -22,9 +22,8 @@ struct VocabSplit {
   int splits;    // row pieces per row, at most
   int per;       // 64-blocks per range
   int n_ranges;  // ranges in total
-  int grid;      // persistent CTAs of the register-path stream kernel (two per SM)
+  int grid;      // persistent CTAs of the stream kernel (two per SM)
   int nblk;      // 64-blocks per row
-  int sms;       // SMs of the device (persistent CTAs of the TMA-path stream kernel)
 };
 
 // Per-(row, split) partial results, laid out in the caller's workspace:
@@ -36,6 +35,14 @@ struct Partials {
   unsigned long long* part_keys;
   float* sel_logit;
   float* bmax;  // standalone reduction: block maxima [rows * nblk] (else unused)
+};
+
+// Final per-row results (the outputs of lmh_project_logprobs / lmh_logprobs_from_logits).
+struct RowOutputs {
+  float* lse;
+  float* sel_logprob;
+  int32_t* topk_ids;
+  float* topk_logprobs;
 };
 
 size_t partials_bytes(int rows, int splits, int k_max);
@@ -90,10 +97,13 @@ cudaError_t launch_gather_rows(const void* hidden, int64_t hidden_stride, int nu
                                const int32_t* row_idx, int rows, int H, void* out, uint32_t* dev_status,
                                cudaStream_t stream);
 
+// final_out != nullptr (a plan with one vocabulary split): every row lies in
+// one CTA's unit, so the kernel writes the final results itself and no merge
+// follows; otherwise it writes the per-split partials.
 cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const void* W, int V,
                         const HeadPlan& plan, const int32_t* sel, const int32_t* row_k, int k_max,
                         Partials parts, float* logits_out, uint32_t* dev_status, cudaStream_t stream,
-                        bool pdl = false);
+                        bool pdl = false, const RowOutputs* final_out = nullptr);
 
 // Launch `kernel` on `stream`; with pdl = true it carries the programmatic
 // stream serialization attribute, so it may start while its predecessor in the

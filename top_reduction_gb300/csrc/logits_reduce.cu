@@ -48,7 +48,7 @@ constexpr int kTConsumerWarps = 8;
 constexpr int kTConsumers = kTConsumerWarps * 32;
 constexpr int kTThreads = kTConsumers + 32;  // + one producer warp
 constexpr int kTChunkBytes = kTConsumers * 128;  // 128 contiguous bytes per consumer thread
-constexpr int kTStages = 6;
+constexpr int kTStages = 3;  // per CTA; two CTAs per SM
 constexpr int kTDescBytes = 32;
 constexpr int kTSmem = kTStages * kTChunkBytes + kTStages * kTDescBytes + 2 * kTStages * 8 + 16;
 // (m, s) slots reserved per row piece: one per consumer warp of the TMA path
@@ -84,6 +84,12 @@ struct Vec16<__nv_bfloat16> {
     const __nv_bfloat162 r = __hmax2(__hmax2(m[0], m[1]), __hmax2(m[2], m[3]));
     return fmaxf(__low2float(r), __high2float(r));
   }
+  // the vector as 4 pairs of fp32 values
+  __device__ __forceinline__ static void pairs(const uint4 w, float2* p) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = make_float2(__uint_as_float(u[i] << 16), __uint_as_float(u[i] & 0xFFFF0000u));
+  }
   __device__ __forceinline__ static __nv_bfloat162 as2(uint32_t u) {
     return *reinterpret_cast<const __nv_bfloat162*>(&u);
   }
@@ -106,6 +112,11 @@ struct Vec16<__half> {
       x[2 * i] = f.x;
       x[2 * i + 1] = f.y;
     }
+  }
+  __device__ __forceinline__ static void pairs(const uint4 w, float2* p) {
+    const __half2* h = reinterpret_cast<const __half2*>(&w);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = __half22float2(h[i]);
   }
   __device__ __forceinline__ static float max8(const uint4* w) {
     const __half2* h = reinterpret_cast<const __half2*>(w);
@@ -134,6 +145,10 @@ struct Vec16<float> {
     x[1] = __uint_as_float(w.y);
     x[2] = __uint_as_float(w.z);
     x[3] = __uint_as_float(w.w);
+  }
+  __device__ __forceinline__ static void pairs(const uint4 w, float2* p) {
+    p[0] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+    p[1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
   }
   __device__ __forceinline__ static float max8(const uint4* w) {
     float m[4];
@@ -259,7 +274,7 @@ struct StreamDesc {  // one per stage, written by the producer before the copy i
 static_assert(sizeof(StreamDesc) <= kTDescBytes, "descriptor slot");
 
 template <typename T>
-__global__ void __launch_bounds__(kTThreads, 1) logits_stream_tma_kernel(const ReduceArgs a) {
+__global__ void __launch_bounds__(kTThreads, 2) logits_stream_tma_kernel(const ReduceArgs a) {
   using VT = Vec16<T>;
   constexpr int ES = static_cast<int>(sizeof(T));
   constexpr int EPV = VT::N;         // elements per 16-byte vector
@@ -367,16 +382,24 @@ __global__ void __launch_bounds__(kTThreads, 1) logits_stream_tma_kernel(const R
         ts *= ex2_approx((tm - vm) * L);  // tm = -inf: ts is 0 and stays 0
         tm = vm;
       }
-      const float mL = tm * L;
-      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // exp(x - m) = 2^(x*log2e - m*log2e): one packed FFMA2 and one packed
+      // FADD2 per pair of logits around the two ex2
+      const float2 L2 = make_float2(L, L), nmL2 = make_float2(-tm * L, -tm * L);
+      float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                       make_float2(0.0f, 0.0f)};
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        float x[EPV];
-        VT::unpack(w[j], x);
+        float2 p[EPV / 2];
+        VT::pairs(w[j], p);
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) acc[e & 3] += ex2_approx(fmaf(x[e], L, -mL));
+        for (int q = 0; q < EPV / 2; ++q) {
+          const float2 y = __ffma2_rn(p[q], L2, nmL2);
+          acc[q & 3] = __fadd2_rn(acc[q & 3], make_float2(ex2_approx(y.x), ex2_approx(y.y)));
+        }
       }
-      ts += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+      const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+      const float2 a = __fadd2_rn(a01, a23);
+      ts += a.x + a.y;
     }
     if (d.piece_end) {
       const float M = warp_max(tm);
@@ -512,17 +535,16 @@ constexpr int kSWarps = kSThreads / 32;
 constexpr int kSKeptCap = 1024;  // kept blocks held in shared memory
 constexpr int kSCandCap = 512;   // candidate keys held in shared memory
 
+constexpr int kSBatch = 16;      // block maxima per thread loaded per round (rows of <= 4096 blocks: one)
+
 // Lower bound on the k-th largest logit of a row from its block maxima.
-// Each thread takes the maximum of its share of the blocks; in every warp the
-// q-th largest of those (q = ceil(k / warps)) is a value that q blocks of the
-// warp reach, so the minimum t over the warps is reached by q * warps >= k
+// `tmax` is each thread's maximum over its share of the blocks; in every warp
+// the q-th largest of those (q = ceil(k / warps)) is a value that q blocks of
+// the warp reach, so the minimum t over the warps is reached by q * warps >= k
 // distinct blocks, each holding a logit >= t: the k-th largest logit is >= t,
 // every top-k logit is >= t and lies in a block whose maximum is >= t.
-__device__ __forceinline__ float topk_lower_bound(const float* bm, int nb, int k, float* wq) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float tmax = -INFINITY;  // never NaN: fmaxf drops NaN block maxima
-#pragma unroll 4
-  for (int b = tid; b < nb; b += kSThreads) tmax = fmaxf(tmax, bm[b]);
+__device__ __forceinline__ float topk_lower_bound(float tmax, int k, float* wq) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int q = (k + kSWarps - 1) / kSWarps;
   int rank = 0;  // position of (tmax, lane) in the warp, by value desc then lane asc
 #pragma unroll
@@ -555,8 +577,21 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
 
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
-  // ---- lse over the row's (m, s) slots ----
   const int64_t b0 = static_cast<int64_t>(row) * a.nblk;
+  // The row's block maxima: loaded first, so that their latency overlaps the
+  // lse; kept in registers when one round covers the row.
+  const int nb = a.nblk;
+  const float* bm = a.parts.bmax + b0;
+  const bool one_round = nb <= kSBatch * kSThreads;
+  float bv[kSBatch];
+  if (one_round) {
+#pragma unroll
+    for (int i = 0; i < kSBatch; ++i) {
+      const int b = tid + i * kSThreads;
+      bv[i] = b < nb ? bm[b] : -INFINITY;
+    }
+  }
+  // ---- lse over the row's (m, s) slots ----
   const int nslots = static_cast<int>((b0 + a.nblk - 1) / a.per - b0 / a.per + 1) * a.W;
   const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.P;
   float tm = -INFINITY, ts = 0.0f;
@@ -599,14 +634,44 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
   }
 
   // ---- t <= the k-th largest logit; kept blocks: maximum >= t ----
-  const int nb = a.nblk;
-  const float* bm = a.parts.bmax + b0;
-  const float t = topk_lower_bound(bm, nb, k, wq);
-  for (int b = tid; b < nb; b += kSThreads)
-    if (bm[b] >= t) {
+  float tmax = -INFINITY;  // never NaN: fmaxf drops NaN block maxima
+  if (one_round) {
+#pragma unroll
+    for (int i = 0; i < kSBatch; ++i) tmax = fmaxf(tmax, bv[i]);
+  } else {
+    for (int base = 0; base < nb; base += kSBatch * kSThreads) {
+      float v[kSBatch];
+#pragma unroll
+      for (int i = 0; i < kSBatch; ++i) {
+        const int b = base + tid + i * kSThreads;
+        v[i] = b < nb ? bm[b] : -INFINITY;
+      }
+#pragma unroll
+      for (int i = 0; i < kSBatch; ++i) tmax = fmaxf(tmax, v[i]);
+    }
+  }
+  const float t = topk_lower_bound(tmax, k, wq);
+  auto keep = [&](int b, float v) {
+    if (b < nb && v >= t) {
       const uint32_t pos = atomicAdd(&misc[3], 1u);
       if (pos < kSKeptCap) kept[pos] = b;
     }
+  };
+  if (one_round) {
+#pragma unroll
+    for (int i = 0; i < kSBatch; ++i) keep(tid + i * kSThreads, bv[i]);
+  } else {
+    for (int base = 0; base < nb; base += kSBatch * kSThreads) {
+      float v[kSBatch];
+#pragma unroll
+      for (int i = 0; i < kSBatch; ++i) {
+        const int b = base + tid + i * kSThreads;
+        v[i] = b < nb ? bm[b] : -INFINITY;
+      }
+#pragma unroll
+      for (int i = 0; i < kSBatch; ++i) keep(base + tid + i * kSThreads, v[i]);
+    }
+  }
   __syncthreads();
   const int nkept = static_cast<int>(misc[3]);
   const T* rowp = reinterpret_cast<const T*>(a.logits) + static_cast<int64_t>(row) * a.row_stride;
@@ -705,7 +770,6 @@ VocabSplit logits_reduce_split(int rows, int V, int k_max, int num_sms) {
   vs.grid = static_cast<int>(vs.n_ranges < G ? vs.n_ranges : G);
   vs.splits = static_cast<int>((nblk + per - 1) / per) + 1;  // row pieces per row, at most
   vs.nblk = nblk;
-  vs.sms = sms;
   return vs;
 }
 
@@ -745,9 +809,8 @@ static cudaError_t launch_both(ReduceArgs a, const VocabSplit& split, float* lse
   trace_begin(kTraceReduce, stream);
   if (a.vec_ok) {
     a.W = kTConsumerWarps;
-    const int grid = split.n_ranges < split.sms ? split.n_ranges : split.sms;
-    e = launch_kernel(logits_stream_tma_kernel<T>, dim3(grid), dim3(kTThreads), static_cast<size_t>(kTSmem), stream,
-                      false, a);
+    e = launch_kernel(logits_stream_tma_kernel<T>, dim3(split.grid), dim3(kTThreads), static_cast<size_t>(kTSmem),
+                      stream, false, a);
   } else {
     a.W = 1;
     e = launch_kernel(logits_stream_regs_kernel<T>, dim3(split.grid), dim3(kRThreads), 0, stream, false, a);

@@ -6,7 +6,8 @@
 // - lse, evaluated only at the survivors and at the scored token; exact ties
 // by ascending id.
 //
-// One CTA per row (see merge_partials_kernel).
+// One CTA per row (merge_partials_kernel), or one warp per row when a row's
+// slots hold few keys (merge_partials_warp_kernel).
 #include "device_common.cuh"
 #include "lmh_internal.h"
 
@@ -33,9 +34,9 @@ struct MergeArgs {
 //         M = max_j m_j (lse = -inf when every logit is -inf);
 //   top-k = the k best keys of the union of the slots' sorted top-k lists.
 //         Every slot list holds that piece's k best, so the union holds the
-//         row's k best.  L = max over slots of their k-th key is a lower
-//         bound of the row's k-th key (one slot alone has k keys >= L), so
-//         only keys >= L are gathered; they are ordered by rank.
+//         row's k best.  A lower bound L of the row's k-th key (the k-th
+//         largest of the slots' leading keys) limits the gather to keys >= L;
+//         they are ordered by rank.
 __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const MergeArgs a) {
   __shared__ uint64_t cand[kMergeCap];
   __shared__ uint32_t hist[256];
@@ -92,12 +93,39 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
   }
 
   const unsigned long long* keys = a.parts.part_keys + static_cast<int64_t>(row) * a.splits * a.k_max;
-  uint64_t lb = 0;  // lower bound of the row's k-th key
-  for (int j = tid; j < nslots; j += kMergeThreads) {
-    const uint64_t kk = keys[static_cast<int64_t>(j) * a.k_max + (k - 1)];
-    lb = kk > lb ? kk : lb;
+  // ---- lb: a lower bound of the row's k-th key ----
+  // U = the q best keys of every slot, q = ceil(k / nslots), so |U| >= k and
+  // the k-th largest key of U is reached by k keys of the row.  (Taking the
+  // largest k-th key of a single slot is also a bound, but with many slots
+  // far more keys pass it.)  Keys are unique; empty entries (0) rank last.
+  uint64_t lb = 0;
+  const int q = (k + nslots - 1) / nslots;
+  const int nu = q * nslots;
+  if (nu <= kMergeCap) {
+    for (int i = tid; i < nu; i += kMergeThreads) {
+      const int j = i / q;
+      cand[i] = keys[static_cast<int64_t>(j) * a.k_max + (i - j * q)];
+    }
+    __syncthreads();
+    for (int i = tid; i < nu; i += kMergeThreads) {
+      const uint64_t key = cand[i];
+      int rank = 0;  // by key desc, then position asc
+      for (int j = 0; j < nu; ++j) {
+        const uint64_t o = cand[j];
+        rank += (o > key) | ((o == key) & (j < i));
+      }
+      if (rank == k - 1) red64[0] = key;
+    }
+    __syncthreads();
+    lb = red64[0];
+    __syncthreads();  // cand is reused below
+  } else {
+    for (int j = tid; j < nslots; j += kMergeThreads) {
+      const uint64_t kk = keys[static_cast<int64_t>(j) * a.k_max + (k - 1)];
+      lb = kk > lb ? kk : lb;
+    }
+    lb = block_max_u64(lb, red64);
   }
-  lb = block_max_u64(lb, red64);
   // gather every key >= lb: independent loads over all (slot, rank) items
   const int n_items = nslots * k;
   auto in_set = [&](int i, uint64_t* key) -> bool {
@@ -149,6 +177,129 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
   }
 }
 
+// ---------------------------------------------------------------------------
+// One warp per row, for plans whose slots hold at most kWarpItems keys per row
+// (many rows, few slots: the CTA-wide barriers of the kernel above would
+// dominate).  Same steps; every candidate fits the warp's buffer, so there
+// is no overflow path.
+// ---------------------------------------------------------------------------
+constexpr int kWarpItems = 512;
+constexpr int kWarpRowsPerCta = 8;
+
+__global__ void __launch_bounds__(kWarpRowsPerCta * 32) merge_partials_warp_kernel(const MergeArgs a) {
+  __shared__ uint64_t sbuf[kWarpRowsPerCta][kWarpItems];
+  pdl_wait();  // the partials come from the kernel launched just before
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int row = blockIdx.x * kWarpRowsPerCta + w;
+  if (row >= a.rows) return;
+  uint64_t* buf = sbuf[w];
+  const int nslots = a.splits;
+  const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.splits;
+
+  // ---- lse ----
+  float tm = -INFINITY, ts = 0.0f;
+  for (int j = lane; j < nslots; j += 32) {
+    const float2 p = ms[j];
+    if (p.x > tm) {
+      ts = (tm == -INFINITY) ? 0.0f : ts * expf(tm - p.x);
+      tm = p.x;
+    }
+    if (p.x != -INFINITY) ts += p.y * expf(p.x - tm);
+  }
+  const float M = warp_max(tm);
+  const float S = warp_sum((tm == -INFINITY) ? 0.0f : ts * expf(tm - M));
+  const float lse = (M == -INFINITY) ? -INFINITY : M + logf(S);
+  if (lane == 0) {
+    a.lse[row] = lse;
+    if (a.sel) {
+      const int t = a.sel[row];
+      float v = __int_as_float(0x7fc00000);  // NaN: no selected token / out of range
+      if (t >= 0 && t < a.V)
+        v = a.parts.sel_logit[row] - lse;
+      else if (t != -1)
+        set_status(a.dev_status, LMH_DS_SEL_OUT_OF_RANGE);
+      a.sel_logprob[row] = v;
+    }
+  }
+  if (a.k_max == 0) return;
+  int k = a.k_max;
+  if (a.row_k) k = min(max(a.row_k[row], 0), a.k_max);
+  int32_t* out_ids = a.topk_ids + static_cast<int64_t>(row) * a.k_max;
+  float* out_lp = a.topk_logprobs + static_cast<int64_t>(row) * a.k_max;
+  if (k == 0) {
+    for (int r = lane; r < a.k_max; r += 32) {
+      out_ids[r] = -1;
+      out_lp[r] = -INFINITY;
+    }
+    return;
+  }
+  const unsigned long long* keys = a.parts.part_keys + static_cast<int64_t>(row) * a.splits * a.k_max;
+
+  // ---- lb: the k-th largest of the slots' q leading keys (q = ceil(k / nslots)) ----
+  const int q = (k + nslots - 1) / nslots;
+  const int nu = q * nslots;  // <= nslots * k <= kWarpItems
+  for (int i = lane; i < nu; i += 32) {
+    const int j = i / q;
+    buf[i] = keys[static_cast<int64_t>(j) * a.k_max + (i - j * q)];
+  }
+  __syncwarp();
+  uint64_t lb = 0;
+  for (int base = 0; base < nu; base += 32) {
+    const int i = base + lane;
+    uint64_t key = 0;
+    bool hit = false;
+    if (i < nu) {
+      key = buf[i];
+      int rank = 0;  // by key desc, then position asc
+      for (int j = 0; j < nu; ++j) {
+        const uint64_t o = buf[j];
+        rank += (o > key) | ((o == key) & (j < i));
+      }
+      hit = rank == k - 1;
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, hit);
+    if (m) lb = __shfl_sync(0xffffffffu, key, __ffs(m) - 1);
+  }
+  __syncwarp();
+
+  // ---- gather the keys >= lb (loads first, then a ballot compaction) ----
+  const int n_items = nslots * k;
+  constexpr int kPer = kWarpItems / 32;
+  uint64_t kv[kPer];
+#pragma unroll
+  for (int t = 0; t < kPer; ++t) {
+    const int i = lane + 32 * t;
+    kv[t] = 0;
+    if (i < n_items) {
+      const int j = i / k;
+      kv[t] = keys[static_cast<int64_t>(j) * a.k_max + (i - j * k)];
+    }
+  }
+  int cnt = 0;
+#pragma unroll
+  for (int t = 0; t < kPer; ++t) {
+    const bool pass = kv[t] != 0ull && kv[t] >= lb;
+    const unsigned m = __ballot_sync(0xffffffffu, pass);
+    if (pass) buf[cnt + __popc(m & ((1u << lane) - 1u))] = kv[t];
+    cnt += __popc(m);
+  }
+  __syncwarp();
+  // ---- exact order by rank (keys are unique) ----
+  for (int i = lane; i < cnt; i += 32) {
+    const uint64_t key = buf[i];
+    int rank = 0;
+    for (int j = 0; j < cnt; ++j) rank += buf[j] > key;
+    if (rank < k) {
+      out_ids[rank] = key_id(key);
+      out_lp[rank] = key_value(key) - lse;
+    }
+  }
+  for (int r = min(cnt, k) + lane; r < a.k_max; r += 32) {  // ranks without a candidate, and ranks >= k
+    out_ids[r] = -1;
+    out_lp[r] = -INFINITY;
+  }
+}
+
 cudaError_t merge_setup() { return cudaSuccess; }
 
 cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts, const int32_t* sel,
@@ -170,6 +321,9 @@ cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts,
   a.topk_ids = topk_ids;
   a.topk_logprobs = topk_logprobs;
   a.dev_status = dev_status;
+  if (flat_per == 0 && static_cast<int64_t>(splits) * k_max <= kWarpItems)
+    return launch_kernel(merge_partials_warp_kernel, dim3((rows + kWarpRowsPerCta - 1) / kWarpRowsPerCta),
+                         dim3(kWarpRowsPerCta * 32), 0, stream, pdl, a);
   return launch_kernel(merge_partials_kernel, dim3(rows), dim3(kMergeThreads), 0, stream, pdl, a);
 }
 
