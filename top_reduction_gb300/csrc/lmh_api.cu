@@ -56,6 +56,8 @@ Partials carve_partials(void* base, int rows, int splits, int k_max) {
   out.part_keys = reinterpret_cast<unsigned long long*>(p);
   p += align256(rs * static_cast<size_t>(k_max) * 8);
   out.sel_logit = reinterpret_cast<float*>(p);
+  out.bmax = nullptr;
+  out.ticket = nullptr;
   return out;
 }
 

@@ -22,8 +22,10 @@ struct VocabSplit {
   int splits;    // row pieces per row, at most
   int per;       // 64-blocks per range
   int n_ranges;  // ranges in total
-  int grid;      // persistent CTAs of the stream kernel (two per SM)
+  int grid;      // persistent CTAs of the register-path stream kernel (one range each)
+  int ctas;      // resident CTAs of a stream kernel: two per SM
   int nblk;      // 64-blocks per row
+  int slots;     // (m, s) slots per row in the workspace (enough for either stream kernel)
 };
 
 // Per-(row, split) partial results, laid out in the caller's workspace:
@@ -34,6 +36,7 @@ struct Partials {
   float2* part_ms;
   unsigned long long* part_keys;
   float* sel_logit;
+  unsigned int* ticket;  // standalone reduction: chunk counter of the dynamic schedule (else unused)
   float* bmax;  // standalone reduction: block maxima [rows * nblk] (else unused)
 };
 
@@ -59,9 +62,8 @@ cudaError_t launch_select_rows(const int32_t* cu, int num_seqs, int num_decode, 
                                int max_out, int32_t* row_idx, int32_t* logits_cu, uint32_t* dev_status,
                                cudaStream_t stream);
 
-// Workspace of the standalone reduction: part_ms [rows * splits * 8] (one
-// (m, s) pair per consumer warp and row piece), sel_logit [rows], bmax
-// [rows * nblk].
+// Workspace of the standalone reduction: part_ms [rows * slots], sel_logit
+// [rows], bmax [rows * nblk], the chunk counter.
 size_t stream_partials_bytes(int rows, const VocabSplit& vs);
 Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs);
 

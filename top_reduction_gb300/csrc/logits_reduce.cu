@@ -6,28 +6,31 @@
 // by ascending token id.
 //
 // GB300 design, two kernels:
-//   * a stream kernel reads every logit once.  A persistent grid splits the
-//     flattened (row, 64-block) space of the whole chunk into equal
-//     contiguous ranges, so every CTA streams the same number of bytes
-//     whatever the row length.  For every 64-block it writes the block's
-//     maximum to the workspace, and it folds the logits into running
-//     (max m, sum exp(x - m)) pairs, one pair per warp and row piece.  It
-//     also picks up the selected token's logit.
+//   * a stream kernel reads every logit once, as a persistent grid (two CTAs
+//     per SM) over the whole chunk, so the work per CTA does not depend on
+//     the row length.  For every 64-block it writes the block's maximum to
+//     the workspace, and it folds the logits into (max m, sum exp(x - m))
+//     pairs.  It also picks up the selected token's logit.
 //       - logits_stream_tma_kernel (rows and the row length 16-byte
-//         aligned): one producer lane streams 32 KB chunks of one row into a
-//         ring of shared-memory stages with bulk copies (cp.async.bulk,
-//         completion on mbarriers); eight consumer warps read them, each
-//         thread owning 128 contiguous bytes (one bf16/f16 block, half an f32
-//         block), so a block's maximum needs no exchange between lanes.
-//       - logits_stream_regs_kernel (any element-aligned layout): every thread
-//         loads 16-byte vectors (or elements at unaligned rows) straight into
-//         registers, two chunks in flight; the lanes of a block combine their
-//         maxima by shuffles.
+//         aligned): the logits are cut into 32 KB chunks of one row, handed
+//         out dynamically (a ticket counter), so CTAs that get more bandwidth
+//         take more chunks.  One producer lane streams its chunks into a ring
+//         of shared-memory stages with bulk copies (cp.async.bulk, completion
+//         on mbarriers); eight consumer warps read them, each thread owning
+//         128 contiguous bytes (one bf16/f16 block, half an f32 block), so a
+//         block's maximum needs no exchange between lanes; one (m, s) pair
+//         per warp and chunk.
+//       - logits_stream_regs_kernel (any element-aligned layout): the
+//         flattened (row, 64-block) space is cut into equal contiguous
+//         ranges, one per CTA; every thread loads 16-byte vectors (or
+//         elements at unaligned rows) straight into registers, two chunks in
+//         flight; the lanes of a block combine their maxima by shuffles; one
+//         (m, s) pair per row piece.
 //   * logits_select_kernel -- one CTA per row: lse from the row's (m, s)
-//     pairs; a lower bound t on the row's k-th largest logit from the block
-//     maxima; candidates = entries >= t of the blocks whose maximum is >= t,
-//     re-read from memory; their exact top-k by key (value desc, id asc),
-//     ordered by rank.
+//     pairs (one warp); a lower bound t on the row's k-th largest logit from
+//     the block maxima; candidates = entries >= t of the blocks whose maximum
+//     is >= t, re-read from memory by the warp that owns the block; their
+//     exact top-k by key (value desc, id asc), ordered by rank.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -51,8 +54,6 @@ constexpr int kTChunkBytes = kTConsumers * 128;  // 128 contiguous bytes per con
 constexpr int kTStages = 3;  // per CTA; two CTAs per SM
 constexpr int kTDescBytes = 32;
 constexpr int kTSmem = kTStages * kTChunkBytes + kTStages * kTDescBytes + 2 * kTStages * 8 + 16;
-// (m, s) slots reserved per row piece: one per consumer warp of the TMA path
-constexpr int kSlotsPerPiece = kTConsumerWarps;
 
 template <typename T>
 struct Vec16;  // 16-byte vector of T widened to fp32
@@ -187,8 +188,8 @@ struct ReduceArgs {
   int64_t nb_total;    // rows * nblk
   int per;             // blocks per range
   int n_ranges;
-  int P;               // (m, s) slots per row: kSlotsPerPiece per row piece
-  int W;               // slots a row piece fills: kTConsumerWarps (TMA path) or 1
+  int P;               // (m, s) slots per row in the workspace
+  int cpr;             // TMA path: chunks per row (a row fills cpr * kTConsumerWarps slots); 0: register path
   bool vec_ok;         // rows and the row length are 16-byte aligned
   const int32_t* sel;
   const int32_t* row_k;
@@ -253,10 +254,10 @@ struct ChunkIter {
   __device__ bool piece_ended() const { return left == 0 || lb == 0; }
 };
 
-// Index of a row piece's first (m, s) slot: row * P + (range - first range of the row) * W.
+// Register path: the (m, s) slot of a row piece, row * P + (range - first range of the row).
 __device__ __forceinline__ int64_t piece_slot(const ReduceArgs& a, int row, int range) {
   const int first = static_cast<int>((static_cast<int64_t>(row) * a.nblk) / a.per);
-  return static_cast<int64_t>(row) * a.P + static_cast<int64_t>(range - first) * a.W;
+  return static_cast<int64_t>(row) * a.P + (range - first);
 }
 
 // ---------------------------------------------------------------------------
@@ -267,9 +268,8 @@ struct StreamDesc {  // one per stage, written by the producer before the copy i
   int lb;            // first 64-block of the chunk within the row
   int nbk;           // blocks in the chunk
   int ne;            // real logits in the chunk (the copied ones)
-  int64_t slot;      // first (m, s) slot of the chunk's row piece
+  int64_t slot;      // first (m, s) slot of the chunk: one per consumer warp
   int sel_rel;       // selected token relative to the chunk's first logit
-  int piece_end;     // the chunk is the last of its row piece
 };
 static_assert(sizeof(StreamDesc) <= kTDescBytes, "descriptor slot");
 
@@ -304,37 +304,47 @@ __global__ void __launch_bounds__(kTThreads, 2) logits_stream_tma_kernel(const R
 
   if (warp == kTConsumerWarps) {
     // ------------------------------ producer ------------------------------
+    // Chunks (CH blocks of one row; chunk c is row c / cpr, part c % cpr) are
+    // handed out dynamically, so CTAs that stream faster take more of them:
+    // the first S of a CTA are fixed (blockIdx.x + j * gridDim.x), the rest
+    // come from the ticket counter, drawn one chunk ahead.
     if (lane != 0) return;
-    ChunkIter<CH> it;
-    it.init(a);
+    const int64_t total = static_cast<int64_t>(a.rows) * a.cpr;
+    const int64_t first_dynamic = static_cast<int64_t>(S) * gridDim.x;
     uint32_t issued = 0;
+    int64_t next = blockIdx.x;
     int sel_row = -1, sel_id = -1;
     for (;; ++issued) {
       const int s = static_cast<int>(issued % S);
       if (issued >= static_cast<uint32_t>(S) &&
           !wait_or_abort(&empty[s], ((issued / S) & 1u) ^ 1u, abort_flag, a.dev_status))
         break;
-      const Chunk c = it.next(a);
+      const int64_t c = next;
       StreamDesc& d = desc[s];
-      if (!c.valid) {
+      if (c >= total) {
         d.row = -1;
         mbar_arrive(&full[s]);  // end marker: completes with no bytes
         ++issued;
         break;
       }
-      if (c.row != sel_row) {
-        sel_row = c.row;
-        sel_id = a.sel ? a.sel[c.row] : -1;
+      next = issued + 1 < static_cast<uint32_t>(S) ? blockIdx.x + static_cast<int64_t>(issued + 1) * gridDim.x
+                                                   : first_dynamic + atomicAdd(a.parts.ticket, 1u);
+      const int row = static_cast<int>(c / a.cpr);
+      const int ci = static_cast<int>(c - static_cast<int64_t>(row) * a.cpr);
+      const int lb = ci * CH;
+      const int nbk = min(CH, a.nblk - lb);
+      if (row != sel_row) {
+        sel_row = row;
+        sel_id = a.sel ? a.sel[row] : -1;
       }
-      const int ne = min(c.nbk * kBlock, a.V - c.lb * kBlock);
-      d.row = c.row;
-      d.lb = c.lb;
-      d.nbk = c.nbk;
+      const int ne = min(nbk * kBlock, a.V - lb * kBlock);
+      d.row = row;
+      d.lb = lb;
+      d.nbk = nbk;
       d.ne = ne;
-      d.slot = piece_slot(a, c.row, c.range);
-      d.sel_rel = sel_id - c.lb * kBlock;
-      d.piece_end = it.piece_ended() ? 1 : 0;
-      const char* src = a.logits + (static_cast<int64_t>(c.row) * a.row_stride + static_cast<int64_t>(c.lb) * kBlock) * ES;
+      d.slot = static_cast<int64_t>(row) * a.P + static_cast<int64_t>(ci) * kTConsumerWarps;
+      d.sel_rel = sel_id - lb * kBlock;
+      const char* src = a.logits + (static_cast<int64_t>(row) * a.row_stride + static_cast<int64_t>(lb) * kBlock) * ES;
       mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(ne * ES));
       bulk_load(stages + static_cast<size_t>(s) * kTChunkBytes, src, static_cast<uint32_t>(ne * ES), &full[s]);
     }
@@ -349,7 +359,6 @@ __global__ void __launch_bounds__(kTThreads, 2) logits_stream_tma_kernel(const R
   const int rot = c & 7;  // vector order rotated by lane: conflict-free 16-byte shared loads
   const int bi = c / TPB;
   const float L = kLog2e;
-  float tm = -INFINITY, ts = 0.0f;  // running max / sum of this thread over the current row piece
   for (uint32_t i = 0;; ++i) {
     const int s = static_cast<int>(i % S);
     bool ok = wait_or_abort(&full[s], (i / S) & 1u, abort_flag, a.dev_status);
@@ -373,18 +382,15 @@ __global__ void __launch_bounds__(kTThreads, 2) logits_stream_tma_kernel(const R
       for (int j = 0; j < 8; ++j)
         if (((j + rot) & 7) * EPV >= ne_t) w[j] = make_uint4(VT::kNegInfWord, VT::kNegInfWord, VT::kNegInfWord, VT::kNegInfWord);
     }
-    const float vm = VT::max8(w);
+    const float vm = VT::max8(w);  // this thread's maximum
     float bmx = vm;
     if (TPB == 2) bmx = fmaxf(bmx, __shfl_xor_sync(0xffffffffu, bmx, 1));
     if ((c % TPB) == 0 && bi < d.nbk) a.parts.bmax[static_cast<int64_t>(d.row) * a.nblk + d.lb + bi] = bmx;
+    float ts = 0.0f;  // sum of exp(x - vm) over this thread's logits
     if (vm > -INFINITY) {
-      if (vm > tm) {
-        ts *= ex2_approx((tm - vm) * L);  // tm = -inf: ts is 0 and stays 0
-        tm = vm;
-      }
       // exp(x - m) = 2^(x*log2e - m*log2e): one packed FFMA2 and one packed
       // FADD2 per pair of logits around the two ex2
-      const float2 L2 = make_float2(L, L), nmL2 = make_float2(-tm * L, -tm * L);
+      const float2 L2 = make_float2(L, L), nmL2 = make_float2(-vm * L, -vm * L);
       float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
                        make_float2(0.0f, 0.0f)};
 #pragma unroll
@@ -399,15 +405,12 @@ __global__ void __launch_bounds__(kTThreads, 2) logits_stream_tma_kernel(const R
       }
       const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
       const float2 a = __fadd2_rn(a01, a23);
-      ts += a.x + a.y;
+      ts = a.x + a.y;
     }
-    if (d.piece_end) {
-      const float M = warp_max(tm);
-      const float sc = warp_sum(tm == -INFINITY ? 0.0f : ts * ex2_approx((tm - M) * L));
-      if (lane == 0) a.parts.part_ms[d.slot + warp] = make_float2(M, M == -INFINITY ? 0.0f : sc);
-      tm = -INFINITY;
-      ts = 0.0f;
-    }
+    // the warp's (m, s) over this chunk
+    const float M = warp_max(vm);
+    const float sc = warp_sum(vm == -INFINITY ? 0.0f : ts * ex2_approx((vm - M) * L));
+    if (lane == 0) a.parts.part_ms[d.slot + warp] = make_float2(M, M == -INFINITY ? 0.0f : sc);
   }
 }
 
@@ -532,9 +535,10 @@ __global__ void __launch_bounds__(kRThreads, kRCtasPerSm) logits_stream_regs_ker
 // ---------------------------------------------------------------------------
 constexpr int kSThreads = 256;
 constexpr int kSWarps = kSThreads / 32;
-constexpr int kSKeptCap = 1024;  // kept blocks held in shared memory
 constexpr int kSCandCap = 512;   // candidate keys held in shared memory
 
+constexpr int kSWarpKept = 64;   // kept blocks listed per warp
+constexpr int kSGather = 4;      // candidate vectors per lane in flight
 constexpr int kSBatch = 16;      // block maxima per thread loaded per round (rows of <= 4096 blocks: one)
 
 // Lower bound on the k-th largest logit of a row from its block maxima.
@@ -568,15 +572,15 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
   constexpr int EPV = VT::N;
   constexpr int VPB = kBlock / EPV;
   __shared__ uint64_t cand[kSCandCap];
-  __shared__ int kept[kSKeptCap];
   __shared__ uint32_t hist[256];
-  __shared__ uint32_t misc[4];  // [0] candidates, [1..2] select broadcast, [3] kept blocks
-  __shared__ float red[32];
+  __shared__ uint32_t misc[4];  // [0] candidates, [1..2] select broadcast, [3] kept-list overflow
   __shared__ float wq[kSWarps];
+  __shared__ int wkept[kSWarps][kSWarpKept];
+  __shared__ float s_lse;
   pdl_wait();  // the block maxima and (m, s) come from the stream kernel just before
 
   const int row = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t b0 = static_cast<int64_t>(row) * a.nblk;
   // The row's block maxima: loaded first, so that their latency overlaps the
   // lse; kept in registers when one round covers the row.
@@ -591,34 +595,38 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
       bv[i] = b < nb ? bm[b] : -INFINITY;
     }
   }
-  // ---- lse over the row's (m, s) slots ----
-  const int nslots = static_cast<int>((b0 + a.nblk - 1) / a.per - b0 / a.per + 1) * a.W;
-  const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.P;
-  float tm = -INFINITY, ts = 0.0f;
-  for (int j = tid; j < nslots; j += kSThreads) {
-    const float2 p = ms[j];
-    if (p.x > tm) {
-      ts = (tm == -INFINITY) ? 0.0f : ts * expf(tm - p.x);
-      tm = p.x;
+  // ---- lse over the row's (m, s) slots: warp 0, while the others go on ----
+  if (warp == 0) {
+    const int nslots = a.cpr > 0 ? a.cpr * kTConsumerWarps
+                                 : static_cast<int>((b0 + a.nblk - 1) / a.per - b0 / a.per + 1);
+    const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.P;
+    float tm = -INFINITY, ts = 0.0f;
+    for (int j = lane; j < nslots; j += 32) {
+      const float2 p = ms[j];
+      if (p.x > tm) {
+        ts = (tm == -INFINITY) ? 0.0f : ts * expf(tm - p.x);
+        tm = p.x;
+      }
+      if (p.x != -INFINITY) ts += p.y * expf(p.x - tm);
     }
-    if (p.x != -INFINITY) ts += p.y * expf(p.x - tm);
-  }
-  const float M = block_max(tm, red);
-  const float S = block_sum((tm == -INFINITY) ? 0.0f : ts * expf(tm - M), red);
-  const float lse = (M == -INFINITY) ? -INFINITY : M + logf(S);
-  if (tid == 0) {
-    lse_out[row] = lse;
-    if (a.sel) {
-      const int t = a.sel[row];
-      float v = __int_as_float(0x7fc00000);  // NaN: no selected token / out of range
-      if (t >= 0 && t < a.V)
-        v = a.parts.sel_logit[row] - lse;
-      else if (t != -1)
-        set_status(a.dev_status, LMH_DS_SEL_OUT_OF_RANGE);
-      sel_logprob[row] = v;
+    const float M = warp_max(tm);
+    const float S = warp_sum((tm == -INFINITY) ? 0.0f : ts * expf(tm - M));
+    const float lse = (M == -INFINITY) ? -INFINITY : M + logf(S);
+    if (lane == 0) {
+      s_lse = lse;
+      lse_out[row] = lse;
+      if (a.sel) {
+        const int t = a.sel[row];
+        float v = __int_as_float(0x7fc00000);  // NaN: no selected token / out of range
+        if (t >= 0 && t < a.V)
+          v = a.parts.sel_logit[row] - lse;
+        else if (t != -1)
+          set_status(a.dev_status, LMH_DS_SEL_OUT_OF_RANGE);
+        sel_logprob[row] = v;
+      }
+      misc[0] = 0;
+      misc[3] = 0;
     }
-    misc[0] = 0;
-    misc[3] = 0;
   }
   if (a.k_max == 0) return;
   int k = a.k_max;
@@ -633,7 +641,7 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
     return;
   }
 
-  // ---- t <= the k-th largest logit; kept blocks: maximum >= t ----
+  // ---- t <= the k-th largest logit ----
   float tmax = -INFINITY;  // never NaN: fmaxf drops NaN block maxima
   if (one_round) {
 #pragma unroll
@@ -650,16 +658,26 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
       for (int i = 0; i < kSBatch; ++i) tmax = fmaxf(tmax, v[i]);
     }
   }
-  const float t = topk_lower_bound(tmax, k, wq);
-  auto keep = [&](int b, float v) {
-    if (b < nb && v >= t) {
-      const uint32_t pos = atomicAdd(&misc[3], 1u);
-      if (pos < kSKeptCap) kept[pos] = b;
+  const float t = topk_lower_bound(tmax, k, wq);  // (its barrier also publishes s_lse and misc[0])
+
+  // ---- kept blocks (maximum >= t), listed per warp; the warp gathers their entries >= t ----
+  const T* rowp = reinterpret_cast<const T*>(a.logits) + static_cast<int64_t>(row) * a.row_stride;
+  int* wk = wkept[warp];
+  int nk = 0;  // the warp's kept blocks (uniform across the warp)
+  auto add_kept = [&](int b, bool keep) {
+    const unsigned m = __ballot_sync(0xffffffffu, keep);
+    if (keep) {
+      const int pos = nk + __popc(m & ((1u << lane) - 1u));
+      if (pos < kSWarpKept) wk[pos] = b;
     }
+    nk += __popc(m);
   };
   if (one_round) {
 #pragma unroll
-    for (int i = 0; i < kSBatch; ++i) keep(tid + i * kSThreads, bv[i]);
+    for (int i = 0; i < kSBatch; ++i) {
+      const int b = tid + i * kSThreads;
+      add_kept(b, b < nb && bv[i] >= t);
+    }
   } else {
     for (int base = 0; base < nb; base += kSBatch * kSThreads) {
       float v[kSBatch];
@@ -669,48 +687,61 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
         v[i] = b < nb ? bm[b] : -INFINITY;
       }
 #pragma unroll
-      for (int i = 0; i < kSBatch; ++i) keep(base + tid + i * kSThreads, v[i]);
+      for (int i = 0; i < kSBatch; ++i) {
+        const int b = base + tid + i * kSThreads;
+        add_kept(b, b < nb && v[i] >= t);
+      }
+    }
+  }
+  __syncwarp();
+  auto add_cand = [&](float x, int e) {
+    if (x >= t) {
+      const uint32_t pos = atomicAdd(&misc[0], 1u);
+      if (pos < kSCandCap) cand[pos] = make_key(x, e);
+    }
+  };
+  if (nk > kSWarpKept) {
+    if (lane == 0) misc[3] = 1;  // more kept blocks than the list holds: exact path below
+  } else if (a.vec_ok) {
+    // 16-byte vectors of the kept blocks, kSGather per lane in flight; none straddles the row end
+    const int n_vec = nk * VPB;
+    for (int base = 0; base < n_vec; base += kSGather * 32) {
+      uint4 w[kSGather];
+      int e0[kSGather];
+#pragma unroll
+      for (int u = 0; u < kSGather; ++u) {
+        const int j = base + u * 32 + lane;
+        e0[u] = -1;
+        if (j < n_vec) {
+          const int e = wk[j / VPB] * kBlock + (j % VPB) * EPV;
+          if (e < a.V) {
+            e0[u] = e;
+            w[u] = *reinterpret_cast<const uint4*>(rowp + e);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kSGather; ++u) {
+        if (e0[u] < 0) continue;
+        float x[EPV];
+        VT::unpack(w[u], x);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) add_cand(x[e], e0[u] + e);
+      }
+    }
+  } else {
+    const int n_el = nk * kBlock;
+    for (int j = lane; j < n_el; j += 32) {
+      const int e = wk[j / kBlock] * kBlock + (j % kBlock);
+      if (e < a.V) add_cand(VT::at(rowp, e), e);
     }
   }
   __syncthreads();
-  const int nkept = static_cast<int>(misc[3]);
-  const T* rowp = reinterpret_cast<const T*>(a.logits) + static_cast<int64_t>(row) * a.row_stride;
-  int cnt;
-  if (nkept <= kSKeptCap) {
-    // the kept blocks' entries >= t: every load of the CTA in one round
-    if (a.vec_ok) {  // whole 16-byte vectors; none straddles the row end
-      const int n_vec = nkept * VPB;
-      for (int i = tid; i < n_vec; i += kSThreads) {
-        const int e0 = kept[i / VPB] * kBlock + (i % VPB) * EPV;
-        if (e0 >= a.V) continue;
-        float x[EPV];
-        VT::load(rowp + e0, x);
-#pragma unroll
-        for (int e = 0; e < EPV; ++e)
-          if (x[e] >= t) {
-            const uint32_t pos = atomicAdd(&misc[0], 1u);
-            if (pos < kSCandCap) cand[pos] = make_key(x[e], e0 + e);
-          }
-      }
-    } else {
-      const int n_el = nkept * kBlock;
-      for (int i = tid; i < n_el; i += kSThreads) {
-        const int e = kept[i / kBlock] * kBlock + (i % kBlock);
-        if (e >= a.V) continue;
-        const float x = VT::at(rowp, e);
-        if (x >= t) {
-          const uint32_t pos = atomicAdd(&misc[0], 1u);
-          if (pos < kSCandCap) cand[pos] = make_key(x, e);
-        }
-      }
-    }
-    __syncthreads();
-    cnt = static_cast<int>(misc[0]);
-  } else {
-    cnt = kSCandCap + 1;  // too many blocks reach t (ties, -inf rows): take the exact path
-  }
-  if (cnt > kSCandCap) {
-    // exact k-th key over the entries >= t of blocks reaching t, then the k keys at or above it
+  int cnt = static_cast<int>(misc[0]);
+  const float lse = s_lse;
+  if (cnt > kSCandCap || misc[3] != 0) {
+    // too many entries reach t (ties, rows of -inf): the exact k-th key over
+    // them, then the k keys at or above it
     auto in_set = [&](int i, uint64_t* key) -> bool {
       if (i >= a.V || !(bm[i / kBlock] >= t)) return false;
       const float x = VT::at(rowp, i);
@@ -768,8 +799,12 @@ VocabSplit logits_reduce_split(int rows, int V, int k_max, int num_sms) {
   vs.per = static_cast<int>(per);
   vs.n_ranges = static_cast<int>((nb_total + per - 1) / per);
   vs.grid = static_cast<int>(vs.n_ranges < G ? vs.n_ranges : G);
+  vs.ctas = static_cast<int>(G);
   vs.splits = static_cast<int>((nblk + per - 1) / per) + 1;  // row pieces per row, at most
   vs.nblk = nblk;
+  // TMA path: 8 slots per chunk; the smallest chunk (f32) has kTChunkBytes / 256 blocks
+  const int cpr_max = (nblk + kTChunkBytes / 256 - 1) / (kTChunkBytes / 256);
+  vs.slots = cpr_max * kTConsumerWarps > vs.splits ? cpr_max * kTConsumerWarps : vs.splits;
   return vs;
 }
 
@@ -785,8 +820,8 @@ cudaError_t logits_reduce_setup() {
 
 size_t stream_partials_bytes(int rows, const VocabSplit& vs) {
   auto al = [](size_t n) { return (n + 255) & ~static_cast<size_t>(255); };
-  return al(static_cast<size_t>(rows) * vs.splits * kSlotsPerPiece * 8) + al(static_cast<size_t>(rows) * 4) +
-         al(static_cast<size_t>(rows) * vs.nblk * 4);
+  return al(static_cast<size_t>(rows) * vs.slots * 8) + al(static_cast<size_t>(rows) * 4) +
+         al(static_cast<size_t>(rows) * vs.nblk * 4) + al(4);
 }
 
 Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs) {
@@ -794,10 +829,12 @@ Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs) {
   char* p = static_cast<char*>(base);
   Partials out;
   out.part_ms = reinterpret_cast<float2*>(p);
-  p += al(static_cast<size_t>(rows) * vs.splits * kSlotsPerPiece * 8);
+  p += al(static_cast<size_t>(rows) * vs.slots * 8);
   out.sel_logit = reinterpret_cast<float*>(p);
   p += al(static_cast<size_t>(rows) * 4);
   out.bmax = reinterpret_cast<float*>(p);
+  p += al(static_cast<size_t>(rows) * vs.nblk * 4);
+  out.ticket = reinterpret_cast<unsigned int*>(p);
   out.part_keys = nullptr;
   return out;
 }
@@ -808,11 +845,16 @@ static cudaError_t launch_both(ReduceArgs a, const VocabSplit& split, float* lse
   cudaError_t e;
   trace_begin(kTraceReduce, stream);
   if (a.vec_ok) {
-    a.W = kTConsumerWarps;
-    e = launch_kernel(logits_stream_tma_kernel<T>, dim3(split.grid), dim3(kTThreads), static_cast<size_t>(kTSmem),
-                      stream, false, a);
+    constexpr int CH = kTChunkBytes / (kBlock * static_cast<int>(sizeof(T)));  // blocks per chunk
+    a.cpr = (a.nblk + CH - 1) / CH;
+    const int64_t chunks = static_cast<int64_t>(a.rows) * a.cpr;
+    const int grid = static_cast<int>(chunks < split.ctas ? chunks : split.ctas);
+    e = cudaMemsetAsync(a.parts.ticket, 0, sizeof(unsigned int), stream);
+    if (e == cudaSuccess)
+      e = launch_kernel(logits_stream_tma_kernel<T>, dim3(grid), dim3(kTThreads), static_cast<size_t>(kTSmem), stream,
+                        false, a);
   } else {
-    a.W = 1;
+    a.cpr = 0;
     e = launch_kernel(logits_stream_regs_kernel<T>, dim3(split.grid), dim3(kRThreads), 0, stream, false, a);
   }
   trace_end(kTraceReduce, stream);
@@ -838,8 +880,8 @@ cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t ro
   a.nb_total = static_cast<int64_t>(rows) * split.nblk;
   a.per = split.per;
   a.n_ranges = split.n_ranges;
-  a.P = split.splits * kSlotsPerPiece;
-  a.W = 1;
+  a.P = split.slots;
+  a.cpr = 0;
   a.vec_ok = (reinterpret_cast<uintptr_t>(logits) % 16) == 0 && ((row_stride * es) % 16) == 0 &&
              ((static_cast<int64_t>(V) * es) % 16) == 0;
   a.sel = sel;
