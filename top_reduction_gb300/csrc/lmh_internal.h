@@ -23,7 +23,7 @@ struct VocabSplit {
   int per;       // 64-blocks per range
   int n_ranges;  // ranges in total
   int grid;      // persistent CTAs of the register-path stream kernel (one range each)
-  int ctas;      // resident CTAs of a stream kernel: two per SM
+  int ctas;      // persistent CTAs of the TMA-path stream kernel (four per SM)
   int nblk;      // 64-blocks per row
   int slots;     // (m, s) slots per row in the workspace (enough for either stream kernel)
 };

@@ -6,26 +6,26 @@
 // by ascending token id.
 //
 // GB300 design, two kernels:
-//   * a stream kernel reads every logit once, as a persistent grid (two CTAs
-//     per SM) over the whole chunk, so the work per CTA does not depend on
-//     the row length.  For every 64-block it writes the block's maximum to
-//     the workspace, and it folds the logits into (max m, sum exp(x - m))
-//     pairs.  It also picks up the selected token's logit.
+//   * a stream kernel reads every logit once, as a persistent grid over the
+//     whole chunk, so the work per CTA does not depend on the row length.
+//     For every 64-block it writes the block's maximum to the workspace, and
+//     it folds the logits into (max m, sum exp(x - m)) pairs.  It also picks
+//     up the selected token's logit.
 //       - logits_stream_tma_kernel (rows and the row length 16-byte
-//         aligned): the logits are cut into 32 KB chunks of one row, handed
-//         out dynamically (a ticket counter), so CTAs that get more bandwidth
-//         take more chunks.  One producer lane streams its chunks into a ring
-//         of shared-memory stages with bulk copies (cp.async.bulk, completion
-//         on mbarriers); eight consumer warps read them, each thread owning
-//         128 contiguous bytes (one bf16/f16 block, half an f32 block), so a
-//         block's maximum needs no exchange between lanes; one (m, s) pair
-//         per warp and chunk.
-//       - logits_stream_regs_kernel (any element-aligned layout): the
-//         flattened (row, 64-block) space is cut into equal contiguous
-//         ranges, one per CTA; every thread loads 16-byte vectors (or
-//         elements at unaligned rows) straight into registers, two chunks in
-//         flight; the lanes of a block combine their maxima by shuffles; one
-//         (m, s) pair per row piece.
+//         aligned; four CTAs per SM): the logits are cut into 16 KB chunks
+//         of one row, handed out dynamically (a ticket counter), so CTAs that
+//         get more bandwidth take more chunks.  One producer lane streams its
+//         chunks into a ring of shared-memory stages with bulk copies
+//         (cp.async.bulk, completion on mbarriers); four consumer warps read
+//         them, each thread owning 128 contiguous bytes (one bf16/f16 block,
+//         half an f32 block), so a block's maximum needs no exchange between
+//         lanes; one (m, s) pair per warp and chunk.
+//       - logits_stream_regs_kernel (any element-aligned layout; two CTAs
+//         per SM): the flattened (row, 64-block) space is cut into equal
+//         contiguous ranges, one per CTA; every thread loads 16-byte vectors
+//         (or elements at unaligned rows) straight into registers, two
+//         chunks in flight; the lanes of a block combine their maxima by
+//         shuffles; one (m, s) pair per row piece.
 //   * logits_select_kernel -- one CTA per row: lse from the row's (m, s)
 //     pairs (one warp); a lower bound t on the row's k-th largest logit from
 //     the block maxima; candidates = entries >= t of the blocks whose maximum
@@ -47,11 +47,12 @@ constexpr int kRCtasPerSm = 2;
 constexpr int kRMaxPer = 4096;  // blocks per range, at most
 constexpr int kRMinPer = 32;    // >= 2048 logits per range
 // TMA-path stream kernel
-constexpr int kTConsumerWarps = 8;
+constexpr int kTConsumerWarps = 4;
 constexpr int kTConsumers = kTConsumerWarps * 32;
 constexpr int kTThreads = kTConsumers + 32;  // + one producer warp
 constexpr int kTChunkBytes = kTConsumers * 128;  // 128 contiguous bytes per consumer thread
-constexpr int kTStages = 3;  // per CTA; two CTAs per SM
+constexpr int kTStages = 3;
+constexpr int kTCtasPerSm = 4;
 constexpr int kTDescBytes = 32;
 constexpr int kTSmem = kTStages * kTChunkBytes + kTStages * kTDescBytes + 2 * kTStages * 8 + 16;
 
@@ -274,7 +275,7 @@ struct StreamDesc {  // one per stage, written by the producer before the copy i
 static_assert(sizeof(StreamDesc) <= kTDescBytes, "descriptor slot");
 
 template <typename T>
-__global__ void __launch_bounds__(kTThreads, 2) logits_stream_tma_kernel(const ReduceArgs a) {
+__global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kernel(const ReduceArgs a) {
   using VT = Vec16<T>;
   constexpr int ES = static_cast<int>(sizeof(T));
   constexpr int EPV = VT::N;         // elements per 16-byte vector
@@ -311,6 +312,7 @@ __global__ void __launch_bounds__(kTThreads, 2) logits_stream_tma_kernel(const R
     if (lane != 0) return;
     const int64_t total = static_cast<int64_t>(a.rows) * a.cpr;
     const int64_t first_dynamic = static_cast<int64_t>(S) * gridDim.x;
+    const uint64_t policy = l2_evict_first_policy();  // logits are read once; the block maxima stay in L2
     uint32_t issued = 0;
     int64_t next = blockIdx.x;
     int sel_row = -1, sel_id = -1;
@@ -346,7 +348,8 @@ __global__ void __launch_bounds__(kTThreads, 2) logits_stream_tma_kernel(const R
       d.sel_rel = sel_id - lb * kBlock;
       const char* src = a.logits + (static_cast<int64_t>(row) * a.row_stride + static_cast<int64_t>(lb) * kBlock) * ES;
       mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(ne * ES));
-      bulk_load(stages + static_cast<size_t>(s) * kTChunkBytes, src, static_cast<uint32_t>(ne * ES), &full[s]);
+      bulk_load_hint(stages + static_cast<size_t>(s) * kTChunkBytes, src, static_cast<uint32_t>(ne * ES), &full[s],
+                     policy);
     }
     // Copies still in flight (only after an abort) land before the CTA exits.
     const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
@@ -582,8 +585,9 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
   const int row = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t b0 = static_cast<int64_t>(row) * a.nblk;
-  // The row's block maxima: loaded first, so that their latency overlaps the
-  // lse; kept in registers when one round covers the row.
+  // Every independent load first, so that their latencies overlap: the row's
+  // block maxima (kept in registers when one round covers the row), its K,
+  // the selected token and its logit, and (warp 0) the (m, s) slots.
   const int nb = a.nblk;
   const float* bm = a.parts.bmax + b0;
   const bool one_round = nb <= kSBatch * kSThreads;
@@ -595,19 +599,34 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
       bv[i] = b < nb ? bm[b] : -INFINITY;
     }
   }
+  const int k_row = a.row_k ? a.row_k[row] : a.k_max;
+  int sel_t = -1;
+  float sel_x = 0.0f;
+  if (tid == 0 && a.sel) {
+    sel_t = a.sel[row];
+    sel_x = a.parts.sel_logit[row];  // meaningful only when sel_t is in range
+  }
   // ---- lse over the row's (m, s) slots: warp 0, while the others go on ----
   if (warp == 0) {
     const int nslots = a.cpr > 0 ? a.cpr * kTConsumerWarps
                                  : static_cast<int>((b0 + a.nblk - 1) / a.per - b0 / a.per + 1);
     const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.P;
     float tm = -INFINITY, ts = 0.0f;
-    for (int j = lane; j < nslots; j += 32) {
-      const float2 p = ms[j];
-      if (p.x > tm) {
-        ts = (tm == -INFINITY) ? 0.0f : ts * expf(tm - p.x);
-        tm = p.x;
+    for (int base = 0; base < nslots; base += 4 * 32) {
+      float2 p[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = base + u * 32 + lane;
+        p[u] = j < nslots ? ms[j] : make_float2(-INFINITY, 0.0f);
       }
-      if (p.x != -INFINITY) ts += p.y * expf(p.x - tm);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (p[u].x > tm) {
+          ts = (tm == -INFINITY) ? 0.0f : ts * expf(tm - p[u].x);
+          tm = p[u].x;
+        }
+        if (p[u].x != -INFINITY) ts += p[u].y * expf(p[u].x - tm);
+      }
     }
     const float M = warp_max(tm);
     const float S = warp_sum((tm == -INFINITY) ? 0.0f : ts * expf(tm - M));
@@ -616,11 +635,10 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
       s_lse = lse;
       lse_out[row] = lse;
       if (a.sel) {
-        const int t = a.sel[row];
         float v = __int_as_float(0x7fc00000);  // NaN: no selected token / out of range
-        if (t >= 0 && t < a.V)
-          v = a.parts.sel_logit[row] - lse;
-        else if (t != -1)
+        if (sel_t >= 0 && sel_t < a.V)
+          v = sel_x - lse;
+        else if (sel_t != -1)
           set_status(a.dev_status, LMH_DS_SEL_OUT_OF_RANGE);
         sel_logprob[row] = v;
       }
@@ -629,8 +647,7 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
     }
   }
   if (a.k_max == 0) return;
-  int k = a.k_max;
-  if (a.row_k) k = min(max(a.row_k[row], 0), a.k_max);
+  const int k = min(max(k_row, 0), a.k_max);
   int32_t* out_ids = topk_ids + static_cast<int64_t>(row) * a.k_max;
   float* out_lp = topk_logprobs + static_cast<int64_t>(row) * a.k_max;
   if (k == 0) {
@@ -799,7 +816,7 @@ VocabSplit logits_reduce_split(int rows, int V, int k_max, int num_sms) {
   vs.per = static_cast<int>(per);
   vs.n_ranges = static_cast<int>((nb_total + per - 1) / per);
   vs.grid = static_cast<int>(vs.n_ranges < G ? vs.n_ranges : G);
-  vs.ctas = static_cast<int>(G);
+  vs.ctas = sms * kTCtasPerSm;
   vs.splits = static_cast<int>((nblk + per - 1) / per) + 1;  // row pieces per row, at most
   vs.nblk = nblk;
   // TMA path: 8 slots per chunk; the smallest chunk (f32) has kTChunkBytes / 256 blocks
