@@ -313,6 +313,10 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
     const int64_t total = static_cast<int64_t>(a.rows) * a.cpr;
     const int64_t first_dynamic = static_cast<int64_t>(S) * gridDim.x;
     const uint64_t policy = l2_evict_first_policy();  // logits are read once; the block maxima stay in L2
+    // The kernel may start while its predecessor (the ticket reset) still runs:
+    // wait for it before the first ticket, load or workspace write (the
+    // consumers write only data that arrived after this point).
+    pdl_wait();
     uint32_t issued = 0;
     int64_t next = blockIdx.x;
     int sel_row = -1, sel_id = -1;
@@ -415,6 +419,16 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
     const float sc = warp_sum(vm == -INFINITY ? 0.0f : ts * ex2_approx((vm - M) * L));
     if (lane == 0) a.parts.part_ms[d.slot + warp] = make_float2(M, M == -INFINITY ? 0.0f : sc);
   }
+}
+
+// Zeroes the chunk ticket before the TMA-path stream kernel.  A kernel (not a
+// memset) so that the chain previous kernel -> reset -> stream can use
+// programmatic dependent launch: it waits for its predecessor, whose work may
+// still read the workspace, and lets the stream kernel be scheduled meanwhile.
+__global__ void ticket_reset_kernel(unsigned int* ticket) {
+  pdl_launch_dependents();
+  pdl_wait();
+  if (threadIdx.x == 0) *ticket = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -553,13 +567,15 @@ constexpr int kSBatch = 16;      // block maxima per thread loaded per round (ro
 __device__ __forceinline__ float topk_lower_bound(float tmax, int k, float* wq) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int q = (k + kSWarps - 1) / kSWarps;
-  int rank = 0;  // position of (tmax, lane) in the warp, by value desc then lane asc
-#pragma unroll
-  for (int o = 0; o < 32; ++o) {
-    const float v = __shfl_sync(0xffffffffu, tmax, o);
-    rank += (v > tmax) | ((v == tmax) & (o < lane));
+  // the q-th largest of the warp's values: q rounds of (warp max, one holder drops out)
+  uint32_t key = f32_ord(tmax);  // > 0 for every value that is not NaN; 0 marks a dropped lane
+  uint32_t m = 0;
+  for (int r = 0; r < q; ++r) {
+    m = __reduce_max_sync(0xffffffffu, key);
+    const unsigned holders = __ballot_sync(0xffffffffu, key == m);
+    if (lane == __ffs(holders) - 1) key = 0;
   }
-  if (rank == q - 1) wq[warp] = tmax;
+  if (lane == 0) wq[warp] = ord_f32(m);
   __syncthreads();
   float t = wq[0];
 #pragma unroll
@@ -581,6 +597,7 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
   __shared__ int wkept[kSWarps][kSWarpKept];
   __shared__ float s_lse;
   pdl_wait();  // the block maxima and (m, s) come from the stream kernel just before
+  pdl_launch_dependents();  // a following kernel may be scheduled; it waits for this grid before using its results
 
   const int row = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -606,30 +623,36 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
     sel_t = a.sel[row];
     sel_x = a.parts.sel_logit[row];  // meaningful only when sel_t is in range
   }
-  // ---- lse over the row's (m, s) slots: warp 0, while the others go on ----
+  // (m, s) slots: warp 0 loads them now and folds them into the lse later,
+  // off the path to the first barrier (rows of <= 128 slots: one round)
+  const int nslots = a.cpr > 0 ? a.cpr * kTConsumerWarps
+                               : static_cast<int>((b0 + a.nblk - 1) / a.per - b0 / a.per + 1);
+  const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.P;
+  float2 msv[4];
   if (warp == 0) {
-    const int nslots = a.cpr > 0 ? a.cpr * kTConsumerWarps
-                                 : static_cast<int>((b0 + a.nblk - 1) / a.per - b0 / a.per + 1);
-    const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.P;
-    float tm = -INFINITY, ts = 0.0f;
-    for (int base = 0; base < nslots; base += 4 * 32) {
-      float2 p[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = base + u * 32 + lane;
-        p[u] = j < nslots ? ms[j] : make_float2(-INFINITY, 0.0f);
-      }
+    for (int u = 0; u < 4; ++u) {
+      const int j = u * 32 + lane;
+      msv[u] = j < nslots ? ms[j] : make_float2(-INFINITY, 0.0f);
+    }
+  }
+  // lse = M + log(sum_j s_j exp(m_j - M)); warp 0 writes it (and the selected
+  // token's logprob) and leaves it in s_lse
+  auto row_lse = [&]() {
+    // two passes over the slots (max, then the rescaled sum): short, parallel dependency chains
+    float tm = fmaxf(fmaxf(msv[0].x, msv[1].x), fmaxf(msv[2].x, msv[3].x));
+    for (int j = 4 * 32 + lane; j < nslots; j += 32) tm = fmaxf(tm, ms[j].x);
+    const float M = warp_max(tm);
+    float ts = 0.0f;
+    if (M != -INFINITY) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (p[u].x > tm) {
-          ts = (tm == -INFINITY) ? 0.0f : ts * expf(tm - p[u].x);
-          tm = p[u].x;
-        }
-        if (p[u].x != -INFINITY) ts += p[u].y * expf(p[u].x - tm);
+      for (int u = 0; u < 4; ++u) ts += msv[u].x == -INFINITY ? 0.0f : msv[u].y * expf(msv[u].x - M);
+      for (int j = 4 * 32 + lane; j < nslots; j += 32) {
+        const float2 p = ms[j];
+        ts += p.x == -INFINITY ? 0.0f : p.y * expf(p.x - M);
       }
     }
-    const float M = warp_max(tm);
-    const float S = warp_sum((tm == -INFINITY) ? 0.0f : ts * expf(tm - M));
+    const float S = warp_sum(ts);
     const float lse = (M == -INFINITY) ? -INFINITY : M + logf(S);
     if (lane == 0) {
       s_lse = lse;
@@ -642,15 +665,18 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
           set_status(a.dev_status, LMH_DS_SEL_OUT_OF_RANGE);
         sel_logprob[row] = v;
       }
-      misc[0] = 0;
-      misc[3] = 0;
     }
+  };
+  if (tid == 0) {
+    misc[0] = 0;
+    misc[3] = 0;
   }
-  if (a.k_max == 0) return;
   const int k = min(max(k_row, 0), a.k_max);
-  int32_t* out_ids = topk_ids + static_cast<int64_t>(row) * a.k_max;
-  float* out_lp = topk_logprobs + static_cast<int64_t>(row) * a.k_max;
   if (k == 0) {
+    if (warp == 0) row_lse();
+    if (a.k_max == 0) return;
+    int32_t* out_ids = topk_ids + static_cast<int64_t>(row) * a.k_max;
+    float* out_lp = topk_logprobs + static_cast<int64_t>(row) * a.k_max;
     for (int r = tid; r < a.k_max; r += kSThreads) {
       out_ids[r] = -1;
       out_lp[r] = -INFINITY;
@@ -675,7 +701,9 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
       for (int i = 0; i < kSBatch; ++i) tmax = fmaxf(tmax, v[i]);
     }
   }
-  const float t = topk_lower_bound(tmax, k, wq);  // (its barrier also publishes s_lse and misc[0])
+  const float t = topk_lower_bound(tmax, k, wq);  // (its barrier also publishes misc[0] and misc[3])
+  int32_t* out_ids = topk_ids + static_cast<int64_t>(row) * a.k_max;
+  float* out_lp = topk_logprobs + static_cast<int64_t>(row) * a.k_max;
 
   // ---- kept blocks (maximum >= t), listed per warp; the warp gathers their entries >= t ----
   const T* rowp = reinterpret_cast<const T*>(a.logits) + static_cast<int64_t>(row) * a.row_stride;
@@ -690,10 +718,24 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
     nk += __popc(m);
   };
   if (one_round) {
+    // this thread's kept blocks as a bit mask; positions by a warp prefix sum of the counts
+    uint32_t kmask = 0;
 #pragma unroll
-    for (int i = 0; i < kSBatch; ++i) {
-      const int b = tid + i * kSThreads;
-      add_kept(b, b < nb && bv[i] >= t);
+    for (int i = 0; i < kSBatch; ++i) kmask |= ((tid + i * kSThreads < nb && bv[i] >= t) ? 1u : 0u) << i;
+    const int mine = __popc(kmask);
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    nk = __shfl_sync(0xffffffffu, incl, 31);
+    int pos = incl - mine;
+    while (kmask) {
+      const int i = __ffs(kmask) - 1;
+      kmask &= kmask - 1;
+      if (pos < kSWarpKept) wk[pos] = tid + i * kSThreads;
+      ++pos;
     }
   } else {
     for (int base = 0; base < nb; base += kSBatch * kSThreads) {
@@ -720,7 +762,8 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
   if (nk > kSWarpKept) {
     if (lane == 0) misc[3] = 1;  // more kept blocks than the list holds: exact path below
   } else if (a.vec_ok) {
-    // 16-byte vectors of the kept blocks, kSGather per lane in flight; none straddles the row end
+    // 16-byte vectors of the kept blocks, kSGather per lane in flight; none straddles the row end.
+    // The warp's candidates are placed with one shared atomic: per-lane bit masks and a prefix sum.
     const int n_vec = nk * VPB;
     for (int base = 0; base < n_vec; base += kSGather * 32) {
       uint4 w[kSGather];
@@ -737,13 +780,41 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
           }
         }
       }
+      uint32_t cmask = 0;  // bit u * EPV + e: element e of vector u reaches t
 #pragma unroll
       for (int u = 0; u < kSGather; ++u) {
-        if (e0[u] < 0) continue;
         float x[EPV];
         VT::unpack(w[u], x);
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) add_cand(x[e], e0[u] + e);
+        for (int e = 0; e < EPV; ++e) cmask |= ((e0[u] >= 0 && x[e] >= t) ? 1u : 0u) << (u * EPV + e);
+      }
+      const int mine = __popc(cmask);
+      int incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int total = __shfl_sync(0xffffffffu, incl, 31);
+      uint32_t wbase = 0;
+      if (lane == 31 && total > 0) wbase = atomicAdd(&misc[0], static_cast<uint32_t>(total));
+      wbase = __shfl_sync(0xffffffffu, wbase, 31);
+      uint32_t pos = wbase + static_cast<uint32_t>(incl - mine);
+#pragma unroll
+      for (int u = 0; u < kSGather; ++u) {
+        uint32_t mu = (cmask >> (u * EPV)) & ((1u << EPV) - 1u);
+        if (!mu) continue;
+        float x[EPV];
+        VT::unpack(w[u], x);
+        while (mu) {
+          const int e = __ffs(mu) - 1;
+          mu &= mu - 1;
+          float v = x[0];  // x[e] without dynamic register indexing
+#pragma unroll
+          for (int ee = 1; ee < EPV; ++ee) v = (e == ee) ? x[ee] : v;
+          if (pos < kSCandCap) cand[pos] = make_key(v, e0[u] + e);
+          ++pos;
+        }
       }
     }
   } else {
@@ -753,6 +824,7 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
       if (e < a.V) add_cand(VT::at(rowp, e), e);
     }
   }
+  if (warp == 0) row_lse();
   __syncthreads();
   int cnt = static_cast<int>(misc[0]);
   const float lse = s_lse;
@@ -782,12 +854,18 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
     __syncthreads();
     cnt = min(k, static_cast<int>(misc[0]));
   }
-  // ---- exact order by rank (keys are unique) ----
-  for (int i = tid; i < cnt; i += kSThreads) {
-    const uint64_t key = cand[i];
+  // ---- exact order by rank (keys are unique): G threads per candidate ----
+  int G = 1;  // a power of two <= 32 with G * cnt <= kSThreads, at least 1
+  while (G < 32 && 2 * G * cnt <= kSThreads) G *= 2;
+  const int groups = kSThreads / G;
+  for (int base = 0; base < cnt; base += groups) {
+    const int i = base + tid / G, sub = tid % G;
+    const uint64_t key = i < cnt ? cand[i] : 0ull;
     int rank = 0;
-    for (int j = 0; j < cnt; ++j) rank += cand[j] > key;
-    if (rank < k) {
+    if (i < cnt)
+      for (int j = sub; j < cnt; j += G) rank += cand[j] > key;
+    for (int o = G / 2; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    if (i < cnt && sub == 0 && rank < k) {
       out_ids[rank] = key_id(key);
       out_lp[rank] = key_value(key) - lse;
     }
@@ -819,19 +897,31 @@ VocabSplit logits_reduce_split(int rows, int V, int k_max, int num_sms) {
   vs.ctas = sms * kTCtasPerSm;
   vs.splits = static_cast<int>((nblk + per - 1) / per) + 1;  // row pieces per row, at most
   vs.nblk = nblk;
-  // TMA path: 8 slots per chunk; the smallest chunk (f32) has kTChunkBytes / 256 blocks
+  // TMA path: one slot per consumer warp and chunk; the smallest chunk (f32) has kTChunkBytes / 256 blocks
   const int cpr_max = (nblk + kTChunkBytes / 256 - 1) / (kTChunkBytes / 256);
   vs.slots = cpr_max * kTConsumerWarps > vs.splits ? cpr_max * kTConsumerWarps : vs.splits;
   return vs;
 }
 
+template <typename T>
+static cudaError_t setup_one() {
+  cudaError_t e =
+      cudaFuncSetAttribute(logits_stream_tma_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
+  // Both kernels ask for the largest shared-memory carveout, so that the SMs
+  // keep one L1 / shared split from one kernel to the next.
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(logits_stream_tma_kernel<T>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(logits_select_kernel<T>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  return e;
+}
+
 cudaError_t logits_reduce_setup() {
-  cudaError_t e = cudaFuncSetAttribute(logits_stream_tma_kernel<__nv_bfloat16>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(logits_stream_tma_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(logits_stream_tma_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
+  cudaError_t e = setup_one<__nv_bfloat16>();
+  if (e == cudaSuccess) e = setup_one<__half>();
+  if (e == cudaSuccess) e = setup_one<float>();
   return e;
 }
 
@@ -866,10 +956,10 @@ static cudaError_t launch_both(ReduceArgs a, const VocabSplit& split, float* lse
     a.cpr = (a.nblk + CH - 1) / CH;
     const int64_t chunks = static_cast<int64_t>(a.rows) * a.cpr;
     const int grid = static_cast<int>(chunks < split.ctas ? chunks : split.ctas);
-    e = cudaMemsetAsync(a.parts.ticket, 0, sizeof(unsigned int), stream);
+    e = launch_kernel(ticket_reset_kernel, dim3(1), dim3(32), 0, stream, true, a.parts.ticket);
     if (e == cudaSuccess)
       e = launch_kernel(logits_stream_tma_kernel<T>, dim3(grid), dim3(kTThreads), static_cast<size_t>(kTSmem), stream,
-                        false, a);
+                        true, a);
   } else {
     a.cpr = 0;
     e = launch_kernel(logits_stream_regs_kernel<T>, dim3(split.grid), dim3(kRThreads), 0, stream, false, a);
