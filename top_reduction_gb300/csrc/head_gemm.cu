@@ -69,6 +69,7 @@ struct HeadArgs {
   Partials parts;
   float* logits_out;
   uint32_t* dev_status;
+  int epi_quarters;  // TMEM lane quarters that ever hold rows: ceil(rows / 32) below 128 rows, else 4
   int final_out;   // one vocabulary split: write the final results (out), not partials
   RowOutputs out;
 };
@@ -178,41 +179,47 @@ __device__ __noinline__ ListState list_insert(uint64_t* list, int r, ListState s
 // ---------------------------------------------------------------------------
 // per-row top-k list in registers (KCAP <= 32)
 // ---------------------------------------------------------------------------
-// L[0..k) holds the row's best keys sorted descending (0 = empty); slots
-// k..KC stay empty.  Insertion is a branchless compare-exchange sweep over the
-// first k slots: the new key settles at its rank and the smallest falls off.
-// tau is the value of the k-th key once k keys are held (else -inf): only
-// entries strictly above tau can still rank, because ids ascend within a
-// CTA's vocabulary range.  Slot k-1 is picked up during the sweep with a
-// predicated select (a plain select by a runtime index would move L to
-// local memory).
+// V[0..KC) holds the row's best values sorted descending, I[] their ids
+// (-inf / -1 in empty slots).  Entries reach a thread with ascending ids (the
+// tiles of a unit, the blocks of a tile and the columns of a block are
+// visited in order), so a new entry ranks after every held entry of equal
+// value and the list stays ordered by (value desc, id asc) with value
+// comparisons alone.  Insertion is a branchless shift: slot i keeps its entry
+// if it is >= x, takes x if it is the first slot below x, otherwise takes
+// slot i-1's entry.  tau = V[KC-1]: only values strictly above it can still
+// enter.  The list keeps KC >= k entries; a row reads its first k.
 template <int KC>
 struct RegTopK {
-  uint64_t L[KC];
+  float V[KC];
+  int32_t I[KC];
   float tau;
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
-    for (int i = 0; i < KC; ++i) L[i] = 0ull;
+    for (int i = 0; i < KC; ++i) {
+      V[i] = -INFINITY;
+      I[i] = -1;
+    }
     tau = -INFINITY;
   }
 
-  __device__ __forceinline__ void insert(uint64_t x, int k) {
-    uint64_t kth = 0ull;
+  __device__ __forceinline__ void insert(float x, int32_t id) {
+    bool ge[KC];
 #pragma unroll
-    for (int i = 0; i < KC; ++i) {
-      const bool gt = (i < k) && x > L[i];
-      const uint64_t lo = gt ? L[i] : x;
-      L[i] = gt ? x : L[i];
-      x = lo;
-      // kth = (i == k - 1) ? L[i] : kth, as a predicated select the compiler
-      // cannot turn into a load from a runtime index
-      asm("{\n\t.reg .pred p;\n\tsetp.eq.s32 p, %2, %3;\n\tselp.b64 %0, %1, %0, p;\n\t}"
-          : "+l"(kth)
-          : "l"(L[i]), "r"(i), "r"(k - 1));
+    for (int i = 0; i < KC; ++i) ge[i] = V[i] >= x;
+#pragma unroll
+    for (int i = KC - 1; i >= 0; --i) {
+      const bool prev_ge = (i == 0) || ge[i > 0 ? i - 1 : 0];
+      const float pv = V[i > 0 ? i - 1 : 0];
+      const int32_t pi = I[i > 0 ? i - 1 : 0];
+      V[i] = ge[i] ? V[i] : (prev_ge ? x : pv);
+      I[i] = ge[i] ? I[i] : (prev_ge ? id : pi);
     }
-    tau = kth ? key_value(kth) : -INFINITY;
+    tau = V[KC - 1];
   }
+
+  // sortable key of slot j (0 for an empty slot)
+  __device__ __forceinline__ uint64_t key(int j) const { return I[j] >= 0 ? make_key(V[j], I[j]) : 0ull; }
 };
 
 // ---------------------------------------------------------------------------
@@ -247,7 +254,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4 * 32);
+      mbar_init(&acc_empty[b], a.epi_quarters * 32);  // the epilogue warps that read accumulators
     }
     *abort_flag = 0;
     mbar_init_fence();
@@ -369,7 +376,10 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
     const int r_local = q * 32 + lane;  // row within the tile
     const float L = kLog2e;
     uint32_t t = 0;
-    bool live = true;
+    // With fewer than 128 rows (one row tile) the quarters beyond the last
+    // row have nothing to read: their warps go straight to the final barrier
+    // instead of polling the accumulator barriers (they are not counted there).
+    bool live = q < a.epi_quarters;
     for (int u = blockIdx.x; u < a.num_units && live; u += gridDim.x) {
       const int m_tile = u % a.m_tiles, split = u / a.m_tiles;
       const int n_begin = split * a.tiles_per_split;
@@ -469,7 +479,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                   const int j = __ffsll(static_cast<long long>(cm)) - 1;
                   cm &= cm - 1;
                   const float x = stg[j * 32 + lane];
-                  if (x > rt.tau) rt.insert(make_key(x, col0 + j), k_row);
+                  if (x > rt.tau) rt.insert(x, col0 + j);
                 }
                 __syncwarp(valid_mask);
               }
@@ -507,7 +517,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         if constexpr (Cfg::kRegList) {
 #pragma unroll
           for (int j = 0; j < (Cfg::kRegList ? KCAP : 1); ++j)
-            if (j < k_row) put(j, rt.L[j]);
+            if (j < k_row) put(j, rt.key(j));
         } else {
           for (int j = 0; j < k_row; ++j) put(j, (j < st.cnt) ? lists[j * kBM + r_local] : 0ull);
         }
@@ -519,7 +529,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         if constexpr (Cfg::kRegList) {
 #pragma unroll
           for (int j = 0; j < (Cfg::kRegList ? KCAP : 1); ++j)
-            if (j < k_row) out[j] = rt.L[j];
+            if (j < k_row) out[j] = rt.key(j);
         } else {
           for (int j = 0; j < k_row; ++j) out[j] = (j < st.cnt) ? lists[j * kBM + r_local] : 0ull;
         }
@@ -577,7 +587,13 @@ HeadPlan head_plan(int rows, int H, int V, int k_max, int num_sms) {
   HeadPlan p;
   p.m_tiles = (rows + kBM - 1) / kBM;
   p.n_tiles = (V + kBN - 1) / kBN;
-  p.kcap = k_max <= 4 ? 4 : k_max <= 8 ? 8 : k_max <= 16 ? 16 : k_max <= 24 ? 24 : k_max <= 32 ? 32 : 128;
+  p.kcap = k_max <= 1    ? 1
+           : k_max <= 5  ? 5
+           : k_max <= 8  ? 8
+           : k_max <= 16 ? 16
+           : k_max <= 20 ? 20
+           : k_max <= 32 ? 32
+                         : 128;
   const int G = num_sms > 0 ? num_sms : 1;
   // choose the vocabulary split that minimises the busiest CTA's tile count
   // (plus a small cost per unit for its flush and pipeline refill)
@@ -643,10 +659,11 @@ cudaError_t head_setup() {
 #define LMH_HEAD_ATTR(KC)                                            \
   if (e == cudaSuccess) e = set_head_attr<KC, false>();              \
   if (e == cudaSuccess) e = set_head_attr<KC, true>();
-  LMH_HEAD_ATTR(4)
+  LMH_HEAD_ATTR(1)
+  LMH_HEAD_ATTR(5)
   LMH_HEAD_ATTR(8)
   LMH_HEAD_ATTR(16)
-  LMH_HEAD_ATTR(24)
+  LMH_HEAD_ATTR(20)
   LMH_HEAD_ATTR(32)
   LMH_HEAD_ATTR(128)
 #undef LMH_HEAD_ATTR
@@ -683,6 +700,7 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   a.parts = parts;
   a.logits_out = logits_out;
   a.dev_status = dev_status;
+  a.epi_quarters = rows < kBM ? (rows + 31) / 32 : 4;
   a.final_out = final_out ? 1 : 0;
   a.out = final_out ? *final_out : RowOutputs{nullptr, nullptr, nullptr, nullptr};
   const dim3 grid(plan.grid), block(kHeadThreads);
@@ -694,10 +712,11 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
                    : launch_kernel(head_logprobs_kernel<KC, false>, grid, block, HeadCfg<KC>::kSmem,       \
                                    stream, pdl, ta, tb, a);                                              \
     break;
-    LMH_HEAD_CASE(4)
+    LMH_HEAD_CASE(1)
+    LMH_HEAD_CASE(5)
     LMH_HEAD_CASE(8)
     LMH_HEAD_CASE(16)
-    LMH_HEAD_CASE(24)
+    LMH_HEAD_CASE(20)
     LMH_HEAD_CASE(32)
     LMH_HEAD_CASE(128)
 #undef LMH_HEAD_CASE

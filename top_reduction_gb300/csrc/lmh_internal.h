@@ -90,7 +90,7 @@ struct HeadPlan {
   int splits;           // vocabulary ranges per row (units = m_tiles * splits)
   int tiles_per_split;  // n-tiles per range
   int grid;             // persistent CTAs
-  int kcap;             // per-row candidate capacity variant (4, 8, 16, 24, 32 or 128)
+  int kcap;             // per-row candidate capacity variant (1, 5, 8, 16, 20, 32 or 128)
 };
 
 HeadPlan head_plan(int rows, int H, int V, int k_max, int num_sms);
