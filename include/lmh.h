@@ -189,8 +189,9 @@ lmh_status lmh_project_logprobs(const void* hidden, int64_t hidden_row_stride, i
  * issue #719 (reusable for decode rows and batches of prompt positions).
  *
  *   logits            device [rows x V] of dtype, row stride row_stride (>= V),
- *                     base aligned to sizeof(dtype).  Rows whose start is
- *                     16-byte aligned are staged with one bulk copy, others
+ *                     base aligned to sizeof(dtype).  When the base, the
+ *                     row stride and the row length are multiples of 16
+ *                     bytes the logits are streamed with bulk copies, else
  *                     with plain loads.
  *   sel_ids, row_k, k_max, lse, sel_logprob, topk_ids, topk_logprobs:
  *                     as for lmh_project_logprobs (logit = the given value
