@@ -48,7 +48,7 @@ constexpr uint32_t kStageBytesB = kBN * kBK * 2;  // 32 KB
 
 // KCAP: per-row candidate capacity.  KCAP <= 32 keeps each row's top-k list
 // in registers and uses the shared region to stage candidate blocks (4 warps x
-// 64 columns x 32 lanes x 4 bytes); KCAP 128 keeps the lists themselves in
+// 64 columns x 32 lanes x 4 bytes); KCAP 128 keeps a min-heap per row in
 // shared memory (slot-major) and has room for only 2 pipeline stages.
 template <int KCAP>
 struct HeadCfg {
@@ -151,29 +151,78 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
 }
 
 // ---------------------------------------------------------------------------
-// per-row sorted candidate list in shared memory (slot-major: list[j*128+r])
+// per-row top-k heap in shared memory (KCAP 128; slot-major: heap[i*128+r])
 // ---------------------------------------------------------------------------
-struct ListState {
-  float tau;  // value of the k-th entry once the list is full, else -inf
+// A min-heap of keys: the root is the worst held entry, so tau (the value a
+// new entry must exceed once kh entries are held) is the root's value, and an
+// insertion costs O(log kh) steps whatever the new entry's rank.  The heap is
+// sorted once, at the end of a unit.
+struct HeapState {
+  float tau;  // value of the root once the heap holds kh keys, else -inf
   int cnt;
 };
 
-__device__ __noinline__ ListState list_insert(uint64_t* list, int r, ListState st, int k, uint64_t key) {
-  int pos;
-  if (st.cnt < k) {
-    pos = st.cnt++;
-  } else {
-    pos = k - 1;  // the caller only inserts keys above the current k-th
+__device__ __noinline__ HeapState heap_push(uint64_t* h, int r, HeapState st, int kh, uint64_t key) {
+  int i;
+  if (st.cnt < kh) {  // grow: sift up from the new last slot
+    i = st.cnt++;
+    while (i > 0) {
+      const int p = (i - 1) >> 1;
+      const uint64_t pk = h[p * kBM + r];
+      if (pk <= key) break;
+      h[i * kBM + r] = pk;
+      i = p;
+    }
+  } else {  // full (the caller only pushes keys above the root): replace the root, sift down
+    i = 0;
+    for (;;) {
+      const int l = 2 * i + 1;
+      if (l >= kh) break;
+      uint64_t ck = h[l * kBM + r];
+      int c = l;
+      if (l + 1 < kh) {
+        const uint64_t rk = h[(l + 1) * kBM + r];
+        if (rk < ck) {
+          ck = rk;
+          c = l + 1;
+        }
+      }
+      if (ck >= key) break;
+      h[i * kBM + r] = ck;
+      i = c;
+    }
   }
-  while (pos > 0) {
-    const uint64_t up = list[(pos - 1) * kBM + r];
-    if (up >= key) break;
-    list[pos * kBM + r] = up;
-    --pos;
-  }
-  list[pos * kBM + r] = key;
-  st.tau = (st.cnt == k) ? key_value(list[(k - 1) * kBM + r]) : -INFINITY;
+  h[i * kBM + r] = key;
+  st.tau = (st.cnt == kh) ? key_value(h[r]) : -INFINITY;
   return st;
+}
+
+// Heapsort of the n held keys into descending order (best first): the root
+// (the minimum) moves to the end of the shrinking heap.
+__device__ __noinline__ void heap_sort_desc(uint64_t* h, int r, int n) {
+  for (int end = n - 1; end > 0; --end) {
+    const uint64_t top = h[r];
+    const uint64_t key = h[end * kBM + r];
+    h[end * kBM + r] = top;
+    int i = 0;
+    for (;;) {
+      const int l = 2 * i + 1;
+      if (l >= end) break;
+      uint64_t ck = h[l * kBM + r];
+      int c = l;
+      if (l + 1 < end) {
+        const uint64_t rk = h[(l + 1) * kBM + r];
+        if (rk < ck) {
+          ck = rk;
+          c = l + 1;
+        }
+      }
+      if (ck >= key) break;
+      h[i * kBM + r] = ck;
+      i = c;
+    }
+    h[i * kBM + r] = key;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -395,7 +444,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
       }
       float m = -INFINITY, ssum = 0.0f, sel_val = 0.0f;
       bool has_sel = false;
-      ListState st;  // shared-memory list (KCAP 128)
+      HeapState st;  // shared-memory heap (KCAP 128)
       st.tau = -INFINITY;
       st.cnt = 0;
       RegTopK<Cfg::kRegList ? KCAP : 1> rt;  // register list (KCAP <= 32)
@@ -487,7 +536,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
               if (k_row > 0 && bm > st.tau) {
 #pragma unroll
                 for (int j = 0; j < kBlock; ++j)
-                  if (v[j] > st.tau) st = list_insert(lists, r_local, st, k_row, make_key(v[j], col0 + j));
+                  if (v[j] > st.tau) st = heap_push(lists, r_local, st, a.k_max, make_key(v[j], col0 + j));
               }
             }
           }
@@ -519,6 +568,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
           for (int j = 0; j < (Cfg::kRegList ? KCAP : 1); ++j)
             if (j < k_row) put(j, rt.key(j));
         } else {
+          heap_sort_desc(lists, r_local, st.cnt);
           for (int j = 0; j < k_row; ++j) put(j, (j < st.cnt) ? lists[j * kBM + r_local] : 0ull);
         }
         for (int j = k_row; j < a.k_max; ++j) put(j, 0ull);
@@ -531,6 +581,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
           for (int j = 0; j < (Cfg::kRegList ? KCAP : 1); ++j)
             if (j < k_row) out[j] = rt.key(j);
         } else {
+          heap_sort_desc(lists, r_local, st.cnt);
           for (int j = 0; j < k_row; ++j) out[j] = (j < st.cnt) ? lists[j * kBM + r_local] : 0ull;
         }
         if (has_sel) a.parts.sel_logit[row] = sel_val;
