@@ -606,6 +606,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
                                                           int num_tokens, const int32_t* __restrict__ row_idx,
                                                           int H, uint16_t* __restrict__ out, uint32_t* dev_status) {
   pdl_launch_dependents();  // the head kernel may start and stream W meanwhile
+  pdl_wait();               // row_idx comes from the kernel launched just before
   const int i = blockIdx.x;
   const int src = row_idx ? row_idx[i] : i;
   const bool ok = src >= 0 && src < num_tokens;
@@ -624,9 +625,9 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
 
 cudaError_t launch_gather_rows(const void* hidden, int64_t hidden_stride, int num_tokens, const int32_t* row_idx,
                                int rows, int H, void* out, uint32_t* dev_status, cudaStream_t stream) {
-  gather_rows_kernel<<<rows, 256, 0, stream>>>(static_cast<const uint16_t*>(hidden), hidden_stride, num_tokens,
-                                               row_idx, H, static_cast<uint16_t*>(out), dev_status);
-  return cudaGetLastError();
+  return launch_kernel(gather_rows_kernel, dim3(rows), dim3(256), 0, stream, true,
+                       static_cast<const uint16_t*>(hidden), hidden_stride, num_tokens, row_idx, H,
+                       static_cast<uint16_t*>(out), dev_status);
 }
 
 // ---------------------------------------------------------------------------

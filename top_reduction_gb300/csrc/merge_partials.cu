@@ -44,6 +44,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
   __shared__ float red[32];
   __shared__ uint64_t red64[32];
   pdl_wait();  // the partials come from the kernel launched just before
+  pdl_launch_dependents();  // a following kernel may be scheduled; it waits for this grid before using its results
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
   const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.splits;
@@ -189,6 +190,7 @@ constexpr int kWarpRowsPerCta = 8;
 __global__ void __launch_bounds__(kWarpRowsPerCta * 32) merge_partials_warp_kernel(const MergeArgs a) {
   __shared__ uint64_t sbuf[kWarpRowsPerCta][kWarpItems];
   pdl_wait();  // the partials come from the kernel launched just before
+  pdl_launch_dependents();  // a following kernel may be scheduled; it waits for this grid before using its results
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int row = blockIdx.x * kWarpRowsPerCta + w;
   if (row >= a.rows) return;

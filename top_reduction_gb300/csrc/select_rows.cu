@@ -24,6 +24,11 @@ __global__ void __launch_bounds__(kSelectThreads)
     select_rows_kernel(const int32_t* __restrict__ cu, int num_seqs, int num_decode,
                        const uint8_t* __restrict__ mask, int max_out, int32_t* __restrict__ row_idx,
                        int32_t* __restrict__ logits_cu, uint32_t* dev_status) {
+  // Launched with programmatic dependent launch: wait for the preceding
+  // kernel (which may write cu_seqlens or still read row_idx), then let the
+  // gather that follows be scheduled.
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ int32_t s_excl[kSelectThreads];
   __shared__ int32_t s_first[kSelectThreads];
   __shared__ int32_t s_warp[32];
@@ -109,9 +114,8 @@ __global__ void __launch_bounds__(kSelectThreads)
 cudaError_t launch_select_rows(const int32_t* cu, int num_seqs, int num_decode, const uint8_t* mask,
                                int max_out, int32_t* row_idx, int32_t* logits_cu, uint32_t* dev_status,
                                cudaStream_t stream) {
-  select_rows_kernel<<<1, kSelectThreads, 0, stream>>>(cu, num_seqs, num_decode, mask, max_out, row_idx,
-                                                        logits_cu, dev_status);
-  return cudaGetLastError();
+  return launch_kernel(select_rows_kernel, dim3(1), dim3(kSelectThreads), 0, stream, true, cu, num_seqs, num_decode,
+                       mask, max_out, row_idx, logits_cu, dev_status);
 }
 
 }  // namespace lmh
