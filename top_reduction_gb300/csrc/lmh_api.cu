@@ -255,7 +255,7 @@ lmh_status lmh_project_logprobs(const void* hidden, int64_t hidden_row_stride, i
   if (e == cudaSuccess && !one_split) {
     Traced tr(kTraceMerge, stream);
     e = launch_merge(rows, plan.splits, V, k_max, parts, sel_ids, row_k, lse, sel_logprob, topk_ids, topk_logprobs,
-                     dev_status, stream, 0, 0, /*pdl=*/true);
+                     dev_status, stream, /*pdl=*/true);
   }
   return from_cuda(e);
 }

@@ -73,13 +73,10 @@ cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t ro
                                  Partials parts, float* lse, float* sel_logprob, int32_t* topk_ids,
                                  float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream);
 
-// Merges the partial slots of every row.  flat_per == 0: every one of the
-// `splits` slots is filled (head path); flat_per > 0: row r fills the slots of
-// the ranges it meets in a VocabSplit with per = flat_per, nblk = flat_nblk.
+// Merges the `splits` partial slots of every row (head path).
 cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts, const int32_t* sel,
                          const int32_t* row_k, float* lse, float* sel_logprob, int32_t* topk_ids,
-                         float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream, int flat_per = 0,
-                         int flat_nblk = 0, bool pdl = false);
+                         float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream, bool pdl = false);
 
 // ---- head projection (head_gemm.cu) ----
 

@@ -18,7 +18,6 @@ constexpr int kMergeCap = 1024;  // candidate keys held in shared memory
 
 struct MergeArgs {
   int rows, splits, V, k_max;
-  int flat_per, flat_nblk;  // flat_per > 0: the slots a row fills follow the range layout
   Partials parts;
   const int32_t* sel;
   const int32_t* row_k;
@@ -37,52 +36,79 @@ struct MergeArgs {
 //         row's k best.  A lower bound L of the row's k-th key (the k-th
 //         largest of the slots' leading keys) limits the gather to keys >= L;
 //         they are ordered by rank.
-__global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const MergeArgs a) {
+constexpr int kMergeItemsPerThread = 8;  // a row's keys held in registers per thread (first round)
+
+__global__ void __launch_bounds__(kMergeThreads, 4) merge_partials_kernel(const MergeArgs a) {
   __shared__ uint64_t cand[kMergeCap];
   __shared__ uint32_t hist[256];
-  __shared__ uint32_t misc[4];
+  __shared__ uint32_t misc[4];  // [0] candidates, [1..2] select broadcast
   __shared__ float red[32];
   __shared__ uint64_t red64[32];
   pdl_wait();  // the partials come from the kernel launched just before
   pdl_launch_dependents();  // a following kernel may be scheduled; it waits for this grid before using its results
   const int row = blockIdx.x;
   const int tid = threadIdx.x;
-  const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.splits;
-  int nslots = a.splits;
-  if (a.flat_per > 0) {
-    const int64_t b0 = static_cast<int64_t>(row) * a.flat_nblk;
-    nslots = static_cast<int>((b0 + a.flat_nblk - 1) / a.flat_per - b0 / a.flat_per) + 1;
-  }
+  const int nslots = a.splits;
+  const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * nslots;
+  const unsigned long long* keys = a.parts.part_keys + static_cast<int64_t>(row) * nslots * a.k_max;
 
-  // ---- lse ----
-  float tm = -INFINITY, ts = 0.0f;
-  for (int j = tid; j < nslots; j += kMergeThreads) {
-    const float2 p = ms[j];
-    if (p.x > tm) {
-      ts = (tm == -INFINITY) ? 0.0f : ts * expf(tm - p.x);
-      tm = p.x;
-    }
-    if (p.x != -INFINITY) ts += p.y * expf(p.x - tm);
+  // ---- every independent load first: K, the selected token, the slots' (m, s) and the row's keys ----
+  // Slot j's sorted list is keys[j * k_max + r], r < k_max: item i = j * k_max + r is keys[i].
+  const int k = a.row_k ? min(max(a.row_k[row], 0), a.k_max) : a.k_max;
+  int sel_t = -1;
+  float sel_x = 0.0f;
+  if (tid == 0 && a.sel) {
+    sel_t = a.sel[row];
+    sel_x = a.parts.sel_logit[row];  // meaningful only when sel_t is in range
   }
-  const float M = block_max(tm, red);
-  const float S = block_sum((tm == -INFINITY) ? 0.0f : ts * expf(tm - M), red);
+  const float2 p0 = tid < nslots ? ms[tid] : make_float2(-INFINITY, 0.0f);
+  const int n_items = nslots * a.k_max;
+  uint64_t kv[kMergeItemsPerThread];
+#pragma unroll
+  for (int u = 0; u < kMergeItemsPerThread; ++u) {
+    const int i = tid + u * kMergeThreads;
+    kv[u] = i < n_items ? keys[i] : 0ull;
+  }
+  // (slot, rank) of the held items, walked without divisions
+  const int km = max(a.k_max, 1);
+  const int step_j = kMergeThreads / km, step_r = kMergeThreads - step_j * km;
+  const int j0 = tid / km, r0 = tid - j0 * km;
+  auto next = [&](int& j, int& r) {
+    j += step_j;
+    r += step_r;
+    if (r >= km) {
+      r -= km;
+      ++j;
+    }
+  };
+
+  // ---- lse = M + log(sum_j s_j exp(m_j - M)) ----
+  float mloc = p0.x;
+  for (int j = tid + kMergeThreads; j < nslots; j += kMergeThreads) mloc = fmaxf(mloc, ms[j].x);
+  const float M = block_max(mloc, red);
+  float sloc = 0.0f;
+  if (M != -INFINITY) {
+    if (p0.x != -INFINITY) sloc = p0.y * expf(p0.x - M);
+    for (int j = tid + kMergeThreads; j < nslots; j += kMergeThreads) {
+      const float2 p = ms[j];
+      if (p.x != -INFINITY) sloc += p.y * expf(p.x - M);
+    }
+  }
+  const float S = block_sum(sloc, red);
   const float lse = (M == -INFINITY) ? -INFINITY : M + logf(S);
   if (tid == 0) {
     a.lse[row] = lse;
     if (a.sel) {
-      const int t = a.sel[row];
       float v = __int_as_float(0x7fc00000);  // NaN: no selected token / out of range
-      if (t >= 0 && t < a.V)
-        v = a.parts.sel_logit[row] - lse;
-      else if (t != -1)
+      if (sel_t >= 0 && sel_t < a.V)
+        v = sel_x - lse;
+      else if (sel_t != -1)
         set_status(a.dev_status, LMH_DS_SEL_OUT_OF_RANGE);
       a.sel_logprob[row] = v;
     }
     misc[0] = 0;
   }
   if (a.k_max == 0) return;
-  int k = a.k_max;
-  if (a.row_k) k = min(max(a.row_k[row], 0), a.k_max);
   int32_t* out_ids = a.topk_ids + static_cast<int64_t>(row) * a.k_max;
   float* out_lp = a.topk_logprobs + static_cast<int64_t>(row) * a.k_max;
   if (k == 0) {
@@ -93,7 +119,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
     return;
   }
 
-  const unsigned long long* keys = a.parts.part_keys + static_cast<int64_t>(row) * a.splits * a.k_max;
   // ---- lb: a lower bound of the row's k-th key ----
   // U = the q best keys of every slot, q = ceil(k / nslots), so |U| >= k and
   // the k-th largest key of U is reached by k keys of the row.  (Taking the
@@ -103,10 +128,17 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
   const int q = (k + nslots - 1) / nslots;
   const int nu = q * nslots;
   if (nu <= kMergeCap) {
-    for (int i = tid; i < nu; i += kMergeThreads) {
-      const int j = i / q;
-      cand[i] = keys[static_cast<int64_t>(j) * a.k_max + (i - j * q)];
+    auto put_u = [&](int i, uint64_t key) {
+      const int j = i / a.k_max, r = i - j * a.k_max;
+      if (r < q) cand[j * q + r] = key;
+    };
+    int j = j0, r = r0;
+#pragma unroll
+    for (int u = 0; u < kMergeItemsPerThread; ++u) {
+      if (tid + u * kMergeThreads < n_items && r < q) cand[j * q + r] = kv[u];
+      next(j, r);
     }
+    for (int i = tid + kMergeItemsPerThread * kMergeThreads; i < n_items; i += kMergeThreads) put_u(i, keys[i]);
     __syncthreads();
     for (int i = tid; i < nu; i += kMergeThreads) {
       const uint64_t key = cand[i];
@@ -127,32 +159,46 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
     }
     lb = block_max_u64(lb, red64);
   }
-  // gather every key >= lb: independent loads over all (slot, rank) items
-  const int n_items = nslots * k;
-  auto in_set = [&](int i, uint64_t* key) -> bool {
-    const int j = i / k, r = i - j * k;
-    const uint64_t kk = keys[static_cast<int64_t>(j) * a.k_max + r];
-    if (kk == 0ull || kk < lb) return false;
-    *key = kk;
-    return true;
-  };
-  for (int i = tid; i < n_items; i += kMergeThreads) {
-    uint64_t key = 0;
-    if (in_set(i, &key)) {
+
+  // ---- candidates: the keys >= lb among the first k of every slot ----
+  auto take = [&](int i, uint64_t key) {
+    const int r = i % a.k_max;
+    if (r < k && key != 0ull && key >= lb) {
       const uint32_t pos = atomicAdd(&misc[0], 1u);
       if (pos < kMergeCap) cand[pos] = key;
     }
+  };
+  {
+    int j = j0, r = r0;
+#pragma unroll
+    for (int u = 0; u < kMergeItemsPerThread; ++u) {
+      const uint64_t key = kv[u];  // 0 beyond n_items
+      if (r < k && key != 0ull && key >= lb) {
+        const uint32_t pos = atomicAdd(&misc[0], 1u);
+        if (pos < kMergeCap) cand[pos] = key;
+      }
+      next(j, r);
+    }
   }
+  for (int i = tid + kMergeItemsPerThread * kMergeThreads; i < n_items; i += kMergeThreads) take(i, keys[i]);
   __syncthreads();
   int cnt = static_cast<int>(misc[0]);
   if (cnt > kMergeCap) {
     // many exact ties: select the k-th key exactly, then keep the k keys at or above it
+    const int n_set = nslots * k;
+    auto in_set = [&](int i, uint64_t* key) -> bool {
+      const int j = i / k, r = i - j * k;
+      const uint64_t kk = keys[static_cast<int64_t>(j) * a.k_max + r];
+      if (kk == 0ull || kk < lb) return false;
+      *key = kk;
+      return true;
+    };
     int above;
-    const uint64_t T64 = cta_radix_select(in_set, n_items, k, 64, hist, misc + 1, &above);
+    const uint64_t T64 = cta_radix_select(in_set, n_set, k, 64, hist, misc + 1, &above);
     __syncthreads();
     if (tid == 0) misc[0] = 0;
     __syncthreads();
-    for (int i = tid; i < n_items; i += kMergeThreads) {
+    for (int i = tid; i < n_set; i += kMergeThreads) {
       uint64_t key = 0;
       if (in_set(i, &key) && key >= T64) {
         const uint32_t pos = atomicAdd(&misc[0], 1u);  // exactly k of them
@@ -162,12 +208,18 @@ __global__ void __launch_bounds__(kMergeThreads) merge_partials_kernel(const Mer
     __syncthreads();
     cnt = min(k, static_cast<int>(misc[0]));
   }
-  // exact order by rank (keys are unique)
-  for (int t = tid; t < cnt; t += kMergeThreads) {
-    const uint64_t key = cand[t];
+  // ---- exact order by rank (keys are unique): G threads per candidate ----
+  int G = 1;  // a power of two <= 32 with G * cnt <= kMergeThreads, at least 1
+  while (G < 32 && 2 * G * cnt <= kMergeThreads) G *= 2;
+  const int groups = kMergeThreads / G;
+  for (int base = 0; base < cnt; base += groups) {
+    const int i = base + tid / G, sub = tid % G;
+    const uint64_t key = i < cnt ? cand[i] : 0ull;
     int rank = 0;
-    for (int j = 0; j < cnt; ++j) rank += cand[j] > key;
-    if (rank < k) {
+    if (i < cnt)
+      for (int j = sub; j < cnt; j += G) rank += cand[j] > key;
+    for (int o = G / 2; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    if (i < cnt && sub == 0 && rank < k) {
       out_ids[rank] = key_id(key);
       out_lp[rank] = key_value(key) - lse;
     }
@@ -306,11 +358,8 @@ cudaError_t merge_setup() { return cudaSuccess; }
 
 cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts, const int32_t* sel,
                          const int32_t* row_k, float* lse, float* sel_logprob, int32_t* topk_ids,
-                         float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream, int flat_per,
-                         int flat_nblk, bool pdl) {
+                         float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream, bool pdl) {
   MergeArgs a;
-  a.flat_per = flat_per;
-  a.flat_nblk = flat_nblk;
   a.rows = rows;
   a.splits = splits;
   a.V = V;
@@ -323,7 +372,7 @@ cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts,
   a.topk_ids = topk_ids;
   a.topk_logprobs = topk_logprobs;
   a.dev_status = dev_status;
-  if (flat_per == 0 && static_cast<int64_t>(splits) * k_max <= kWarpItems)
+  if (static_cast<int64_t>(splits) * k_max <= kWarpItems)
     return launch_kernel(merge_partials_warp_kernel, dim3((rows + kWarpRowsPerCta - 1) / kWarpRowsPerCta),
                          dim3(kWarpRowsPerCta * 32), 0, stream, pdl, a);
   return launch_kernel(merge_partials_kernel, dim3(rows), dim3(kMergeThreads), 0, stream, pdl, a);
