@@ -254,10 +254,14 @@ def e2e_leg(lmh, b, device, steps):
 
     Every step copies its inputs host->device (hidden rows, cu_seqlens,
     selected ids; the head weight stays resident like model weights), runs
-    the path, copies the compact result device->host and waits for it.
+    the path, copies the compact result device->host and reads it on the
+    host.  Two buffer sets alternate, as in a serving loop: step i+1 is
+    issued before the host waits for step i's result, so the host's own work
+    overlaps the GPU's.
     """
     import torch
-    if b["name"] == "logits_chunk":
+    chunk = b["name"] == "logits_chunk"
+    if chunk:
         h_in = {"logits": b["logits"].pin_memory(), "sel": b["sel"].pin_memory()}
     else:
         h_in = {"hidden": b["hidden"].pin_memory(), "cu": b["cu_seqlens"].pin_memory(),
@@ -265,36 +269,59 @@ def e2e_leg(lmh, b, device, steps):
         W = b["W"].to(device)
         mask = None if b["all_rows_mask"] is None else b["all_rows_mask"].to(device)
         row_k = None if b["row_k"] is None else b["row_k"].to(device)
-    d_in = {k: torch.empty_like(v, device=device) for k, v in h_in.items()}
-    rows = b["rows"] if b["name"] == "logits_chunk" else int(b["n_sel"])
+    rows = b["rows"] if chunk else int(b["n_sel"])
     k = int(b["k"])
-    h_out = {"lse": torch.empty(rows, dtype=torch.float32).pin_memory(),
-             "sel_logprob": torch.empty(rows, dtype=torch.float32).pin_memory(),
-             "topk_ids": torch.empty((rows, k), dtype=torch.int32).pin_memory(),
-             "topk_logprobs": torch.empty((rows, k), dtype=torch.float32).pin_memory()}
-    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
-    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+    if chunk:
+        ws_bytes = lmh.workspace_bytes(rows, 0, b["V"], k, lmh.PATH_FROM_LOGITS)
+    else:
+        ws_bytes = lmh.workspace_bytes(rows, int(b["H"]), int(b["V"]), k, lmh.PATH_PROJECT)
 
-    def one():
+    def buffers():
+        d_in = {key: torch.empty_like(v, device=device) for key, v in h_in.items()}
+        out = {"lse": torch.empty(rows, dtype=torch.float32, device=device),
+               "sel_logprob": torch.empty(rows, dtype=torch.float32, device=device),
+               "topk_ids": torch.empty((rows, k), dtype=torch.int32, device=device),
+               "topk_logprobs": torch.empty((rows, k), dtype=torch.float32, device=device)}
+        h_out = {key: torch.empty(v.shape, dtype=v.dtype).pin_memory() for key, v in out.items()}
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+        return {"d_in": d_in, "out": out, "h_out": h_out, "ws": ws, "ev": torch.cuda.Event()}
+
+    bufs = [buffers(), buffers()]
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in bufs[0]["h_out"].values())
+
+    def issue(bf):
+        d_in = bf["d_in"]
         for key, v in h_in.items():
             d_in[key].copy_(v, non_blocking=True)
-        if b["name"] == "logits_chunk":
-            o = lmh.logprobs_from_logits(d_in["logits"], sel=d_in["sel"], k_max=k)
+        if chunk:
+            o = lmh.logprobs_from_logits(d_in["logits"], sel=d_in["sel"], k_max=k, workspace=bf["ws"],
+                                         out=bf["out"])
         else:
             ri, _ = lmh.select_rows(d_in["cu"], b["num_decode"], mask, max_out_rows=rows)
-            o = lmh.project_logprobs(d_in["hidden"], W, row_idx=ri, sel=d_in["sel"], row_k=row_k, k_max=k)
-        for key, v in h_out.items():
+            o = lmh.project_logprobs(d_in["hidden"], W, row_idx=ri, sel=d_in["sel"], row_k=row_k, k_max=k,
+                                     workspace=bf["ws"], out=bf["out"])
+        for key, v in bf["h_out"].items():
             v.copy_(o[key], non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        bf["ev"].record()
 
-    for _ in range(5):
-        one()
+    def read(bf):  # the host waits for, and touches, the step's result
+        bf["ev"].synchronize()
+        return float(bf["h_out"]["lse"][0])
+
+    for s in range(5):
+        issue(bufs[s % 2])
+        read(bufs[s % 2])
     t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
+    for s in range(steps):
+        issue(bufs[s % 2])
+        if s > 0:
+            read(bufs[(s - 1) % 2])
+    read(bufs[(steps - 1) % 2])
     dt = time.perf_counter() - t0
     return {"value": rows * steps / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": 1e3 * dt / steps}
+            "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": 1e3 * dt / steps,
+            "pipelining": "two buffer sets: step i+1 is issued before step i's result is read"}
 
 
 def load_peaks():
