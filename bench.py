@@ -230,6 +230,21 @@ class Step:
                                     k_max=self.k, workspace=self.ws, out=self.out, dev_status=self.status)
 
 
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time (all ranks get it); `ms` unchanged on one process."""
+    import torch
+    if not dist:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(rows_per_step, steps, world, ms):
+    """Whole-job rows/s: the rows every rank processed over the slowest rank's time."""
+    return rows_per_step * steps * world / (ms / 1e3)
+
+
 def timed_region(step, steps, dist, world):
     import torch
     if dist:
@@ -241,12 +256,7 @@ def timed_region(step, steps, dist, world):
         step.run()
     stop.record()
     torch.cuda.synchronize()
-    ms = start.elapsed_time(stop)
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return ms
+    return max_over_ranks(start.elapsed_time(stop), dist, "cuda")
 
 
 def e2e_leg(lmh, b, device, steps):
@@ -470,8 +480,7 @@ def run_ours(args):
     if status:
         raise RuntimeError("device status %#x during the benchmark" % status)
 
-    rows_total = step.rows * args.steps * world
-    value = rows_total / (ms / 1e3)
+    value = job_value(step.rows, args.steps, world, ms)
     peaks, peak_src = load_peaks()
     avg_us = per_kernel.get(kernel, {}).get("avg_us")
     if bound == "hbm":

@@ -259,7 +259,8 @@ int32_t lmh_version(void);
  * lmh_trace_read waits for the recorded events, then reports the launches
  * and total milliseconds of the named kernel ("select_rows", "gather_rows",
  * "head_logprobs", "merge_partials", "logits_reduce" (the streaming pass of
- * lmh_logprobs_from_logits), "logits_select" (its per-row selection)) since
+ * lmh_logprobs_from_logits), "logits_select" (its per-row selection),
+ * "ticket_reset" (the chunk-counter reset before the streaming pass)) since
  * the last reset.
  * lmh_trace_reset clears the totals.
  */

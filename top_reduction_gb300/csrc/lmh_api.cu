@@ -65,7 +65,8 @@ Partials carve_partials(void* base, int rows, int splits, int k_max) {
 // kernel trace
 // ---------------------------------------------------------------------------
 static const char* const kTraceNames[kTraceCount] = {"select_rows",   "gather_rows",    "head_logprobs",
-                                                     "logits_reduce", "merge_partials", "logits_select"};
+                                                     "logits_reduce", "merge_partials", "logits_select",
+                                                     "ticket_reset"};
 
 struct TraceRecord {
   int kernel;

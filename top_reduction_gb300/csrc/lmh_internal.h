@@ -132,6 +132,7 @@ enum TraceKernel {
   kTraceReduce,
   kTraceMerge,
   kTraceLogitsSelect,
+  kTraceReset,
   kTraceCount
 };
 void trace_begin(TraceKernel k, cudaStream_t s);

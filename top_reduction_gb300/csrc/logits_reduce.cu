@@ -950,18 +950,21 @@ template <typename T>
 static cudaError_t launch_both(ReduceArgs a, const VocabSplit& split, float* lse, float* sel_logprob,
                                int32_t* topk_ids, float* topk_logprobs, cudaStream_t stream) {
   cudaError_t e;
-  trace_begin(kTraceReduce, stream);
   if (a.vec_ok) {
     constexpr int CH = kTChunkBytes / (kBlock * static_cast<int>(sizeof(T)));  // blocks per chunk
     a.cpr = (a.nblk + CH - 1) / CH;
     const int64_t chunks = static_cast<int64_t>(a.rows) * a.cpr;
     const int grid = static_cast<int>(chunks < split.ctas ? chunks : split.ctas);
+    trace_begin(kTraceReset, stream);
     e = launch_kernel(ticket_reset_kernel, dim3(1), dim3(32), 0, stream, true, a.parts.ticket);
-    if (e == cudaSuccess)
-      e = launch_kernel(logits_stream_tma_kernel<T>, dim3(grid), dim3(kTThreads), static_cast<size_t>(kTSmem), stream,
-                        true, a);
+    trace_end(kTraceReset, stream);
+    if (e != cudaSuccess) return e;
+    trace_begin(kTraceReduce, stream);
+    e = launch_kernel(logits_stream_tma_kernel<T>, dim3(grid), dim3(kTThreads), static_cast<size_t>(kTSmem), stream,
+                      true, a);
   } else {
     a.cpr = 0;
+    trace_begin(kTraceReduce, stream);
     e = launch_kernel(logits_stream_regs_kernel<T>, dim3(split.grid), dim3(kRThreads), 0, stream, false, a);
   }
   trace_end(kTraceReduce, stream);
