@@ -68,7 +68,7 @@ typedef enum lmh_w_layout {
 } lmh_w_layout;
 
 /* Which entry point a workspace is sized for. */
-typedef enum lmh_path { LMH_PATH_PROJECT = 0, LMH_PATH_FROM_LOGITS = 1 } lmh_path;
+typedef enum lmh_path { LMH_PATH_PROJECT = 0, LMH_PATH_FROM_LOGITS = 1, LMH_PATH_PROBE = 2 } lmh_path;
 
 /* Device status bits (OR-ed into *dev_status). */
 #define LMH_DS_BAD_CU_SEQLENS 0x1u       /* cu[0] != 0, cu decreasing, or an empty prefill segment */
@@ -176,6 +176,60 @@ lmh_status lmh_project_logprobs(const void* hidden, int64_t hidden_row_stride, i
                                 float* sel_logprob, int32_t* topk_ids, float* topk_logprobs,
                                 float* logits_out, void* workspace, size_t workspace_bytes,
                                 uint32_t* dev_status, cudaStream_t stream);
+
+/*
+ * lmh_project_logprobs_scaled -- lmh_project_logprobs with a head transform.
+ *
+ * Defined by: vllm-metal release v0.4.0.dev20260831, "Summary": some models
+ * scale their head output (Cohere's logit_scale multiplies the logits,
+ * Granite's logits_scaling divides them), and a head reproduced without the
+ * scale gives silently wrong logits.  Here every logit is
+ * fp32(logit_scale * (A . W)) before the reduction (and in logits_out):
+ * pass logit_scale = s for Cohere, 1 / d for Granite's logits_scaling = d.
+ *
+ *   logit_scale       finite and > 0 (LMH_ERR_INVALID_ARG otherwise); 1 is
+ *                     lmh_project_logprobs itself.
+ * Every other argument, result and error as lmh_project_logprobs.
+ */
+lmh_status lmh_project_logprobs_scaled(const void* hidden, int64_t hidden_row_stride, int32_t num_tokens,
+                                       const int32_t* row_idx, int32_t rows, int32_t H, const void* W,
+                                       lmh_w_layout w_layout, int32_t V, const int32_t* sel_ids,
+                                       const int32_t* row_k, int32_t k_max, float* lse, float* sel_logprob,
+                                       int32_t* topk_ids, float* topk_logprobs, float* logits_out,
+                                       void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                       float logit_scale, cudaStream_t stream);
+
+/*
+ * lmh_probe_selective -- does this library's selective head reproduce the
+ * model's own head output?
+ *
+ * Defined by: vllm-metal release v0.4.0.dev20260831, "Summary"
+ * (supports_selective_logits probes once at load and demands bit-exact
+ * equality with the model's own output; on a mismatch the engine keeps full
+ * logits) and "Testing" (the probe rejects a model that scales its head
+ * output when the scale is not reproduced).
+ *
+ *   hidden, hidden_row_stride, num_tokens, row_idx, rows, H, W, V:
+ *                     as lmh_project_logprobs (row_idx = the rows to probe).
+ *   logit_scale       the head transform to reproduce (1 = none; > 0).
+ *   ref_logits        device f32 [rows x V] (row stride V): the model's own
+ *                     logits of those rows.
+ *   tolerance         an element mismatches when |ours - ref| > tolerance or
+ *                     exactly one of them is NaN; 0 asks for bit-exact values
+ *                     (except that +0 and -0 match).
+ *   mismatches        device u32, out: the number of mismatching elements
+ *                     (written, not accumulated).
+ *   workspace         >= lmh_workspace_bytes(rows, H, V, 0, LMH_PATH_PROBE)
+ *                     bytes, 256-byte aligned.
+ * Errors: as lmh_project_logprobs, and LMH_ERR_INVALID_ARG for a null
+ * ref_logits or mismatches, a negative or NaN tolerance, or a logit_scale
+ * that is not finite and > 0.
+ */
+lmh_status lmh_probe_selective(const void* hidden, int64_t hidden_row_stride, int32_t num_tokens,
+                               const int32_t* row_idx, int32_t rows, int32_t H, const void* W, int32_t V,
+                               float logit_scale, const float* ref_logits, float tolerance,
+                               uint32_t* mismatches, void* workspace, size_t workspace_bytes,
+                               uint32_t* dev_status, cudaStream_t stream);
 
 /*
  * lmh_logprobs_from_logits -- the same per-row reduction for logits that are

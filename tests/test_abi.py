@@ -156,3 +156,25 @@ def test_product_path_has_no_fallback():
     finally:
         lmh.LIB_PATH = real
         lmh._lib = saved
+
+
+def test_head_transform_and_probe_argument_checks(lib):
+    """The scaled projection and the probe reject bad transforms before any launch."""
+    from top_reduction_gb300 import lmh as E
+    P = ctypes.c_void_p
+    for bad in (0.0, -0.5, float("inf"), float("nan")):
+        st = lib.lmh_project_logprobs_scaled(
+            P(0x1000), 64, 8, None, 8, 64, P(0x2000), 0, 4096, None, None, 5, P(0x3000), None, P(0x4000),
+            P(0x5000), None, P(0x10000), 1 << 30, None, bad, None)
+        assert st == E.ERR_INVALID_ARG, bad
+    probe = dict(ref=P(0x8000), tol=0.0, count=P(0x9000), scale=1.0)
+
+    def call(**kw):
+        a = dict(probe, **kw)
+        return lib.lmh_probe_selective(P(0x1000), 64, 8, None, 8, 64, P(0x2000), 4096, a["scale"], a["ref"],
+                                       a["tol"], a["count"], P(0x10000), 1 << 30, None, None)
+    assert call(ref=None) == E.ERR_INVALID_ARG
+    assert call(count=None) == E.ERR_INVALID_ARG
+    assert call(tol=-1.0) == E.ERR_INVALID_ARG
+    assert call(tol=float("nan")) == E.ERR_INVALID_ARG
+    assert call(scale=0.0) == E.ERR_INVALID_ARG

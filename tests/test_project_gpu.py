@@ -201,3 +201,54 @@ def test_single_split_plans(lmh, rows, H, V, k, gather):
     z, orc, A = oracle_rows(b, packed, sel.numpy()[sample], k, row_k=rk)
     sub = {key: v[torch.as_tensor(sample)] for key, v in o.items() if v is not None}
     check_fused(sub, orc, z, A, b["W"], k, row_k=rk, what="one split %s" % ((rows, H, V, k),))
+
+
+@pytest.mark.parametrize("scale", [0.0625, 1.0 / 8.0, 3.5])
+def test_head_transform_logit_scale(lmh, scale):
+    """Head transform (vllm-metal release, Summary: Cohere's logit_scale multiplies
+    the logits, Granite's logits_scaling divides them): every logit is
+    scale * (A . W) before the reduction, and in logits_out."""
+    rows, H, V, k = 200, 136, 4100, 20
+    g = torch.Generator().manual_seed(int(scale * 1000) + 11)
+    T = rows + 5
+    b = {"hidden": torch.randn(T, H, generator=g).to(torch.bfloat16),
+         "W": (torch.randn(V, H, generator=g) / H ** 0.5 * 4).to(torch.bfloat16)}
+    ri = torch.randperm(T, generator=g)[:rows].to(torch.int32)
+    sel = torch.randint(-1, V, (rows,), generator=g, dtype=torch.int32)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    logits = torch.empty((rows, V), dtype=torch.float32, device="cuda")
+    o = lmh.project_logprobs(b["hidden"].cuda(), b["W"].cuda(), row_idx=ri.cuda(), sel=sel, k_max=k,
+                             logits_out=logits, dev_status=st, logit_scale=scale)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rows_np = ri.numpy()
+    z = oracle.project(_bits(b["hidden"]), _bits(b["W"]), row_idx=rows_np) * scale
+    orc = oracle.logprobs(z, sel=sel.numpy(), k_max=k)
+    A = b["hidden"][ri.long()].float().double().numpy()
+    assert_close(logits.cpu().numpy(), z, TOL_FUSED, "scaled logits")
+    check_fused(o, orc, z, A, b["W"], k, what="logit_scale %g" % scale, scale=scale)
+
+
+def test_probe_selective(lmh, tiny):
+    """The load-time probe (vllm-metal release, Summary and Testing): the selective
+    head reproduces the full projection's rows bit-exactly; a head transform that is
+    not reproduced is rejected."""
+    b = tiny
+    hid, W = b["hidden"].cuda(), b["W"].cuda()
+    T, V = hid.shape[0], W.shape[0]
+    ri, _ = gpu_select(lmh, b)
+    rows = ri.numel()
+    full = torch.empty((T, V), dtype=torch.float32, device="cuda")
+    lmh.project_logprobs(hid, W, k_max=0, logits_out=full)
+    full_s = torch.empty((T, V), dtype=torch.float32, device="cuda")
+    lmh.project_logprobs(hid, W, k_max=0, logits_out=full_s, logit_scale=0.0625)
+    ref = full[ri.long()].contiguous()
+    ref_s = full_s[ri.long()].contiguous()
+    assert int(lmh.probe_selective(hid, W, ref, row_idx=ri).item()) == 0
+    assert int(lmh.probe_selective(hid, W, ref_s, row_idx=ri, logit_scale=0.0625).item()) == 0
+    bad = int(lmh.probe_selective(hid, W, ref, row_idx=ri, logit_scale=0.0625).item())
+    assert bad > rows * V // 2       # a scaled head checked against unscaled logits: rejected
+    assert int(lmh.probe_selective(hid, W, ref_s, row_idx=ri, tolerance=1e30).item()) == 0
+    ref_one = ref.clone()
+    ref_one[rows - 1, V - 1] += 1.0
+    assert int(lmh.probe_selective(hid, W, ref_one, row_idx=ri).item()) == 1

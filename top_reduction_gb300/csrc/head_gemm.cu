@@ -70,6 +70,7 @@ struct HeadArgs {
   float* logits_out;
   uint32_t* dev_status;
   int epi_quarters;  // TMEM lane quarters that ever hold rows: ceil(rows / 32) below 128 rows, else 4
+  float logit_scale;  // head transform: every logit is logit_scale * (A . W) (1: none)
   int final_out;   // one vocabulary split: write the final results (out), not partials
   RowOutputs out;
 };
@@ -465,6 +466,10 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kBN + c * kBlock;
             __syncwarp();
             tmem_ld64(taddr, v);
+            if (a.logit_scale != 1.0f) {  // head transform, applied before everything else reads the logits
+#pragma unroll
+              for (int j = 0; j < kBlock; ++j) v[j] *= a.logit_scale;
+            }
             const int nvalid = a.V - col0;
             if (nvalid < kBlock) {
 #pragma unroll
@@ -724,7 +729,8 @@ cudaError_t head_setup() {
 
 cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const void* W, int V, const HeadPlan& plan,
                         const int32_t* sel, const int32_t* row_k, int k_max, Partials parts, float* logits_out,
-                        uint32_t* dev_status, cudaStream_t stream, bool pdl, const RowOutputs* final_out) {
+                        uint32_t* dev_status, cudaStream_t stream, bool pdl, const RowOutputs* final_out,
+                        float logit_scale) {
   if (final_out && plan.splits != 1) return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
   // With fewer than 128 rows (one row tile) the A box covers only the real
@@ -753,6 +759,7 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   a.logits_out = logits_out;
   a.dev_status = dev_status;
   a.epi_quarters = rows < kBM ? (rows + 31) / 32 : 4;
+  a.logit_scale = logit_scale;
   a.final_out = final_out ? 1 : 0;
   a.out = final_out ? *final_out : RowOutputs{nullptr, nullptr, nullptr, nullptr};
   const dim3 grid(plan.grid), block(kHeadThreads);

@@ -3,6 +3,7 @@
 //
 // Nothing here computes results: every step of the path runs in the kernels
 // of select_rows.cu, head_gemm.cu, logits_reduce.cu and merge_partials.cu.
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -139,6 +140,18 @@ static lmh_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LMH_OK : 
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Workspace of lmh_probe_selective: the projection's own workspace (k_max 0),
+// then the materialized logits f32 [rows x V] and an lse [rows].
+static size_t probe_project_bytes(int rows, int hidden, int vocab, int sms) {
+  const HeadPlan p = head_plan(rows, hidden, vocab, 0, sms);
+  return align256(static_cast<size_t>(rows) * static_cast<size_t>(hidden) * 2) + partials_bytes(rows, p.splits, 0);
+}
+static size_t probe_bytes(int rows, int hidden, int vocab, int sms) {
+  if (hidden <= 0) return 0;
+  return probe_project_bytes(rows, hidden, vocab, sms) +
+         align256(static_cast<size_t>(rows) * static_cast<size_t>(vocab) * 4) + align256(static_cast<size_t>(rows) * 4);
+}
+
 }  // namespace lmh
 
 using namespace lmh;
@@ -204,15 +217,19 @@ size_t lmh_workspace_bytes(int32_t rows, int32_t hidden, int32_t vocab, int32_t 
     const VocabSplit vs = logits_reduce_split(rows, vocab, k_max, sms);
     return stream_partials_bytes(rows, vs);
   }
+  if (path == LMH_PATH_PROBE) return probe_bytes(rows, hidden, vocab, sms);
   return 0;
 }
 
-lmh_status lmh_project_logprobs(const void* hidden, int64_t hidden_row_stride, int32_t num_tokens,
-                                const int32_t* row_idx, int32_t rows, int32_t H, const void* W,
-                                lmh_w_layout w_layout, int32_t V, const int32_t* sel_ids, const int32_t* row_k,
-                                int32_t k_max, float* lse, float* sel_logprob, int32_t* topk_ids,
-                                float* topk_logprobs, float* logits_out, void* workspace, size_t workspace_bytes,
-                                uint32_t* dev_status, cudaStream_t stream) {
+}  // extern "C"
+
+// The projection with a head transform (logit_scale 1: none).
+static lmh_status project_impl(const void* hidden, int64_t hidden_row_stride, int32_t num_tokens,
+                               const int32_t* row_idx, int32_t rows, int32_t H, const void* W,
+                               lmh_w_layout w_layout, int32_t V, const int32_t* sel_ids, const int32_t* row_k,
+                               int32_t k_max, float* lse, float* sel_logprob, int32_t* topk_ids,
+                               float* topk_logprobs, float* logits_out, void* workspace, size_t workspace_bytes,
+                               uint32_t* dev_status, float logit_scale, cudaStream_t stream) {
   if (rows < 0 || H <= 0 || V <= 0 || num_tokens < 0) return LMH_ERR_INVALID_ARG;
   if (k_max < 0 || k_max > LMH_K_MAX) return LMH_ERR_UNSUPPORTED;
   if (k_max > V) return LMH_ERR_INVALID_ARG;
@@ -251,7 +268,7 @@ lmh_status lmh_project_logprobs(const void* hidden, int64_t hidden_row_stride, i
   if (e == cudaSuccess) {
     Traced tr(kTraceHead, stream);
     e = launch_head(A, a_stride, rows, H, W, V, plan, sel_ids, row_k, k_max, parts, logits_out, dev_status, stream,
-                    /*pdl=*/gather, one_split ? &outs : nullptr);
+                    /*pdl=*/gather, one_split ? &outs : nullptr, logit_scale);
   }
   if (e == cudaSuccess && !one_split) {
     Traced tr(kTraceMerge, stream);
@@ -259,6 +276,34 @@ lmh_status lmh_project_logprobs(const void* hidden, int64_t hidden_row_stride, i
                      dev_status, stream, /*pdl=*/true);
   }
   return from_cuda(e);
+}
+
+extern "C" {
+
+lmh_status lmh_project_logprobs(const void* hidden, int64_t hidden_row_stride, int32_t num_tokens,
+                                const int32_t* row_idx, int32_t rows, int32_t H, const void* W,
+                                lmh_w_layout w_layout, int32_t V, const int32_t* sel_ids, const int32_t* row_k,
+                                int32_t k_max, float* lse, float* sel_logprob, int32_t* topk_ids,
+                                float* topk_logprobs, float* logits_out, void* workspace, size_t workspace_bytes,
+                                uint32_t* dev_status, cudaStream_t stream) {
+  return project_impl(hidden, hidden_row_stride, num_tokens, row_idx, rows, H, W, w_layout, V, sel_ids, row_k, k_max,
+                      lse, sel_logprob, topk_ids, topk_logprobs, logits_out, workspace, workspace_bytes, dev_status,
+                      1.0f, stream);
+}
+
+static bool valid_scale(float s) { return std::isfinite(s) && s > 0.0f; }
+
+lmh_status lmh_project_logprobs_scaled(const void* hidden, int64_t hidden_row_stride, int32_t num_tokens,
+                                       const int32_t* row_idx, int32_t rows, int32_t H, const void* W,
+                                       lmh_w_layout w_layout, int32_t V, const int32_t* sel_ids,
+                                       const int32_t* row_k, int32_t k_max, float* lse, float* sel_logprob,
+                                       int32_t* topk_ids, float* topk_logprobs, float* logits_out,
+                                       void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                       float logit_scale, cudaStream_t stream) {
+  if (!valid_scale(logit_scale)) return LMH_ERR_INVALID_ARG;
+  return project_impl(hidden, hidden_row_stride, num_tokens, row_idx, rows, H, W, w_layout, V, sel_ids, row_k, k_max,
+                      lse, sel_logprob, topk_ids, topk_logprobs, logits_out, workspace, workspace_bytes, dev_status,
+                      logit_scale, stream);
 }
 
 lmh_status lmh_logprobs_from_logits(const void* logits, lmh_dtype dtype, int32_t rows, int32_t V, int64_t row_stride,
@@ -285,6 +330,29 @@ lmh_status lmh_logprobs_from_logits(const void* logits, lmh_dtype dtype, int32_t
   const cudaError_t e = launch_logits_reduce(logits, dtype, row_stride, rows, V, vs, sel_ids, row_k, k_max, parts,
                                              lse, sel_logprob, topk_ids, topk_logprobs, dev_status, stream);
   return from_cuda(e);
+}
+
+lmh_status lmh_probe_selective(const void* hidden, int64_t hidden_row_stride, int32_t num_tokens,
+                               const int32_t* row_idx, int32_t rows, int32_t H, const void* W, int32_t V,
+                               float logit_scale, const float* ref_logits, float tolerance, uint32_t* mismatches,
+                               void* workspace, size_t workspace_bytes, uint32_t* dev_status, cudaStream_t stream) {
+  if (!ref_logits || !mismatches || !(tolerance >= 0.0f) || !valid_scale(logit_scale)) return LMH_ERR_INVALID_ARG;
+  if (rows < 0 || H <= 0 || V <= 0) return LMH_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return LMH_ERR_INVALID_ARG;
+  int sms = 0;
+  if (device_setup(&sms) != cudaSuccess) return LMH_ERR_CUDA;
+  if (workspace_bytes < probe_bytes(rows, H, V, sms)) return LMH_ERR_WORKSPACE_TOO_SMALL;
+  if (rows == 0) return from_cuda(cudaMemsetAsync(mismatches, 0, sizeof(uint32_t), stream));
+  char* ws = static_cast<char*>(workspace);
+  const size_t proj = probe_project_bytes(rows, H, V, sms);
+  float* ours = reinterpret_cast<float*>(ws + proj);
+  float* lse = reinterpret_cast<float*>(ws + proj + align256(static_cast<size_t>(rows) * static_cast<size_t>(V) * 4));
+  const lmh_status st = project_impl(hidden, hidden_row_stride, num_tokens, row_idx, rows, H, W, LMH_W_VH, V, nullptr,
+                                     nullptr, 0, lse, nullptr, nullptr, nullptr, ours, workspace, proj, dev_status,
+                                     logit_scale, stream);
+  if (st != LMH_OK) return st;
+  return from_cuda(launch_probe_compare(ours, ref_logits, static_cast<int64_t>(rows) * V, tolerance, mismatches, sms,
+                                        stream));
 }
 
 lmh_status lmh_trace_enable(int32_t enable) {

@@ -78,6 +78,10 @@ cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts,
                          const int32_t* row_k, float* lse, float* sel_logprob, int32_t* topk_ids,
                          float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream, bool pdl = false);
 
+// Counts the elements of ours / ref [n] that differ by more than tol (probe.cu).
+cudaError_t launch_probe_compare(const float* ours, const float* ref, int64_t n, float tol, uint32_t* count,
+                                 int num_sms, cudaStream_t stream);
+
 // ---- head projection (head_gemm.cu) ----
 
 // Tile scheduling of the fused head kernel.
@@ -102,7 +106,7 @@ cudaError_t launch_gather_rows(const void* hidden, int64_t hidden_stride, int nu
 cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const void* W, int V,
                         const HeadPlan& plan, const int32_t* sel, const int32_t* row_k, int k_max,
                         Partials parts, float* logits_out, uint32_t* dev_status, cudaStream_t stream,
-                        bool pdl = false, const RowOutputs* final_out = nullptr);
+                        bool pdl = false, const RowOutputs* final_out = nullptr, float logit_scale = 1.0f);
 
 // Launch `kernel` on `stream`; with pdl = true it carries the programmatic
 // stream serialization attribute, so it may start while its predecessor in the

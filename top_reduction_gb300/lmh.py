@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "liblmh.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_TIMEOUT = range(6)
 BF16, F16, F32 = 0, 1, 2
 W_VH, W_HV = 0, 1
-PATH_PROJECT, PATH_FROM_LOGITS = 0, 1
+PATH_PROJECT, PATH_FROM_LOGITS, PATH_PROBE = 0, 1, 2
 K_MAX = 128
 
 DS_BAD_CU_SEQLENS = 0x1
@@ -27,7 +27,8 @@ DS_ROW_IDX_OUT_OF_RANGE = 0x8
 DS_TIMEOUT = 0x10
 
 EXPORTS = ("lmh_select_rows", "lmh_count_selected_rows", "lmh_workspace_bytes",
-           "lmh_project_logprobs", "lmh_logprobs_from_logits", "lmh_status_string",
+           "lmh_project_logprobs", "lmh_project_logprobs_scaled", "lmh_probe_selective",
+           "lmh_logprobs_from_logits", "lmh_status_string",
            "lmh_version", "lmh_trace_enable", "lmh_trace_read", "lmh_trace_reset")
 
 _lib = None
@@ -58,6 +59,12 @@ def load():
     lib.lmh_project_logprobs.argtypes = [P, i64, i32, P, i32, i32, P, ctypes.c_int, i32, P, P, i32,
                                          P, P, P, P, P, P, u64, P, P]
     lib.lmh_project_logprobs.restype = ctypes.c_int
+    lib.lmh_project_logprobs_scaled.argtypes = [P, i64, i32, P, i32, i32, P, ctypes.c_int, i32, P, P, i32,
+                                                P, P, P, P, P, P, u64, P, ctypes.c_float, P]
+    lib.lmh_project_logprobs_scaled.restype = ctypes.c_int
+    lib.lmh_probe_selective.argtypes = [P, i64, i32, P, i32, i32, P, i32, ctypes.c_float, P, ctypes.c_float, P,
+                                        P, u64, P, P]
+    lib.lmh_probe_selective.restype = ctypes.c_int
     lib.lmh_logprobs_from_logits.argtypes = [P, ctypes.c_int, i32, i32, i64, P, P, i32, P, P, P, P,
                                              P, u64, P, P]
     lib.lmh_logprobs_from_logits.restype = ctypes.c_int
@@ -162,11 +169,13 @@ def _workspace(workspace, nbytes, device):
 
 
 def project_logprobs(hidden, W, row_idx=None, rows=None, sel=None, row_k=None, k_max=0,
-                     logits_out=None, workspace=None, dev_status=None, out=None, stream=None):
+                     logits_out=None, workspace=None, dev_status=None, out=None, stream=None, logit_scale=1.0):
     """Selective head projection + per-row lse / selected logprob / top-k.
 
     hidden: bf16 [T, H] (rows may be strided); W: bf16 [V, H] (lm_head.weight);
     row_idx: int32 [rows] device tensor or None (rows 0..rows-1).
+    logit_scale: head transform, every logit is logit_scale * (A . W)
+    (lmh_project_logprobs_scaled); 1.0 is the plain projection.
     Returns a dict with lse, sel_logprob (or None), topk_ids, topk_logprobs.
     """
     assert hidden.is_cuda and hidden.dtype == torch.bfloat16 and hidden.dim() == 2
@@ -185,13 +194,40 @@ def project_logprobs(hidden, W, row_idx=None, rows=None, sel=None, row_k=None, k
     rk_t = _dev_i32(row_k, dev, rows, "row_k")
     o = out if out is not None else _outputs(rows, k_max, sel_t is not None, dev)
     ws = _workspace(workspace, workspace_bytes(rows, H, V, k_max, PATH_PROJECT), dev)
-    st = load().lmh_project_logprobs(
-        _p(hidden), hidden.stride(0) if T > 1 else H, T, _p(row_idx), int(rows), H, _p(W), W_VH, V,
-        _p(sel_t), _p(rk_t), int(k_max), _p(o["lse"]), _p(o["sel_logprob"]), _p(o["topk_ids"]),
-        _p(o["topk_logprobs"]), _p(logits_out), _p(ws), ws.numel() * ws.element_size(), _p(dev_status),
-        _stream(stream))
-    _check(st, "lmh_project_logprobs")
+    args = (_p(hidden), hidden.stride(0) if T > 1 else H, T, _p(row_idx), int(rows), H, _p(W), W_VH, V,
+            _p(sel_t), _p(rk_t), int(k_max), _p(o["lse"]), _p(o["sel_logprob"]), _p(o["topk_ids"]),
+            _p(o["topk_logprobs"]), _p(logits_out), _p(ws), ws.numel() * ws.element_size(), _p(dev_status))
+    if logit_scale == 1.0:
+        _check(load().lmh_project_logprobs(*args, _stream(stream)), "lmh_project_logprobs")
+    else:
+        _check(load().lmh_project_logprobs_scaled(*args, float(logit_scale), _stream(stream)),
+               "lmh_project_logprobs_scaled")
     return o
+
+
+def probe_selective(hidden, W, ref_logits, row_idx=None, rows=None, logit_scale=1.0, tolerance=0.0,
+                    workspace=None, dev_status=None, stream=None):
+    """Mismatching elements between this library's head output for the given rows and the
+    model's own logits `ref_logits` (f32 [rows, V]); returns a device uint32 tensor [1]."""
+    assert hidden.is_cuda and hidden.dtype == torch.bfloat16 and hidden.dim() == 2 and hidden.stride(1) == 1
+    assert W.is_cuda and W.dtype == torch.bfloat16 and W.is_contiguous()
+    T, H = hidden.shape
+    V = W.shape[0]
+    if row_idx is not None:
+        rows = row_idx.numel() if rows is None else rows
+    elif rows is None:
+        rows = T
+    assert ref_logits.is_cuda and ref_logits.dtype == torch.float32 and ref_logits.is_contiguous()
+    assert tuple(ref_logits.shape) == (rows, V)
+    dev = hidden.device
+    count = torch.empty(1, dtype=torch.int32, device=dev)
+    ws = _workspace(workspace, workspace_bytes(rows, H, V, 0, PATH_PROBE), dev)
+    st = load().lmh_probe_selective(
+        _p(hidden), hidden.stride(0) if T > 1 else H, T, _p(row_idx), int(rows), H, _p(W), V, float(logit_scale),
+        _p(ref_logits), float(tolerance), _p(count), _p(ws), ws.numel() * ws.element_size(), _p(dev_status),
+        _stream(stream))
+    _check(st, "lmh_probe_selective")
+    return count
 
 
 _DTYPES = {torch.bfloat16: BF16, torch.float16: F16, torch.float32: F32}
