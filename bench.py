@@ -48,6 +48,10 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
+    p.add_argument("--k", type=int, default=None,
+                   help="override the workload's K (-1: the full-vocabulary output, every id's logprob)")
+    p.add_argument("--logit-scale", type=float, default=1.0,
+                   help="head transform: every logit scaled by this factor (head workloads)")
     return p.parse_args()
 
 
@@ -73,24 +77,44 @@ def make_workload(name, rank=0):
     return b
 
 
+def apply_options(b, args):
+    """--k and --logit-scale on a workload (K -1: every id's logprob; per-row K is then unused)."""
+    if getattr(args, "k", None) is not None:
+        b = dict(b, k=args.k, row_k=None if args.k < 0 else b.get("row_k"))
+    if getattr(args, "logit_scale", 1.0) != 1.0:
+        b = dict(b, logit_scale=args.logit_scale)
+    return b
+
+
 def workload_config(b):
     if b["name"] == "logits_chunk":
         return {"workload": "logits_chunk", "rows": b["rows"], "V": b["V"], "k": b["k"], "dtype_in": "bf16",
                 "l2": "inputs larger than L2 (a 127 MB chunk; 4 chunks rotated)"}
-    return {"workload": b["name"], "rows": int(b["n_sel"]), "tokens": int(b["hidden"].shape[0]),
-            "H": int(b["H"]), "V": int(b["V"]), "k": int(b["k"]),
-            "l2": "inputs larger than L2 (the %.0f MB head is streamed from HBM every step)"
-                  % (b["V"] * b["H"] * 2 / 1e6)}
+    cfg = {"workload": b["name"], "rows": int(b["n_sel"]), "tokens": int(b["hidden"].shape[0]),
+           "H": int(b["H"]), "V": int(b["V"]), "k": int(b["k"]),
+           "l2": "inputs larger than L2 (the %.0f MB head is streamed from HBM every step)"
+                 % (b["V"] * b["H"] * 2 / 1e6)}
+    if b.get("logit_scale", 1.0) != 1.0:
+        cfg["logit_scale"] = b["logit_scale"]
+    return cfg
 
 
 def algorithmic(b):
-    """(bound, per-launch algorithmic amount, unit, peak key) of the dominant kernel."""
+    """(bound, per-launch algorithmic amount, unit) of the dominant kernel (dominant_kernel(b))."""
     if b["name"] == "logits_chunk":
+        if b["k"] < 0:  # the full-vocabulary pass: read the logits, write every fp32 logprob
+            return "hbm", b["rows"] * b["V"] * (2 + 4), "GB/s"
         return "hbm", b["rows"] * b["V"] * 2 + b["rows"] * (2 + 2 * b["k"]) * 4, "GB/s"
     rows, H, V = int(b["n_sel"]), int(b["H"]), int(b["V"])
     if rows >= 256:  # the projection is tensor-bound from a few hundred rows on
         return "tensor", 2.0 * rows * H * V, "TFLOP/s"
     return "hbm", V * H * 2 + rows * H * 2, "GB/s"
+
+
+def dominant_kernel(b):
+    if b["name"] == "logits_chunk":
+        return "full_logprobs" if b["k"] < 0 else "logits_reduce"
+    return "head_logprobs"
 
 
 # ---------------------------------------------------------------------------
@@ -170,6 +194,15 @@ def rejected(clocks):
 # our arm
 # ---------------------------------------------------------------------------
 
+def step_outputs(rows, k, V, with_sel, device):
+    """Preallocated outputs of one call (K -1: [rows, V] logprobs, no ids)."""
+    import torch
+    return {"lse": torch.empty(rows, dtype=torch.float32, device=device),
+            "sel_logprob": torch.empty(rows, dtype=torch.float32, device=device) if with_sel else None,
+            "topk_ids": None if k < 0 else torch.empty((rows, k), dtype=torch.int32, device=device),
+            "topk_logprobs": torch.empty((rows, V if k < 0 else k), dtype=torch.float32, device=device)}
+
+
 class Step:
     """Device-resident inputs, preallocated outputs/workspace and one step of the path."""
 
@@ -189,6 +222,7 @@ class Step:
             self.i = 0
             return
         self.full = b.get("full", False)
+        self.scale = b.get("logit_scale", 1.0)
         self.hidden = b["hidden"].to(device)
         self.W = b["W"].to(device)
         self.cu = b["cu_seqlens"].to(device)
@@ -203,12 +237,7 @@ class Step:
         self.out = self._outputs(self.rows, self.k, True)
 
     def _outputs(self, rows, k, with_sel):
-        import torch
-        d = self.dev
-        return {"lse": torch.empty(rows, dtype=torch.float32, device=d),
-                "sel_logprob": torch.empty(rows, dtype=torch.float32, device=d) if with_sel else None,
-                "topk_ids": torch.empty((rows, k), dtype=torch.int32, device=d),
-                "topk_logprobs": torch.empty((rows, k), dtype=torch.float32, device=d)}
+        return step_outputs(rows, k, int(self.b["V"]), with_sel, self.dev)
 
     def launches_per_step(self):
         if self.chunk:
@@ -223,11 +252,13 @@ class Step:
             return lmh.logprobs_from_logits(x, sel=self.sel, k_max=self.k, workspace=self.ws, out=self.out)
         if self.full:
             return lmh.project_logprobs(self.hidden, self.W, sel=self.sel, row_k=self.row_k, k_max=self.k,
-                                        workspace=self.ws, out=self.out, dev_status=self.status)
+                                        workspace=self.ws, out=self.out, dev_status=self.status,
+                                        logit_scale=self.scale)
         ri, _ = lmh.select_rows(self.cu, self.b["num_decode"], self.mask, max_out_rows=self.rows,
                                 dev_status=self.status)
         return lmh.project_logprobs(self.hidden, self.W, row_idx=ri, sel=self.sel, row_k=self.row_k,
-                                    k_max=self.k, workspace=self.ws, out=self.out, dev_status=self.status)
+                                    k_max=self.k, workspace=self.ws, out=self.out, dev_status=self.status,
+                                    logit_scale=self.scale)
 
 
 def max_over_ranks(ms, dist, device):
@@ -288,11 +319,8 @@ def e2e_leg(lmh, b, device, steps):
 
     def buffers():
         d_in = {key: torch.empty_like(v, device=device) for key, v in h_in.items()}
-        out = {"lse": torch.empty(rows, dtype=torch.float32, device=device),
-               "sel_logprob": torch.empty(rows, dtype=torch.float32, device=device),
-               "topk_ids": torch.empty((rows, k), dtype=torch.int32, device=device),
-               "topk_logprobs": torch.empty((rows, k), dtype=torch.float32, device=device)}
-        h_out = {key: torch.empty(v.shape, dtype=v.dtype).pin_memory() for key, v in out.items()}
+        out = step_outputs(rows, k, int(b["V"]), True, device)
+        h_out = {key: torch.empty(v.shape, dtype=v.dtype).pin_memory() for key, v in out.items() if v is not None}
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
         return {"d_in": d_in, "out": out, "h_out": h_out, "ws": ws, "ev": torch.cuda.Event()}
 
@@ -310,7 +338,7 @@ def e2e_leg(lmh, b, device, steps):
         else:
             ri, _ = lmh.select_rows(d_in["cu"], b["num_decode"], mask, max_out_rows=rows)
             o = lmh.project_logprobs(d_in["hidden"], W, row_idx=ri, sel=d_in["sel"], row_k=row_k, k_max=k,
-                                     workspace=bf["ws"], out=bf["out"])
+                                     workspace=bf["ws"], out=bf["out"], logit_scale=b.get("logit_scale", 1.0))
         for key, v in bf["h_out"].items():
             v.copy_(o[key], non_blocking=True)
         bf["ev"].record()
@@ -402,12 +430,12 @@ class OracleStep:
         self.pos = (self.pos + self.per) % self.n
         sel = b["sel"].numpy()[idx]
         if b["name"] == "logits_chunk":
-            r = o.logprobs(self.x[idx], dtype=o.BF16, sel=sel, k_max=b["k"], return_threads=True)
+            r = o.logprobs(self.x[idx], dtype=o.BF16, sel=sel, k_max=max(int(b["k"]), 0), return_threads=True)
             self.threads = r["threads"]
         else:
             rk = None if b["row_k"] is None else b["row_k"].numpy()[idx]
             z, self.threads = o.project(self.hid, self.W, row_idx=self.ri[idx], return_threads=True)
-            o.logprobs(z, sel=sel, row_k=rk, k_max=b["k"])
+            o.logprobs(z, sel=sel, row_k=rk, k_max=max(int(b["k"]), 0))
         return self.per
 
     def describe(self):
@@ -444,14 +472,14 @@ def run_ours(args):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     _build.build()
-    b = make_workload(args.workload, rank)
+    b = apply_options(make_workload(args.workload, rank), args)
     step = Step(lmh, b, device)
     for _ in range(max(args.warmup, 3)):
         step.run()
     torch.cuda.synchronize()
 
     bound, amount, unit = algorithmic(b)
-    kernel = "logits_reduce" if step.chunk else "head_logprobs"
+    kernel = dominant_kernel(b)
     # Region 1 (the value): plain launches, no per-kernel events, so consecutive kernels of a
     # call can overlap their launch through programmatic dependent launch.
     # Region 2 (the roofline): the same steps with an event pair recorded around every launch
@@ -521,7 +549,7 @@ def run_reference(args):
     if rank != 0:
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    b = make_workload(args.workload)
+    b = apply_options(make_workload(args.workload), args)
     st = OracleStep(b)
     budget = 150.0
     for _ in range(min(args.warmup, 1)):

@@ -49,6 +49,11 @@ extern "C" {
 
 /* Largest k (top-k entries per row) any entry point accepts. */
 #define LMH_K_MAX 128
+/* k_max = LMH_K_FULL asks for the full-vocabulary output: topk_logprobs
+ * receives [rows x V] logprobs in token-id order and topk_ids is not written
+ * (openinfer issue #719, "Acceptance criteria": the -1 behaviour is the
+ * frontend's full-vocabulary contract). */
+#define LMH_K_FULL (-1)
 
 typedef enum lmh_status {
     LMH_OK = 0,
@@ -153,18 +158,21 @@ size_t lmh_workspace_bytes(int32_t rows, int32_t hidden, int32_t vocab, int32_t 
  *   W                 device bf16, layout w_layout (LMH_W_VH only), 16-byte aligned.
  *   sel_ids           device int32 [rows] or NULL; -1 = no selected token (NaN).
  *   row_k             device int32 [rows] or NULL (= k_max); values clamped to [0, k_max].
- *   k_max             0..LMH_K_MAX and <= V.
+ *   k_max             0..LMH_K_MAX and <= V, or LMH_K_FULL.
  *   lse               device fp32 [rows], out.
  *   sel_logprob       device fp32 [rows], out (required when sel_ids != NULL).
  *   topk_ids          device int32 [rows x k_max], out (required when k_max > 0).
- *   topk_logprobs     device fp32 [rows x k_max], out (required when k_max > 0).
+ *   topk_logprobs     device fp32 [rows x k_max], out (required when k_max > 0);
+ *                     with k_max = LMH_K_FULL: device fp32 [rows x V], out,
+ *                     16-byte aligned, entry [i][v] = fp32(z[i][v]) - lse[i]
+ *                     (row_k and topk_ids are ignored).
  *   logits_out        device fp32 [rows x V] or NULL (16-byte aligned): when
  *                     given, the fp32 logits are also written (the
  *                     materializing arm and debugging); the reduction
  *                     results are unchanged.
  *   workspace         device, >= lmh_workspace_bytes(rows, H, V, k_max,
  *                     LMH_PATH_PROJECT) bytes, 256-byte aligned.
- * Errors: LMH_ERR_INVALID_ARG, LMH_ERR_UNSUPPORTED (k_max < 0 or > LMH_K_MAX,
+ * Errors: LMH_ERR_INVALID_ARG, LMH_ERR_UNSUPPORTED (k_max < -1 or > LMH_K_MAX,
  * W layout LMH_W_HV, H % 8 != 0, misaligned pointers),
  * LMH_ERR_WORKSPACE_TOO_SMALL, LMH_ERR_CUDA.  Device: LMH_DS_SEL_OUT_OF_RANGE,
  * LMH_DS_ROW_IDX_OUT_OF_RANGE, LMH_DS_TIMEOUT.
@@ -314,7 +322,8 @@ int32_t lmh_version(void);
  * and total milliseconds of the named kernel ("select_rows", "gather_rows",
  * "head_logprobs", "merge_partials", "logits_reduce" (the streaming pass of
  * lmh_logprobs_from_logits), "logits_select" (its per-row selection),
- * "ticket_reset" (the chunk-counter reset before the streaming pass)) since
+ * "ticket_reset" (the chunk-counter reset before the streaming pass),
+ * "full_logprobs" (the pass that writes the k_max = LMH_K_FULL output)) since
  * the last reset.
  * lmh_trace_reset clears the totals.
  */

@@ -94,7 +94,9 @@ def test_project_argument_checks_return_before_launch(lib):
     assert _call_project(lib, rows=-1) == E.ERR_INVALID_ARG
     assert _call_project(lib, H=0) == E.ERR_INVALID_ARG
     assert _call_project(lib, V=0) == E.ERR_INVALID_ARG
-    assert _call_project(lib, k_max=-1) == E.ERR_UNSUPPORTED        # full-vocabulary -1 output
+    assert _call_project(lib, k_max=-2) == E.ERR_UNSUPPORTED
+    assert _call_project(lib, k_max=-1, lps=None) == E.ERR_INVALID_ARG  # full-vocabulary output needs the buffer
+    assert _call_project(lib, k_max=-1, lps=0x5004) == E.ERR_INVALID_ARG  # ... 16-byte aligned
     assert _call_project(lib, k_max=129) == E.ERR_UNSUPPORTED
     assert _call_project(lib, k_max=5, V=4) == E.ERR_INVALID_ARG     # k > vocab
     assert _call_project(lib, hidden=0) == E.ERR_INVALID_ARG

@@ -168,3 +168,42 @@ def test_layout_paths(lmh, dtype):
         o, st = gpu_run(lmh, wide.cuda()[:, offset:offset + V], sel, k)
         assert st == 0
         check_from_logits(o, oracle_ref(x.contiguous(), sel, k), k, what="%s V=%d offset=%d" % (dtype, V, offset))
+
+
+def _oracle_full(x, lse):
+    """Full-vocabulary logprobs from the oracle's lse: x - lse in f64 (x widened exactly)."""
+    return x.float().double().numpy() - np.asarray(lse)[:, None]
+
+
+def test_full_vocabulary_output(lmh, chunk):
+    """k_max = LMH_K_FULL (openinfer issue #719, Acceptance criteria: the -1 full-vocabulary
+    contract): every id's logprob in id order, within 1e-5 of x - lse."""
+    if chunk["dist"] not in ("normal", "neginf"):
+        pytest.skip("two distributions suffice for the elementwise output")
+    from top_reduction_gb300 import lmh as L
+    x = chunk["logits"]
+    o, st = gpu_run(lmh, x.cuda(), chunk["sel"], L.K_FULL)
+    assert st == 0 and o["topk_ids"] is None
+    assert o["topk_logprobs"].shape == x.shape
+    orc = chunk["oracle"]
+    check_from_logits({"lse": o["lse"], "sel_logprob": o["sel_logprob"]},
+                      {"lse": orc["lse"], "sel_logprob": orc["sel_logprob"]}, 0, what="full lse")
+    got = o["topk_logprobs"].cpu().numpy()
+    want = _oracle_full(x, orc["lse"])
+    fin = np.isfinite(want)
+    assert np.array_equal(np.isfinite(got), fin)
+    assert np.max(np.abs(got[fin] - want[fin])) <= 1e-5
+
+
+@pytest.mark.parametrize("dtype,V", [(torch.bfloat16, 4100), (torch.float32, 1001), (torch.float16, 3000)])
+def test_full_vocabulary_ragged(lmh, dtype, V):
+    from top_reduction_gb300 import lmh as L
+    g = torch.Generator().manual_seed(V)
+    x = (torch.randn(7, V, generator=g) * 3).to(dtype)
+    sel = torch.randint(-1, V, (7,), generator=g, dtype=torch.int32)
+    o, st = gpu_run(lmh, x.cuda(), sel, L.K_FULL)
+    assert st == 0
+    orc = oracle_ref(x, sel, 0)
+    check_from_logits({"lse": o["lse"], "sel_logprob": o["sel_logprob"]},
+                      {"lse": orc["lse"], "sel_logprob": orc["sel_logprob"]}, 0, what="full ragged")
+    assert np.max(np.abs(o["topk_logprobs"].cpu().numpy() - _oracle_full(x, orc["lse"]))) <= 1e-5

@@ -252,3 +252,27 @@ def test_probe_selective(lmh, tiny):
     ref_one = ref.clone()
     ref_one[rows - 1, V - 1] += 1.0
     assert int(lmh.probe_selective(hid, W, ref_one, row_idx=ri).item()) == 1
+
+
+@pytest.mark.parametrize("rows,H,V", [(129, 64, 1000), (8, 1024, 20000)])
+def test_full_vocabulary_output(lmh, rows, H, V):
+    """k_max = LMH_K_FULL on the head path: every id's logprob z - lse in id order
+    (within 2e-2 of the oracle) and exactly fp32(logits_out) - lse."""
+    from top_reduction_gb300 import lmh as L
+    g = torch.Generator().manual_seed(rows + V)
+    T = rows + 3
+    b = {"hidden": torch.randn(T, H, generator=g).to(torch.bfloat16),
+         "W": (torch.randn(V, H, generator=g) / H ** 0.5).to(torch.bfloat16)}
+    ri = torch.randperm(T, generator=g)[:rows].to(torch.int32)
+    sel = torch.randint(-1, V, (rows,), generator=g, dtype=torch.int32)
+    o, st, logits = gpu_project(lmh, b["hidden"].cuda(), b["W"].cuda(), row_idx=ri.cuda(), sel=sel, k=L.K_FULL,
+                                materialize=True)
+    assert st == 0 and o["topk_ids"] is None
+    z, orc, A = oracle_rows(b, ri.numpy(), sel, 0)
+    assert_close(o["lse"].cpu().numpy(), orc["lse"], TOL_FUSED, "full lse")
+    full = o["topk_logprobs"].cpu().numpy()
+    assert_close(full, z - orc["lse"][:, None], TOL_FUSED, "full logprobs")
+    exact = logits.cpu().numpy() - o["lse"].cpu().numpy()[:, None]
+    assert np.array_equal(full, exact.astype(np.float32))
+    o2, _, _ = gpu_project(lmh, b["hidden"].cuda(), b["W"].cuda(), row_idx=ri.cuda(), sel=sel, k=L.K_FULL)
+    assert torch.equal(o2["topk_logprobs"], o["topk_logprobs"])   # same without logits_out

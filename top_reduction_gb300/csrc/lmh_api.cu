@@ -67,7 +67,7 @@ Partials carve_partials(void* base, int rows, int splits, int k_max) {
 // ---------------------------------------------------------------------------
 static const char* const kTraceNames[kTraceCount] = {"select_rows",   "gather_rows",    "head_logprobs",
                                                      "logits_reduce", "merge_partials", "logits_select",
-                                                     "ticket_reset"};
+                                                     "ticket_reset",  "full_logprobs"};
 
 struct TraceRecord {
   int kernel;
@@ -203,6 +203,7 @@ int32_t lmh_count_selected_rows(const int32_t* cu, int32_t num_seqs, int32_t num
 }
 
 size_t lmh_workspace_bytes(int32_t rows, int32_t hidden, int32_t vocab, int32_t k_max, lmh_path path) {
+  if (k_max == LMH_K_FULL) k_max = 0;  // the full-vocabulary output needs the K 0 workspace
   if (rows < 0 || vocab <= 0 || k_max < 0 || k_max > LMH_K_MAX || k_max > vocab) return 0;
   int sms = 0;
   if (device_setup(&sms) != cudaSuccess) return 0;
@@ -227,12 +228,18 @@ size_t lmh_workspace_bytes(int32_t rows, int32_t hidden, int32_t vocab, int32_t 
 static lmh_status project_impl(const void* hidden, int64_t hidden_row_stride, int32_t num_tokens,
                                const int32_t* row_idx, int32_t rows, int32_t H, const void* W,
                                lmh_w_layout w_layout, int32_t V, const int32_t* sel_ids, const int32_t* row_k,
-                               int32_t k_max, float* lse, float* sel_logprob, int32_t* topk_ids,
+                               int32_t k_req, float* lse, float* sel_logprob, int32_t* topk_ids,
                                float* topk_logprobs, float* logits_out, void* workspace, size_t workspace_bytes,
                                uint32_t* dev_status, float logit_scale, cudaStream_t stream) {
   if (rows < 0 || H <= 0 || V <= 0 || num_tokens < 0) return LMH_ERR_INVALID_ARG;
-  if (k_max < 0 || k_max > LMH_K_MAX) return LMH_ERR_UNSUPPORTED;
-  if (k_max > V) return LMH_ERR_INVALID_ARG;
+  if (k_req < LMH_K_FULL || k_req > LMH_K_MAX) return LMH_ERR_UNSUPPORTED;
+  if (k_req > V) return LMH_ERR_INVALID_ARG;
+  // Full-vocabulary output: the reduction runs with K 0 (lse, selected token)
+  // and a pass writes z - lse; the fp32 logits are materialized in the output.
+  const bool full = k_req == LMH_K_FULL;
+  const int32_t k_max = full ? 0 : k_req;
+  if (full && (!topk_logprobs || !aligned(topk_logprobs, 16))) return LMH_ERR_INVALID_ARG;
+  float* z_out = (full && !logits_out) ? topk_logprobs : logits_out;
   if (w_layout != LMH_W_VH && w_layout != LMH_W_HV) return LMH_ERR_INVALID_ARG;
   if (!hidden || !W || !lse || (sel_ids && !sel_logprob) || (k_max > 0 && (!topk_ids || !topk_logprobs)))
     return LMH_ERR_INVALID_ARG;
@@ -267,7 +274,7 @@ static lmh_status project_impl(const void* hidden, int64_t hidden_row_stride, in
   const bool one_split = plan.splits == 1;
   if (e == cudaSuccess) {
     Traced tr(kTraceHead, stream);
-    e = launch_head(A, a_stride, rows, H, W, V, plan, sel_ids, row_k, k_max, parts, logits_out, dev_status, stream,
+    e = launch_head(A, a_stride, rows, H, W, V, plan, sel_ids, row_k, k_max, parts, z_out, dev_status, stream,
                     /*pdl=*/gather, one_split ? &outs : nullptr, logit_scale);
   }
   if (e == cudaSuccess && !one_split) {
@@ -275,6 +282,8 @@ static lmh_status project_impl(const void* hidden, int64_t hidden_row_stride, in
     e = launch_merge(rows, plan.splits, V, k_max, parts, sel_ids, row_k, lse, sel_logprob, topk_ids, topk_logprobs,
                      dev_status, stream, /*pdl=*/true);
   }
+  if (e == cudaSuccess && full)
+    e = launch_full_logprobs(z_out, LMH_F32, V, rows, V, lse, topk_logprobs, stream);
   return from_cuda(e);
 }
 
@@ -312,10 +321,11 @@ lmh_status lmh_logprobs_from_logits(const void* logits, lmh_dtype dtype, int32_t
                                     size_t workspace_bytes, uint32_t* dev_status, cudaStream_t stream) {
   if (rows < 0 || V <= 0 || row_stride < V) return LMH_ERR_INVALID_ARG;
   if (dtype != LMH_BF16 && dtype != LMH_F16 && dtype != LMH_F32) return LMH_ERR_INVALID_ARG;
-  if (k_max < 0 || k_max > LMH_K_MAX) return LMH_ERR_UNSUPPORTED;
+  if (k_max < LMH_K_FULL || k_max > LMH_K_MAX) return LMH_ERR_UNSUPPORTED;
   if (k_max > V) return LMH_ERR_INVALID_ARG;
   if (!logits || !lse || (sel_ids && !sel_logprob) || (k_max > 0 && (!topk_ids || !topk_logprobs)))
     return LMH_ERR_INVALID_ARG;
+  if (k_max == LMH_K_FULL && (!topk_logprobs || !aligned(topk_logprobs, 16))) return LMH_ERR_INVALID_ARG;
   const int64_t elem = dtype == LMH_F32 ? 4 : 2;
   if (!aligned(logits, static_cast<size_t>(elem))) return LMH_ERR_UNSUPPORTED;
   if (rows == 0) return LMH_OK;

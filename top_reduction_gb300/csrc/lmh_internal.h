@@ -78,6 +78,10 @@ cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts,
                          const int32_t* row_k, float* lse, float* sel_logprob, int32_t* topk_ids,
                          float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream, bool pdl = false);
 
+// Full-vocabulary output: out[r][v] = fp32(x[r][v]) - lse[r] (x may alias out for f32).
+cudaError_t launch_full_logprobs(const void* x, lmh_dtype dtype, int64_t row_stride, int rows, int V, const float* lse,
+                                 float* out, cudaStream_t stream);
+
 // Counts the elements of ours / ref [n] that differ by more than tol (probe.cu).
 cudaError_t launch_probe_compare(const float* ours, const float* ref, int64_t n, float tol, uint32_t* count,
                                  int num_sms, cudaStream_t stream);
@@ -137,6 +141,7 @@ enum TraceKernel {
   kTraceMerge,
   kTraceLogitsSelect,
   kTraceReset,
+  kTraceFull,
   kTraceCount
 };
 void trace_begin(TraceKernel k, cudaStream_t s);

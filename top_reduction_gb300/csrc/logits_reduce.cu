@@ -877,6 +877,61 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
 }
 
 // ---------------------------------------------------------------------------
+// full-vocabulary output (k_max = LMH_K_FULL)
+// ---------------------------------------------------------------------------
+// out[r][v] = fp32(x[r][v]) - lse[r] for every id: one coalesced pass, 8
+// elements per thread, reads x, writes f32.  `x` may be `out` itself (the
+// head path materializes its fp32 logits there first).
+constexpr int kFThreads = 256;
+constexpr int kFPerThread = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(kFThreads) full_logprobs_kernel(const T* x, int64_t row_stride, int V,
+                                                                   const float* __restrict__ lse, float* out) {
+  pdl_wait();  // lse (and in place, the logits) come from the kernels launched just before
+  const int row = blockIdx.x;  // rows on x (no 65535 limit), column chunks on y
+  const float l = lse[row];
+  const T* src = x + static_cast<int64_t>(row) * row_stride;
+  float* dst = out + static_cast<int64_t>(row) * V;
+  const int base = blockIdx.y * (kFThreads * kFPerThread) + threadIdx.x;
+  float v[kFPerThread];
+#pragma unroll
+  for (int u = 0; u < kFPerThread; ++u) {
+    const int c = base + u * kFThreads;
+    v[u] = c < V ? Vec16<T>::at(src, c) : 0.0f;
+  }
+#pragma unroll
+  for (int u = 0; u < kFPerThread; ++u) {
+    const int c = base + u * kFThreads;
+    if (c < V) dst[c] = v[u] - l;
+  }
+}
+
+cudaError_t launch_full_logprobs(const void* x, lmh_dtype dtype, int64_t row_stride, int rows, int V, const float* lse,
+                                 float* out, cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  const dim3 grid(rows, (V + kFThreads * kFPerThread - 1) / (kFThreads * kFPerThread));
+  cudaError_t e;
+  trace_begin(kTraceFull, stream);
+  switch (dtype) {
+    case LMH_BF16:
+      e = launch_kernel(full_logprobs_kernel<__nv_bfloat16>, grid, dim3(kFThreads), 0, stream, true,
+                        static_cast<const __nv_bfloat16*>(x), row_stride, V, lse, out);
+      break;
+    case LMH_F16:
+      e = launch_kernel(full_logprobs_kernel<__half>, grid, dim3(kFThreads), 0, stream, true,
+                        static_cast<const __half*>(x), row_stride, V, lse, out);
+      break;
+    default:
+      e = launch_kernel(full_logprobs_kernel<float>, grid, dim3(kFThreads), 0, stream, true,
+                        static_cast<const float*>(x), row_stride, V, lse, out);
+      break;
+  }
+  trace_end(kTraceFull, stream);
+  return e;
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 
@@ -980,6 +1035,9 @@ cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t ro
                                  VocabSplit split, const int32_t* sel, const int32_t* row_k, int k_max,
                                  Partials parts, float* lse, float* sel_logprob, int32_t* topk_ids,
                                  float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream) {
+  // Full-vocabulary output: the reduction with K 0 (lse, selected token), then z - lse for every id.
+  const bool full = k_max == LMH_K_FULL;
+  if (full) k_max = 0;
   const int64_t es = dtype == LMH_F32 ? 4 : 2;
   ReduceArgs a;
   a.logits = static_cast<const char*>(logits);
@@ -999,14 +1057,20 @@ cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t ro
   a.k_max = k_max;
   a.parts = parts;
   a.dev_status = dev_status;
+  cudaError_t e;
   switch (dtype) {
     case LMH_BF16:
-      return launch_both<__nv_bfloat16>(a, split, lse, sel_logprob, topk_ids, topk_logprobs, stream);
+      e = launch_both<__nv_bfloat16>(a, split, lse, sel_logprob, topk_ids, topk_logprobs, stream);
+      break;
     case LMH_F16:
-      return launch_both<__half>(a, split, lse, sel_logprob, topk_ids, topk_logprobs, stream);
+      e = launch_both<__half>(a, split, lse, sel_logprob, topk_ids, topk_logprobs, stream);
+      break;
     default:
-      return launch_both<float>(a, split, lse, sel_logprob, topk_ids, topk_logprobs, stream);
+      e = launch_both<float>(a, split, lse, sel_logprob, topk_ids, topk_logprobs, stream);
+      break;
   }
+  if (e == cudaSuccess && full) e = launch_full_logprobs(logits, dtype, row_stride, rows, V, lse, topk_logprobs, stream);
+  return e;
 }
 
 }  // namespace lmh

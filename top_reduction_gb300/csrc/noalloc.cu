@@ -81,9 +81,11 @@ extern "C" lmh_status lmh_logprobs_from_logits_static(const void* logits, lmh_dt
                                                       uint32_t* dev_status, cudaStream_t stream) {
   if (rows < 0 || V <= 0 || row_stride < V) return LMH_ERR_INVALID_ARG;
   if (dtype != LMH_BF16 && dtype != LMH_F16 && dtype != LMH_F32) return LMH_ERR_INVALID_ARG;
-  if (k_max < 0 || k_max > LMH_K_MAX) return LMH_ERR_UNSUPPORTED;
+  if (k_max < LMH_K_FULL || k_max > LMH_K_MAX) return LMH_ERR_UNSUPPORTED;
   if (k_max > V) return LMH_ERR_INVALID_ARG;
   if (!logits || !lse || (sel_ids && !sel_logprob) || (k_max > 0 && (!topk_ids || !topk_logprobs)))
+    return LMH_ERR_INVALID_ARG;
+  if (k_max == LMH_K_FULL && (!topk_logprobs || (reinterpret_cast<uintptr_t>(topk_logprobs) % 16) != 0))
     return LMH_ERR_INVALID_ARG;
   const int64_t elem = dtype == LMH_F32 ? 4 : 2;
   if ((reinterpret_cast<uintptr_t>(logits) % static_cast<uintptr_t>(elem)) != 0) return LMH_ERR_UNSUPPORTED;

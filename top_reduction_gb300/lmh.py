@@ -19,6 +19,7 @@ BF16, F16, F32 = 0, 1, 2
 W_VH, W_HV = 0, 1
 PATH_PROJECT, PATH_FROM_LOGITS, PATH_PROBE = 0, 1, 2
 K_MAX = 128
+K_FULL = -1  # k_max for the full-vocabulary output: topk_logprobs is [rows, V] in id order
 
 DS_BAD_CU_SEQLENS = 0x1
 DS_SEL_OUT_OF_RANGE = 0x2
@@ -153,9 +154,13 @@ def workspace_bytes(rows, hidden, vocab, k_max, path):
     return int(n)
 
 
-def _outputs(rows, k_max, with_sel, device):
+def _outputs(rows, k_max, with_sel, device, V=None):
     out = {"lse": torch.empty(rows, dtype=torch.float32, device=device)}
     out["sel_logprob"] = torch.empty(rows, dtype=torch.float32, device=device) if with_sel else None
+    if k_max == K_FULL:  # every id's logprob, in id order; no ids
+        out["topk_ids"] = None
+        out["topk_logprobs"] = torch.empty((rows, V), dtype=torch.float32, device=device)
+        return out
     out["topk_ids"] = torch.empty((rows, k_max), dtype=torch.int32, device=device)
     out["topk_logprobs"] = torch.empty((rows, k_max), dtype=torch.float32, device=device)
     return out
@@ -192,7 +197,7 @@ def project_logprobs(hidden, W, row_idx=None, rows=None, sel=None, row_k=None, k
         rows = T
     sel_t = _dev_i32(sel, dev, rows, "sel")
     rk_t = _dev_i32(row_k, dev, rows, "row_k")
-    o = out if out is not None else _outputs(rows, k_max, sel_t is not None, dev)
+    o = out if out is not None else _outputs(rows, k_max, sel_t is not None, dev, V)
     ws = _workspace(workspace, workspace_bytes(rows, H, V, k_max, PATH_PROJECT), dev)
     args = (_p(hidden), hidden.stride(0) if T > 1 else H, T, _p(row_idx), int(rows), H, _p(W), W_VH, V,
             _p(sel_t), _p(rk_t), int(k_max), _p(o["lse"]), _p(o["sel_logprob"]), _p(o["topk_ids"]),
@@ -241,7 +246,7 @@ def logprobs_from_logits(logits, sel=None, row_k=None, k_max=0, workspace=None, 
     dev = logits.device
     sel_t = _dev_i32(sel, dev, rows, "sel")
     rk_t = _dev_i32(row_k, dev, rows, "row_k")
-    o = out if out is not None else _outputs(rows, k_max, sel_t is not None, dev)
+    o = out if out is not None else _outputs(rows, k_max, sel_t is not None, dev, V)
     ws = _workspace(workspace, workspace_bytes(rows, 0, V, k_max, PATH_FROM_LOGITS), dev)
     stride = logits.stride(0) if rows > 1 else V
     st = load().lmh_logprobs_from_logits(
@@ -257,7 +262,7 @@ def logprobs_from_logits(logits, sel=None, row_k=None, k_max=0, workspace=None, 
 # ---------------------------------------------------------------------------
 
 TRACE_KERNELS = ("select_rows", "gather_rows", "head_logprobs", "logits_reduce", "merge_partials",
-                 "logits_select", "ticket_reset")
+                 "logits_select", "ticket_reset", "full_logprobs")
 
 
 def trace_enable(on=True):
