@@ -29,6 +29,10 @@ MUT_LOGPROB_SIGN = 5
 MUT_TIE_ID_DESC = 6
 MUT_TOPK_SKIP_FIRST = 7
 MUT_DECODE_LAST_ONLY = 8
+MUT_PHILOX_9_ROUNDS = 9
+MUT_GUMBEL_SIGN = 10
+MUT_MASK_IGNORED = 11
+MUT_TEMP_TIMES = 12
 
 _lib = None
 
@@ -57,6 +61,12 @@ def _load():
         lib.oracle_set_mutation.argtypes = [ctypes.c_int]
         lib.oracle_get_mutation.restype = ctypes.c_int
         lib.oracle_cores.restype = ctypes.c_int
+        lib.oracle_philox4x32_10.argtypes = [P, P, P]
+        lib.oracle_philox4x32_10.restype = None
+        lib.oracle_sample_uniform.argtypes = [ctypes.c_uint64, i64, i32]
+        lib.oracle_sample_uniform.restype = ctypes.c_double
+        lib.oracle_sample.argtypes = [P, i32, i32, P, P, i32, ctypes.c_uint64, P, P, P, P]
+        lib.oracle_sample.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -176,3 +186,43 @@ def logprobs(x, dtype=None, sel=None, row_k=None, k_max=0, threads=0, return_thr
     if return_threads:
         out["threads"] = int(used[0])
     return out
+
+
+def philox4x32_10(counter, key):
+    """Philox4x32 with 10 rounds (Salmon et al., SC 2011): 4 uint32 counter words and
+    2 key words to 4 uint32 output words."""
+    c = np.ascontiguousarray(counter, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    assert c.shape == (4,) and k.shape == (2,)
+    out = np.empty(4, dtype=np.uint32)
+    _load().oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def sample_uniform(seed, offset, token):
+    """The uniform in (0, 1) that Gumbel-max sampling draws for `token` of a row."""
+    return float(_load().oracle_sample_uniform(int(seed) & (2 ** 64 - 1), int(offset), int(token)))
+
+
+def sample(z, temperature=None, mask=None, seed=0, offsets=None):
+    """Gumbel-max sampling over f64 logits z [rows, V]: ids, best scores and runner-up scores.
+
+    temperature: [rows] float32 or None (1.0); T <= 0 is greedy.  mask: uint32
+    [rows, ceil(V/32)] allowed-token bits or None.  offsets: int64 [rows] or None
+    (= row index), the per-row counter offset.  Ties go to the smaller id; -1 when
+    no token is allowed.
+    """
+    z = np.ascontiguousarray(z, dtype=np.float64)
+    rows, V = z.shape
+    t = None if temperature is None else np.ascontiguousarray(temperature, dtype=np.float32)
+    m = None if mask is None else np.ascontiguousarray(mask, dtype=np.uint32)
+    words = (V + 31) // 32 if m is None else m.shape[1]
+    off = None if offsets is None else np.ascontiguousarray(offsets, dtype=np.int64)
+    ids = np.empty(rows, dtype=np.int32)
+    best = np.empty(rows, dtype=np.float64)
+    second = np.empty(rows, dtype=np.float64)
+    rc = _load().oracle_sample(_ptr(z), rows, V, _ptr(t), _ptr(m), int(words), int(seed) & (2 ** 64 - 1),
+                               _ptr(off), _ptr(ids), _ptr(best), _ptr(second))
+    if rc:
+        raise OracleError(rc, "sample")
+    return ids, best, second

@@ -24,6 +24,19 @@
  *       then a top-k pass; MTPLX PR #532, "Change": logprob = logit - lse
  *       at the survivors and at the scored token, exact ties listed by
  *       ascending token id.
+ *   oracle_philox4x32_10 -- the counter-based generator Philox4x32 with
+ *       10 rounds, from its published definition (Salmon, Moraes, Dror,
+ *       Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011):
+ *       per round, two 32x32->64 products of counter words with the round
+ *       multipliers, the high halves XORed with the other counter words and
+ *       the key, the key bumped by the Weyl constants.
+ *   oracle_sample       -- Gumbel-max sampling: the token maximising
+ *       z / T + g over the allowed tokens (g = -log(-log u) Gumbel noise,
+ *       u uniform in (0, 1) from Philox keyed by (seed, row offset, token));
+ *       T <= 0 is greedy (argmax z).  No page defines it: it is the NEXT
+ *       item "device-side sampling in the head epilogue" with the grammar
+ *       bitmask applied in the compacted layout (vllm-metal release,
+ *       "Testing": bitmask application under the compacted layout).
  *
  * Readings where the pages are silent (each also listed in the design doc):
  *   - decode sequences keep all their rows [cu[s], cu[s+1]);
@@ -74,6 +87,10 @@
 #define MUT_TIE_ID_DESC 6       /* exact ties by descending id                */
 #define MUT_TOPK_SKIP_FIRST 7   /* rank j reports sorted entry j+1            */
 #define MUT_DECODE_LAST_ONLY 8  /* decode sequences keep only their last row  */
+#define MUT_PHILOX_9_ROUNDS 9   /* Philox with 9 rounds                       */
+#define MUT_GUMBEL_SIGN 10      /* g = +log(-log u)                           */
+#define MUT_MASK_IGNORED 11     /* disallowed tokens can be sampled           */
+#define MUT_TEMP_TIMES 12       /* z * T instead of z / T                     */
 
 static int g_mutation = MUT_NONE;
 
@@ -418,3 +435,93 @@ int oracle_logprobs(const void* x, int dtype, int32_t rows, int32_t V, int64_t r
 
 /* number of online cores, for reporting */
 int oracle_cores(void) { return resolve_threads(0); }
+
+/* ------------------------------------------------------------------------
+ * Philox4x32-10 (Salmon et al., SC 2011).  One round maps counter (c0..c3)
+ * and key (k0, k1) to
+ *     (hi(M1*c2) ^ c1 ^ k0, lo(M1*c2), hi(M0*c0) ^ c3 ^ k1, lo(M0*c0))
+ * with M0 = 0xD2511F53, M1 = 0xCD9E8D57; after each round the key grows by
+ * the Weyl increments (0x9E3779B9, 0xBB67AE85).  Ten rounds.
+ * ------------------------------------------------------------------------ */
+void oracle_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    const int rounds = g_mutation == MUT_PHILOX_9_ROUNDS ? 9 : 10;
+    for (int r = 0; r < rounds; ++r) {
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        const uint32_t n1 = (uint32_t)p1;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        const uint32_t n3 = (uint32_t)p0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The uniform of token v in a row with counter offset `off` under `seed`:
+ * Philox word (v & 3) of counter (v >> 2, lo(off), hi(off), 0x53414D50),
+ * key (lo(seed), hi(seed)); u = ((w >> 9) + 0.5) * 2^-23, exactly
+ * representable in fp32 and strictly inside (0, 1). */
+double oracle_sample_uniform(uint64_t seed, int64_t off, int32_t v)
+{
+    const uint32_t ctr[4] = {(uint32_t)v >> 2, (uint32_t)(uint64_t)off, (uint32_t)((uint64_t)off >> 32),
+                             0x53414D50u};
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t w[4];
+    oracle_philox4x32_10(ctr, key, w);
+    return ((double)(w[v & 3] >> 9) + 0.5) * ldexp(1.0, -23);
+}
+
+/* Gumbel-max sampling over z (f64 [rows x V], row stride V).
+ *   temperature  [rows] or NULL (= 1); T <= 0 selects argmax z (greedy)
+ *   mask         [rows x mask_words] or NULL: token v is allowed when bit
+ *                (v % 32) of word v / 32 is set
+ *   offsets      [rows] or NULL (= the row index): the counter offset
+ * out_ids[i] = the allowed token with the largest score z/T + g (greedy: z),
+ * ties to the smaller id; -1 when no token is allowed.  out_score[i] is
+ * that score, out_second[i] the largest score of any other allowed token
+ * (-inf if none), for near-tie checks. */
+int oracle_sample(const double* z, int32_t rows, int32_t V, const float* temperature, const uint32_t* mask,
+                  int32_t mask_words, uint64_t seed, const int64_t* offsets, int32_t* out_ids,
+                  double* out_score, double* out_second)
+{
+    if (!z || rows < 0 || V <= 0 || !out_ids || !out_score || !out_second) return ORACLE_ERR_ARG;
+    if (mask && mask_words < (V + 31) / 32) return ORACLE_ERR_ARG;
+    for (int32_t i = 0; i < rows; ++i) {
+        const double T = temperature ? (double)temperature[i] : 1.0;
+        const int greedy = T <= 0.0;
+        const int64_t off = offsets ? offsets[i] : (int64_t)i;
+        int32_t best = -1;
+        double bs = -INFINITY, second = -INFINITY;
+        for (int32_t v = 0; v < V; ++v) {
+            if (mask && g_mutation != MUT_MASK_IGNORED &&
+                !((mask[(int64_t)i * mask_words + v / 32] >> (v % 32)) & 1u))
+                continue;
+            const double x = z[(int64_t)i * V + v];
+            double s;
+            if (greedy) {
+                s = x;
+            } else {
+                const double u = oracle_sample_uniform(seed, off, v);
+                double g = -log(-log(u));
+                if (g_mutation == MUT_GUMBEL_SIGN) g = -g;
+                s = (g_mutation == MUT_TEMP_TIMES ? x * T : x / T) + g;
+            }
+            if (best < 0 || s > bs) {
+                if (best >= 0) second = bs;
+                best = v;
+                bs = s;
+            } else if (s > second) {
+                second = s;
+            }
+        }
+        out_ids[i] = best;
+        out_score[i] = best >= 0 ? bs : -INFINITY;
+        out_second[i] = second;
+    }
+    return ORACLE_OK;
+}

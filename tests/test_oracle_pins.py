@@ -316,11 +316,74 @@ def pin_page_sizes():
     assert workloads.decode_batch.__defaults__ is not None
 
 
+def pin_philox_kat():
+    """Philox4x32-10 reproduces the generator's published known-answer vectors."""
+    for vec in _golden("philox4x32_10_kat.json")["vectors"]:
+        ctr = [int(w, 16) for w in vec["counter"]]
+        key = [int(w, 16) for w in vec["key"]]
+        want = [int(w, 16) for w in vec["output"]]
+        assert oracle.philox4x32_10(ctr, key).tolist() == want, vec
+
+
+def pin_sample_uniforms():
+    """The sampling uniforms lie strictly inside (0, 1) on the 2^-24 grid (odd multiples,
+    so exact in fp32), and differ across tokens, offsets and seeds."""
+    us = [oracle.sample_uniform(7, 3, v) for v in range(400)]
+    for u in us:
+        assert 0.0 < u < 1.0
+        m = u * 2 ** 24
+        assert m == int(m) and int(m) % 2 == 1
+    assert len(set(us)) == len(us)
+    assert oracle.sample_uniform(7, 4, 0) != oracle.sample_uniform(7, 3, 0)
+    assert oracle.sample_uniform(8, 3, 0) != oracle.sample_uniform(7, 3, 0)
+
+
+def pin_gumbel_max_distribution():
+    """argmax(z/T + Gumbel) draws token v with probability softmax(z/T)_v: the frequencies
+    over 20000 row offsets pass a chi-square test (4 degrees of freedom) at T = 0.5, 1, 2."""
+    z = np.array([0.2, -1.0, 1.5, 0.0, 0.7])
+    n = 20000
+    for T in (0.5, 1.0, 2.0):
+        ids, _, _ = oracle.sample(np.tile(z, (n, 1)), temperature=np.full(n, T, np.float32), seed=12345,
+                                  offsets=np.arange(n, dtype=np.int64))
+        p = np.exp(z / T - np.max(z / T))
+        p /= p.sum()
+        counts = np.bincount(ids, minlength=len(z))
+        chi2 = float(np.sum((counts - n * p) ** 2 / (n * p)))
+        assert chi2 < 30.0, (T, chi2, counts, n * p)
+
+
+def pin_sample_greedy_and_mask():
+    """T <= 0 is argmax z with ties to the smaller id; disallowed tokens are never drawn;
+    a row with no allowed token gives -1; a fixed (seed, offset) gives a fixed draw."""
+    z = np.array([[0.5, 2.0, 2.0, -1.0], [3.0, 1.0, 0.0, -1.0], [0.0, 0.0, 0.0, 0.0]])
+    ids, _, _ = oracle.sample(z, temperature=np.array([0.0, -1.0, 0.0], np.float32))
+    assert ids.tolist() == [1, 0, 0]
+    n, V = 3000, 40
+    rng = np.random.default_rng(5)
+    zz = rng.normal(size=(n, V))
+    allowed = [3, 17, 33, 39]
+    mask = np.zeros((n, 2), np.uint32)
+    for v in allowed:
+        mask[:, v // 32] |= np.uint32(1 << (v % 32))
+    ids, _, _ = oracle.sample(zz, mask=mask, seed=9)
+    assert set(ids.tolist()) <= set(allowed) and len(set(ids.tolist())) == len(allowed)
+    ids_g, _, _ = oracle.sample(zz, temperature=np.zeros(n, np.float32), mask=mask)
+    assert np.array_equal(ids_g, np.array(allowed)[np.argmax(zz[:, allowed], axis=1)])
+    none, _, _ = oracle.sample(zz[:2], mask=np.zeros((2, 2), np.uint32))
+    assert none.tolist() == [-1, -1]
+    a, _, _ = oracle.sample(zz[:50], seed=1)
+    b, _, _ = oracle.sample(zz[:50], seed=1)
+    c, _, _ = oracle.sample(zz[:50], seed=2)
+    assert np.array_equal(a, b) and not np.array_equal(a, c)
+
+
 PINS = [pin_select_examples, pin_select_properties, pin_select_rejects,
         pin_project_exact_integers, pin_project_against_exact_sum,
         pin_selected_equals_full_sliced, pin_brute_force_tiny, pin_torch_f64_crosscheck,
         pin_invariants, pin_closed_forms, pin_hand_example, pin_fewer_finite_than_k,
-        pin_dtype_conversions, pin_selected_id_range, pin_page_sizes]
+        pin_dtype_conversions, pin_selected_id_range, pin_page_sizes,
+        pin_philox_kat, pin_sample_uniforms, pin_gumbel_max_distribution, pin_sample_greedy_and_mask]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -337,6 +400,10 @@ MUTATIONS = {
     oracle.MUT_TIE_ID_DESC: "exact ties by descending id",
     oracle.MUT_TOPK_SKIP_FIRST: "top-K off by one rank",
     oracle.MUT_DECODE_LAST_ONLY: "multi-row decode keeps only its last row",
+    oracle.MUT_PHILOX_9_ROUNDS: "Philox with 9 rounds",
+    oracle.MUT_GUMBEL_SIGN: "Gumbel noise with the wrong sign",
+    oracle.MUT_MASK_IGNORED: "grammar bitmask ignored",
+    oracle.MUT_TEMP_TIMES: "logits multiplied by the temperature",
 }
 
 
