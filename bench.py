@@ -52,6 +52,8 @@ def parse_args():
                    help="override the workload's K (-1: the full-vocabulary output, every id's logprob)")
     p.add_argument("--logit-scale", type=float, default=1.0,
                    help="head transform: every logit scaled by this factor (head workloads)")
+    p.add_argument("--sample", action="store_true",
+                   help="device-side Gumbel-max sampling of every row at temperature 1 (head workloads)")
     return p.parse_args()
 
 
@@ -83,6 +85,8 @@ def apply_options(b, args):
         b = dict(b, k=args.k, row_k=None if args.k < 0 else b.get("row_k"))
     if getattr(args, "logit_scale", 1.0) != 1.0:
         b = dict(b, logit_scale=args.logit_scale)
+    if getattr(args, "sample", False) and b["name"] != "logits_chunk":
+        b = dict(b, sample=True)
     return b
 
 
@@ -96,6 +100,8 @@ def workload_config(b):
                  % (b["V"] * b["H"] * 2 / 1e6)}
     if b.get("logit_scale", 1.0) != 1.0:
         cfg["logit_scale"] = b["logit_scale"]
+    if b.get("sample"):
+        cfg["sampling"] = "Gumbel-max, temperature 1, every row"
     return cfg
 
 
@@ -223,6 +229,10 @@ class Step:
             return
         self.full = b.get("full", False)
         self.scale = b.get("logit_scale", 1.0)
+        self.sampling = None
+        if b.get("sample"):
+            self.sampling = {"temperature": torch.ones(int(b["n_sel"]), dtype=torch.float32, device=device),
+                             "seed": 1234, "offsets": torch.arange(int(b["n_sel"]), dtype=torch.int64, device=device)}
         self.hidden = b["hidden"].to(device)
         self.W = b["W"].to(device)
         self.cu = b["cu_seqlens"].to(device)
@@ -253,12 +263,12 @@ class Step:
         if self.full:
             return lmh.project_logprobs(self.hidden, self.W, sel=self.sel, row_k=self.row_k, k_max=self.k,
                                         workspace=self.ws, out=self.out, dev_status=self.status,
-                                        logit_scale=self.scale)
+                                        logit_scale=self.scale, sampling=self.sampling)
         ri, _ = lmh.select_rows(self.cu, self.b["num_decode"], self.mask, max_out_rows=self.rows,
                                 dev_status=self.status)
         return lmh.project_logprobs(self.hidden, self.W, row_idx=ri, sel=self.sel, row_k=self.row_k,
                                     k_max=self.k, workspace=self.ws, out=self.out, dev_status=self.status,
-                                    logit_scale=self.scale)
+                                    logit_scale=self.scale, sampling=self.sampling)
 
 
 def max_over_ranks(ms, dist, device):

@@ -81,6 +81,7 @@ typedef enum lmh_path { LMH_PATH_PROJECT = 0, LMH_PATH_FROM_LOGITS = 1, LMH_PATH
 #define LMH_DS_ROWS_OVERFLOW 0x4u        /* more selected rows than max_out_rows (extra rows dropped) */
 #define LMH_DS_ROW_IDX_OUT_OF_RANGE 0x8u /* a row index outside [0, num_tokens) (row reads zeros)   */
 #define LMH_DS_TIMEOUT 0x10u             /* a bounded device-side wait gave up (kernel returned)     */
+#define LMH_DS_NO_ALLOWED_TOKEN 0x20u    /* sampling: a row's mask allows no token (id -1, NaN)      */
 
 /*
  * lmh_select_rows -- which rows of a packed batch are sampled.
@@ -206,6 +207,55 @@ lmh_status lmh_project_logprobs_scaled(const void* hidden, int64_t hidden_row_st
                                        int32_t* topk_ids, float* topk_logprobs, float* logits_out,
                                        void* workspace, size_t workspace_bytes, uint32_t* dev_status,
                                        float logit_scale, cudaStream_t stream);
+
+/*
+ * Device-side sampling (lmh_project_logprobs_sample), Gumbel-max over the
+ * allowed tokens of each row; the grammar bitmask is given per selected row
+ * (the compacted layout: vllm-metal release v0.4.0.dev20260831, "Testing",
+ * bitmask application under the compacted layout).
+ *
+ * For row i, with z the (scaled) fp32 logits of lmh_project_logprobs:
+ *   allowed(v)  = allowed_mask is NULL, or bit (v % 32) of
+ *                 allowed_mask[i * mask_words + v / 32] is set;
+ *   T           = temperature[i] (1 when temperature is NULL);
+ *   score(v)    = z[i][v] / T + g(v) for T > 0, z[i][v] for T <= 0 (greedy);
+ *   g(v)        = -log(-log u), u = ((w >> 9) + 0.5) * 2^-23, w = word (v & 3)
+ *                 of Philox4x32-10 (Salmon et al., SC 2011) with counter
+ *                 (v >> 2, lo(off), hi(off), 0x53414D50), key (lo(seed),
+ *                 hi(seed)), off = offsets[i] (i when offsets is NULL);
+ *   sampled_ids[i] = the allowed v with the largest score, ties to the
+ *                 smaller id; -1 when no token is allowed (and
+ *                 LMH_DS_NO_ALLOWED_TOKEN is set);
+ *   sampled_logprob[i] = z[i][sampled] - lse[i] (the unmasked, untempered
+ *                 distribution); NaN for -1.
+ * The noise is computed with fast fp32 logarithms; a draw can differ from an
+ * exact-arithmetic draw only when two scores are within the fp32 rounding of
+ * the head and the noise.
+ */
+typedef struct lmh_sampling {
+  const float* temperature;     /* device fp32 [rows] or NULL */
+  const uint32_t* allowed_mask; /* device u32 [rows x mask_words] or NULL */
+  int32_t mask_words;           /* >= ceil(V / 32) when allowed_mask is given */
+  uint64_t seed;
+  const int64_t* offsets;       /* device int64 [rows] or NULL */
+  int32_t* sampled_ids;         /* device int32 [rows], out (required) */
+  float* sampled_logprob;       /* device fp32 [rows], out, or NULL */
+} lmh_sampling;
+
+/*
+ * lmh_project_logprobs_sample -- lmh_project_logprobs_scaled plus the
+ * sampled token of every row (the same pass over W).  sampling may not be
+ * NULL; its pointers are all device memory owned by the caller.
+ * Errors: as lmh_project_logprobs_scaled, and LMH_ERR_INVALID_ARG for a
+ * NULL sampling or sampled_ids, or mask_words < ceil(V / 32) with a mask.
+ */
+lmh_status lmh_project_logprobs_sample(const void* hidden, int64_t hidden_row_stride, int32_t num_tokens,
+                                       const int32_t* row_idx, int32_t rows, int32_t H, const void* W,
+                                       lmh_w_layout w_layout, int32_t V, const int32_t* sel_ids,
+                                       const int32_t* row_k, int32_t k_max, float* lse, float* sel_logprob,
+                                       int32_t* topk_ids, float* topk_logprobs, float* logits_out,
+                                       void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                       float logit_scale, const lmh_sampling* sampling, cudaStream_t stream);
 
 /*
  * lmh_probe_selective -- does this library's selective head reproduce the

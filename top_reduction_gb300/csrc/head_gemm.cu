@@ -71,6 +71,7 @@ struct HeadArgs {
   uint32_t* dev_status;
   int epi_quarters;  // TMEM lane quarters that ever hold rows: ceil(rows / 32) below 128 rows, else 4
   float logit_scale;  // head transform: every logit is logit_scale * (A . W) (1: none)
+  SampleArgs samp;    // device-side sampling (samp.enabled)
   int final_out;   // one vocabulary split: write the final results (out), not partials
   RowOutputs out;
 };
@@ -273,6 +274,35 @@ struct RegTopK {
 };
 
 // ---------------------------------------------------------------------------
+// Gumbel-max sampling noise
+// ---------------------------------------------------------------------------
+// Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3", SC 2011): per round two 32x32->64 products
+// of counter words with the round multipliers; the high halves are XORed
+// with the other counter words and the key; the key grows by the Weyl
+// increments.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+    k.x += 0x9E3779B9u;
+    k.y += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// Gumbel noise -log(-log u) of one Philox word, u = ((w >> 9) + 0.5) * 2^-23
+// (exact in fp32, strictly inside (0, 1)).  u <= 1 - 2^-24 bounds the noise:
+// g <= -log(-log(1 - 2^-24)) < kGumbelMax.
+constexpr float kGumbelMax = 16.65f;
+__device__ __forceinline__ float gumbel_of(uint32_t w) {
+  const float u = (static_cast<float>(w >> 9) + 0.5f) * 1.1920928955078125e-7f;
+  return -__logf(-__logf(u));
+}
+
+// ---------------------------------------------------------------------------
 // the fused kernel
 // ---------------------------------------------------------------------------
 template <int KCAP, bool kMaterialize>
@@ -445,6 +475,19 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
       }
       float m = -INFINITY, ssum = 0.0f, sel_val = 0.0f;
       bool has_sel = false;
+      // sampling: the row's best score z/T + g (greedy: z) over the allowed tokens so far
+      float s_best = -INFINITY, s_z = -INFINITY, s_inv_t = 0.0f;
+      int32_t s_id = -1;
+      bool s_greedy = true;
+      uint32_t s_off_lo = 0, s_off_hi = 0;
+      if (valid && a.samp.enabled) {
+        const float T = a.samp.temperature ? a.samp.temperature[row] : 1.0f;
+        s_greedy = !(T > 0.0f);
+        s_inv_t = s_greedy ? 0.0f : 1.0f / T;
+        const uint64_t off = a.samp.offsets ? static_cast<uint64_t>(a.samp.offsets[row]) : static_cast<uint64_t>(row);
+        s_off_lo = static_cast<uint32_t>(off);
+        s_off_hi = static_cast<uint32_t>(off >> 32);
+      }
       HeapState st;  // shared-memory heap (KCAP 128)
       st.tau = -INFINITY;
       st.cnt = 0;
@@ -513,6 +556,45 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
               sel_val = sv;
               has_sel = true;
             }
+            if (a.samp.enabled) {
+              // Gumbel-max over the block's allowed tokens; ids ascend, so ">" keeps the smaller id
+              uint64_t allow = ~0ull;
+              if (a.samp.mask) {
+                const uint32_t* mrow = a.samp.mask + static_cast<int64_t>(row) * a.samp.mask_words;
+                const int wd = col0 >> 5;
+                allow = mrow[wd];
+                if (wd + 1 < a.samp.mask_words) allow |= static_cast<uint64_t>(mrow[wd + 1]) << 32;
+              }
+              if (s_greedy) {
+                if (bm > s_best) {
+#pragma unroll
+                  for (int j = 0; j < kBlock; ++j)
+                    if (((allow >> j) & 1ull) && v[j] > s_best) {
+                      s_best = v[j];
+                      s_z = v[j];
+                      s_id = col0 + j;
+                    }
+                }
+              } else if (fmaf(bm, s_inv_t, kGumbelMax) > s_best) {  // else no token of the block can win
+                const uint2 key = make_uint2(static_cast<uint32_t>(a.samp.seed), static_cast<uint32_t>(a.samp.seed >> 32));
+#pragma unroll
+                for (int q = 0; q < kBlock / 4; ++q) {
+                  const uint4 w = philox4x32_10(
+                      make_uint4(static_cast<uint32_t>(col0 >> 2) + q, s_off_lo, s_off_hi, 0x53414D50u), key);
+                  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const int j = 4 * q + e;
+                    const float sc = fmaf(v[j], s_inv_t, gumbel_of(ws[e]));
+                    if (((allow >> j) & 1ull) && sc > s_best) {
+                      s_best = sc;
+                      s_z = v[j];
+                      s_id = col0 + j;
+                    }
+                  }
+                }
+              }
+            }
             if constexpr (Cfg::kRegList) {
               // Stage the block for the lanes that have candidates; each lane then walks only its
               // own candidate mask, so the warp pays the largest per-lane count, not their union.
@@ -577,6 +659,11 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
           for (int j = 0; j < k_row; ++j) put(j, (j < st.cnt) ? lists[j * kBM + r_local] : 0ull);
         }
         for (int j = k_row; j < a.k_max; ++j) put(j, 0ull);
+        if (a.samp.enabled) {
+          a.samp.ids_out[row] = s_id;
+          if (a.samp.lp_out) a.samp.lp_out[row] = s_id >= 0 ? s_z - lse : __int_as_float(0x7fc00000);
+          if (s_id < 0) set_status(a.dev_status, LMH_DS_NO_ALLOWED_TOKEN);
+        }
       } else if (valid) {
         const int64_t pidx = static_cast<int64_t>(row) * a.splits + split;
         a.parts.part_ms[pidx] = make_float2(m, ssum);
@@ -590,6 +677,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
           for (int j = 0; j < k_row; ++j) out[j] = (j < st.cnt) ? lists[j * kBM + r_local] : 0ull;
         }
         if (has_sel) a.parts.sel_logit[row] = sel_val;
+        if (a.samp.enabled) a.parts.part_samp[pidx] = make_float4(s_best, __int_as_float(s_id), s_z, 0.0f);
       }
     }
   }
@@ -730,7 +818,7 @@ cudaError_t head_setup() {
 cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const void* W, int V, const HeadPlan& plan,
                         const int32_t* sel, const int32_t* row_k, int k_max, Partials parts, float* logits_out,
                         uint32_t* dev_status, cudaStream_t stream, bool pdl, const RowOutputs* final_out,
-                        float logit_scale) {
+                        float logit_scale, const SampleArgs* samp) {
   if (final_out && plan.splits != 1) return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
   // With fewer than 128 rows (one row tile) the A box covers only the real
@@ -760,6 +848,7 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   a.dev_status = dev_status;
   a.epi_quarters = rows < kBM ? (rows + 31) / 32 : 4;
   a.logit_scale = logit_scale;
+  a.samp = samp ? *samp : SampleArgs{};
   a.final_out = final_out ? 1 : 0;
   a.out = final_out ? *final_out : RowOutputs{nullptr, nullptr, nullptr, nullptr};
   const dim3 grid(plan.grid), block(kHeadThreads);

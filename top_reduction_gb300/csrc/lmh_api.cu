@@ -45,7 +45,8 @@ static inline size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t
 
 size_t partials_bytes(int rows, int splits, int k_max) {
   const size_t rs = static_cast<size_t>(rows) * static_cast<size_t>(splits);
-  return align256(rs * 8) + align256(rs * static_cast<size_t>(k_max) * 8) + align256(static_cast<size_t>(rows) * 4);
+  return align256(rs * 8) + align256(rs * static_cast<size_t>(k_max) * 8) + align256(static_cast<size_t>(rows) * 4) +
+         align256(rs * 16);
 }
 
 Partials carve_partials(void* base, int rows, int splits, int k_max) {
@@ -57,6 +58,8 @@ Partials carve_partials(void* base, int rows, int splits, int k_max) {
   out.part_keys = reinterpret_cast<unsigned long long*>(p);
   p += align256(rs * static_cast<size_t>(k_max) * 8);
   out.sel_logit = reinterpret_cast<float*>(p);
+  p += align256(static_cast<size_t>(rows) * 4);
+  out.part_samp = reinterpret_cast<float4*>(p);
   out.bmax = nullptr;
   out.ticket = nullptr;
   return out;
@@ -230,7 +233,8 @@ static lmh_status project_impl(const void* hidden, int64_t hidden_row_stride, in
                                lmh_w_layout w_layout, int32_t V, const int32_t* sel_ids, const int32_t* row_k,
                                int32_t k_req, float* lse, float* sel_logprob, int32_t* topk_ids,
                                float* topk_logprobs, float* logits_out, void* workspace, size_t workspace_bytes,
-                               uint32_t* dev_status, float logit_scale, cudaStream_t stream) {
+                               uint32_t* dev_status, float logit_scale, cudaStream_t stream,
+                               const SampleArgs* samp = nullptr) {
   if (rows < 0 || H <= 0 || V <= 0 || num_tokens < 0) return LMH_ERR_INVALID_ARG;
   if (k_req < LMH_K_FULL || k_req > LMH_K_MAX) return LMH_ERR_UNSUPPORTED;
   if (k_req > V) return LMH_ERR_INVALID_ARG;
@@ -275,12 +279,12 @@ static lmh_status project_impl(const void* hidden, int64_t hidden_row_stride, in
   if (e == cudaSuccess) {
     Traced tr(kTraceHead, stream);
     e = launch_head(A, a_stride, rows, H, W, V, plan, sel_ids, row_k, k_max, parts, z_out, dev_status, stream,
-                    /*pdl=*/gather, one_split ? &outs : nullptr, logit_scale);
+                    /*pdl=*/gather, one_split ? &outs : nullptr, logit_scale, samp);
   }
   if (e == cudaSuccess && !one_split) {
     Traced tr(kTraceMerge, stream);
     e = launch_merge(rows, plan.splits, V, k_max, parts, sel_ids, row_k, lse, sel_logprob, topk_ids, topk_logprobs,
-                     dev_status, stream, /*pdl=*/true);
+                     dev_status, stream, /*pdl=*/true, samp);
   }
   if (e == cudaSuccess && full)
     e = launch_full_logprobs(z_out, LMH_F32, V, rows, V, lse, topk_logprobs, stream);
@@ -340,6 +344,29 @@ lmh_status lmh_logprobs_from_logits(const void* logits, lmh_dtype dtype, int32_t
   const cudaError_t e = launch_logits_reduce(logits, dtype, row_stride, rows, V, vs, sel_ids, row_k, k_max, parts,
                                              lse, sel_logprob, topk_ids, topk_logprobs, dev_status, stream);
   return from_cuda(e);
+}
+
+lmh_status lmh_project_logprobs_sample(const void* hidden, int64_t hidden_row_stride, int32_t num_tokens,
+                                       const int32_t* row_idx, int32_t rows, int32_t H, const void* W,
+                                       lmh_w_layout w_layout, int32_t V, const int32_t* sel_ids,
+                                       const int32_t* row_k, int32_t k_max, float* lse, float* sel_logprob,
+                                       int32_t* topk_ids, float* topk_logprobs, float* logits_out,
+                                       void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                       float logit_scale, const lmh_sampling* sampling, cudaStream_t stream) {
+  if (!sampling || !sampling->sampled_ids || !valid_scale(logit_scale) || V <= 0) return LMH_ERR_INVALID_ARG;
+  if (sampling->allowed_mask && sampling->mask_words < (V + 31) / 32) return LMH_ERR_INVALID_ARG;
+  SampleArgs sa{};
+  sa.enabled = 1;
+  sa.temperature = sampling->temperature;
+  sa.mask = sampling->allowed_mask;
+  sa.mask_words = sampling->mask_words;
+  sa.seed = sampling->seed;
+  sa.offsets = sampling->offsets;
+  sa.ids_out = sampling->sampled_ids;
+  sa.lp_out = sampling->sampled_logprob;
+  return project_impl(hidden, hidden_row_stride, num_tokens, row_idx, rows, H, W, w_layout, V, sel_ids, row_k, k_max,
+                      lse, sel_logprob, topk_ids, topk_logprobs, logits_out, workspace, workspace_bytes, dev_status,
+                      logit_scale, stream, &sa);
 }
 
 lmh_status lmh_probe_selective(const void* hidden, int64_t hidden_row_stride, int32_t num_tokens,

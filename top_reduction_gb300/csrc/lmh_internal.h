@@ -37,7 +37,21 @@ struct Partials {
   unsigned long long* part_keys;
   float* sel_logit;
   unsigned int* ticket;  // standalone reduction: chunk counter of the dynamic schedule (else unused)
+  float4* part_samp;     // head path: per-(row, split) sampling partial (best score, id bits, z, -)
   float* bmax;  // standalone reduction: block maxima [rows * nblk] (else unused)
+};
+
+// Device-side sampling on the head path (lmh_project_logprobs_sample): Gumbel-max
+// over the allowed tokens, Philox4x32-10 noise keyed by (seed, row offset, token).
+struct SampleArgs {
+  int enabled;
+  const float* temperature;  // [rows] or null (1); <= 0: greedy
+  const uint32_t* mask;      // [rows x mask_words] allowed-token bits, or null (all allowed)
+  int mask_words;
+  uint64_t seed;
+  const int64_t* offsets;  // [rows] counter offsets, or null (the row index)
+  int32_t* ids_out;        // [rows]
+  float* lp_out;           // [rows] z[id] - lse, or null
 };
 
 // Final per-row results (the outputs of lmh_project_logprobs / lmh_logprobs_from_logits).
@@ -76,7 +90,8 @@ cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t ro
 // Merges the `splits` partial slots of every row (head path).
 cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts, const int32_t* sel,
                          const int32_t* row_k, float* lse, float* sel_logprob, int32_t* topk_ids,
-                         float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream, bool pdl = false);
+                         float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream, bool pdl = false,
+                         const SampleArgs* samp = nullptr);
 
 // Full-vocabulary output: out[r][v] = fp32(x[r][v]) - lse[r] (x may alias out for f32).
 cudaError_t launch_full_logprobs(const void* x, lmh_dtype dtype, int64_t row_stride, int rows, int V, const float* lse,
@@ -110,7 +125,8 @@ cudaError_t launch_gather_rows(const void* hidden, int64_t hidden_stride, int nu
 cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const void* W, int V,
                         const HeadPlan& plan, const int32_t* sel, const int32_t* row_k, int k_max,
                         Partials parts, float* logits_out, uint32_t* dev_status, cudaStream_t stream,
-                        bool pdl = false, const RowOutputs* final_out = nullptr, float logit_scale = 1.0f);
+                        bool pdl = false, const RowOutputs* final_out = nullptr, float logit_scale = 1.0f,
+                        const SampleArgs* samp = nullptr);
 
 // Launch `kernel` on `stream`; with pdl = true it carries the programmatic
 // stream serialization attribute, so it may start while its predecessor in the

@@ -998,6 +998,7 @@ Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs) {
   p += al(static_cast<size_t>(rows) * vs.nblk * 4);
   out.ticket = reinterpret_cast<unsigned int*>(p);
   out.part_keys = nullptr;
+  out.part_samp = nullptr;
   return out;
 }
 

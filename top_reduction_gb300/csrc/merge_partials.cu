@@ -26,7 +26,38 @@ struct MergeArgs {
   int32_t* topk_ids;
   float* topk_logprobs;
   uint32_t* dev_status;
+  SampleArgs samp;
 };
+
+// Sampling partials (score, id bits, z, -): a beats b when it has a token and a
+// higher score, ties to the smaller id (the order in which one stream meets them).
+__device__ __forceinline__ bool samp_better(const float4& a, const float4& b) {
+  const int ia = __float_as_int(a.y), ib = __float_as_int(b.y);
+  if (ia < 0) return false;
+  if (ib < 0) return true;
+  return a.x > b.x || (a.x == b.x && ia < ib);
+}
+
+__device__ __forceinline__ float4 samp_warp_best(float4 v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float4 w;
+    w.x = __shfl_xor_sync(0xffffffffu, v.x, o);
+    w.y = __shfl_xor_sync(0xffffffffu, v.y, o);
+    w.z = __shfl_xor_sync(0xffffffffu, v.z, o);
+    w.w = 0.0f;
+    if (samp_better(w, v)) v = w;
+  }
+  return v;
+}
+
+// The row's sampled token from its slots' partials; writes id and z - lse.
+__device__ __forceinline__ void samp_write(const MergeArgs& a, int row, float4 best, float lse) {
+  const int id = __float_as_int(best.y);
+  a.samp.ids_out[row] = id;
+  if (a.samp.lp_out) a.samp.lp_out[row] = id >= 0 ? best.z - lse : __int_as_float(0x7fc00000);
+  if (id < 0) set_status(a.dev_status, LMH_DS_NO_ALLOWED_TOKEN);
+}
 
 // One CTA per row:
 //   lse = M + log(sum_j s_j * exp(m_j - M)) over the row's slots j, with
@@ -36,6 +67,28 @@ struct MergeArgs {
 //         row's k best.  A lower bound L of the row's k-th key (the k-th
 //         largest of the slots' leading keys) limits the gather to keys >= L;
 //         they are ordered by rank.
+// The best of a row's slot partials, by the whole CTA (kept out of line so
+// that its registers do not add to the merge's).
+__device__ __noinline__ void cta_sample(const MergeArgs& a, int row, int nslots, float lse) {
+  __shared__ float4 s_samp[kMergeThreads / 32];
+  const int tid = threadIdx.x;
+  const float4* ps = a.parts.part_samp + static_cast<int64_t>(row) * nslots;
+  float4 b = make_float4(-INFINITY, __int_as_float(-1), -INFINITY, 0.0f);
+  for (int j = tid; j < nslots; j += kMergeThreads) {
+    const float4 c = ps[j];
+    if (samp_better(c, b)) b = c;
+  }
+  b = samp_warp_best(b);
+  if ((tid & 31) == 0) s_samp[tid >> 5] = b;
+  __syncthreads();
+  if (tid == 0) {
+    float4 r = s_samp[0];
+    for (int w = 1; w < kMergeThreads / 32; ++w)
+      if (samp_better(s_samp[w], r)) r = s_samp[w];
+    samp_write(a, row, r, lse);
+  }
+}
+
 constexpr int kMergeItemsPerThread = 8;  // a row's keys held in registers per thread (first round)
 
 __global__ void __launch_bounds__(kMergeThreads, 4) merge_partials_kernel(const MergeArgs a) {
@@ -108,6 +161,7 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_partials_kernel(const 
     }
     misc[0] = 0;
   }
+  if (a.samp.enabled) cta_sample(a, row, nslots, lse);  // the sampled token: the best slot partial
   if (a.k_max == 0) return;
   int32_t* out_ids = a.topk_ids + static_cast<int64_t>(row) * a.k_max;
   float* out_lp = a.topk_logprobs + static_cast<int64_t>(row) * a.k_max;
@@ -275,6 +329,16 @@ __global__ void __launch_bounds__(kWarpRowsPerCta * 32) merge_partials_warp_kern
       a.sel_logprob[row] = v;
     }
   }
+  if (a.samp.enabled) {  // the sampled token: the best of the slots' partials
+    const float4* ps = a.parts.part_samp + static_cast<int64_t>(row) * a.splits;
+    float4 b = make_float4(-INFINITY, __int_as_float(-1), -INFINITY, 0.0f);
+    for (int j = lane; j < a.splits; j += 32) {
+      const float4 c = ps[j];
+      if (samp_better(c, b)) b = c;
+    }
+    b = samp_warp_best(b);
+    if (lane == 0) samp_write(a, row, b, lse);
+  }
   if (a.k_max == 0) return;
   int k = a.k_max;
   if (a.row_k) k = min(max(a.row_k[row], 0), a.k_max);
@@ -358,7 +422,8 @@ cudaError_t merge_setup() { return cudaSuccess; }
 
 cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts, const int32_t* sel,
                          const int32_t* row_k, float* lse, float* sel_logprob, int32_t* topk_ids,
-                         float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream, bool pdl) {
+                         float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream, bool pdl,
+                         const SampleArgs* samp) {
   MergeArgs a;
   a.rows = rows;
   a.splits = splits;
@@ -372,6 +437,7 @@ cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts,
   a.topk_ids = topk_ids;
   a.topk_logprobs = topk_logprobs;
   a.dev_status = dev_status;
+  a.samp = samp ? *samp : SampleArgs{};
   if (static_cast<int64_t>(splits) * k_max <= kWarpItems)
     return launch_kernel(merge_partials_warp_kernel, dim3((rows + kWarpRowsPerCta - 1) / kWarpRowsPerCta),
                          dim3(kWarpRowsPerCta * 32), 0, stream, pdl, a);

@@ -26,9 +26,18 @@ DS_SEL_OUT_OF_RANGE = 0x2
 DS_ROWS_OVERFLOW = 0x4
 DS_ROW_IDX_OUT_OF_RANGE = 0x8
 DS_TIMEOUT = 0x10
+DS_NO_ALLOWED_TOKEN = 0x20
+
+
+class Sampling(ctypes.Structure):
+    """struct lmh_sampling (include/lmh.h)."""
+    _fields_ = [("temperature", ctypes.c_void_p), ("allowed_mask", ctypes.c_void_p), ("mask_words", ctypes.c_int32),
+                ("seed", ctypes.c_uint64), ("offsets", ctypes.c_void_p), ("sampled_ids", ctypes.c_void_p),
+                ("sampled_logprob", ctypes.c_void_p)]
 
 EXPORTS = ("lmh_select_rows", "lmh_count_selected_rows", "lmh_workspace_bytes",
-           "lmh_project_logprobs", "lmh_project_logprobs_scaled", "lmh_probe_selective",
+           "lmh_project_logprobs", "lmh_project_logprobs_scaled", "lmh_project_logprobs_sample",
+           "lmh_probe_selective",
            "lmh_logprobs_from_logits", "lmh_status_string",
            "lmh_version", "lmh_trace_enable", "lmh_trace_read", "lmh_trace_reset")
 
@@ -63,6 +72,10 @@ def load():
     lib.lmh_project_logprobs_scaled.argtypes = [P, i64, i32, P, i32, i32, P, ctypes.c_int, i32, P, P, i32,
                                                 P, P, P, P, P, P, u64, P, ctypes.c_float, P]
     lib.lmh_project_logprobs_scaled.restype = ctypes.c_int
+    lib.lmh_project_logprobs_sample.argtypes = [P, i64, i32, P, i32, i32, P, ctypes.c_int, i32, P, P, i32,
+                                                P, P, P, P, P, P, u64, P, ctypes.c_float,
+                                                ctypes.POINTER(Sampling), P]
+    lib.lmh_project_logprobs_sample.restype = ctypes.c_int
     lib.lmh_probe_selective.argtypes = [P, i64, i32, P, i32, i32, P, i32, ctypes.c_float, P, ctypes.c_float, P,
                                         P, u64, P, P]
     lib.lmh_probe_selective.restype = ctypes.c_int
@@ -174,13 +187,17 @@ def _workspace(workspace, nbytes, device):
 
 
 def project_logprobs(hidden, W, row_idx=None, rows=None, sel=None, row_k=None, k_max=0,
-                     logits_out=None, workspace=None, dev_status=None, out=None, stream=None, logit_scale=1.0):
+                     logits_out=None, workspace=None, dev_status=None, out=None, stream=None, logit_scale=1.0,
+                     sampling=None):
     """Selective head projection + per-row lse / selected logprob / top-k.
 
     hidden: bf16 [T, H] (rows may be strided); W: bf16 [V, H] (lm_head.weight);
     row_idx: int32 [rows] device tensor or None (rows 0..rows-1).
     logit_scale: head transform, every logit is logit_scale * (A . W)
     (lmh_project_logprobs_scaled); 1.0 is the plain projection.
+    sampling: dict with optional temperature (fp32 [rows]), mask (int32/uint32 [rows, words]
+    allowed-token bits), seed (int), offsets (int64 [rows]): device-side Gumbel-max sampling
+    (lmh_project_logprobs_sample); adds sampled_ids and sampled_logprob to the result.
     Returns a dict with lse, sel_logprob (or None), topk_ids, topk_logprobs.
     """
     assert hidden.is_cuda and hidden.dtype == torch.bfloat16 and hidden.dim() == 2
@@ -202,7 +219,26 @@ def project_logprobs(hidden, W, row_idx=None, rows=None, sel=None, row_k=None, k
     args = (_p(hidden), hidden.stride(0) if T > 1 else H, T, _p(row_idx), int(rows), H, _p(W), W_VH, V,
             _p(sel_t), _p(rk_t), int(k_max), _p(o["lse"]), _p(o["sel_logprob"]), _p(o["topk_ids"]),
             _p(o["topk_logprobs"]), _p(logits_out), _p(ws), ws.numel() * ws.element_size(), _p(dev_status))
-    if logit_scale == 1.0:
+    if sampling is not None:
+        def dev(t, dtype):
+            return None if t is None else torch.as_tensor(t, dtype=dtype, device=dev_).contiguous()
+        dev_ = hidden.device
+        temp = dev(sampling.get("temperature"), torch.float32)
+        mask = sampling.get("mask")
+        if mask is not None:
+            mask = torch.as_tensor(mask, device=dev_).contiguous()
+            assert mask.dim() == 2 and mask.shape[0] == rows and mask.element_size() == 4
+        offs = dev(sampling.get("offsets"), torch.int64)
+        o["sampled_ids"] = torch.empty(rows, dtype=torch.int32, device=dev_)
+        o["sampled_logprob"] = torch.empty(rows, dtype=torch.float32, device=dev_)
+        def addr(t):
+            return None if t is None else t.data_ptr()
+        sp = Sampling(addr(temp), addr(mask), 0 if mask is None else mask.shape[1],
+                      int(sampling.get("seed", 0)) & (2 ** 64 - 1), addr(offs), addr(o["sampled_ids"]),
+                      addr(o["sampled_logprob"]))
+        _check(load().lmh_project_logprobs_sample(*args, float(logit_scale), ctypes.byref(sp), _stream(stream)),
+               "lmh_project_logprobs_sample")
+    elif logit_scale == 1.0:
         _check(load().lmh_project_logprobs(*args, _stream(stream)), "lmh_project_logprobs")
     else:
         _check(load().lmh_project_logprobs_scaled(*args, float(logit_scale), _stream(stream)),
