@@ -276,3 +276,31 @@ def test_full_vocabulary_output(lmh, rows, H, V):
     assert np.array_equal(full, exact.astype(np.float32))
     o2, _, _ = gpu_project(lmh, b["hidden"].cuda(), b["W"].cuda(), row_idx=ri.cuda(), sel=sel, k=L.K_FULL)
     assert torch.equal(o2["topk_logprobs"], o["topk_logprobs"])   # same without logits_out
+
+
+@pytest.mark.parametrize("rows,H,V,k", [(40, 128, 200, 20), (50, 256, 40000, 16), (32, 64, 70001, 5),
+                                        (33, 192, 3000, 8), (9, 1024, 151936, 20), (2, 64, 513, 1)])
+def test_small_batch_column_split(lmh, rows, H, V, k):
+    """Batches of at most 64 rows split each tile's columns over the epilogue
+    warps (4 copies of 32 rows, or 2 of 64) and fold the copies' lse, top-k,
+    selected logit and draw together per row: per-row K, selected ids in every
+    block position, a one-split plan (V 200) and equal logits across copies
+    (duplicated W rows) must all match the oracle."""
+    g = torch.Generator().manual_seed(rows * 131 + V)
+    T = rows + 3
+    W = torch.randn(V, H, generator=g) / H ** 0.5
+    dup = torch.randint(0, V, (V // 50 + 1,), generator=g)
+    W[torch.randint(0, V, (dup.numel(),), generator=g)] = W[dup]  # equal logits at ids in different blocks
+    b = {"hidden": torch.randn(T, H, generator=g).to(torch.bfloat16), "W": W.to(torch.bfloat16)}
+    ri = torch.randperm(T, generator=g)[:rows].to(torch.int32)
+    sel = torch.randint(-1, V, (rows,), generator=g, dtype=torch.int32)
+    row_k = torch.randint(0, k + 1, (rows,), generator=g, dtype=torch.int32)
+    o, st, logits = gpu_project(lmh, b["hidden"].cuda(), b["W"].cuda(), row_idx=ri.cuda(), sel=sel, row_k=row_k,
+                                k=k, materialize=True)
+    assert st == 0
+    z, orc, A = oracle_rows(b, ri.numpy(), sel.numpy(), k, row_k=row_k.numpy())
+    assert_close(logits.cpu().numpy(), z, TOL_FUSED, "column split logits")
+    check_fused(o, orc, z, A, b["W"], k, row_k=row_k.numpy(), what="column split %s" % ((rows, H, V, k),))
+    r = lmh.logprobs_from_logits(logits, sel=sel, row_k=row_k.cuda(), k_max=k)
+    torch.cuda.synchronize()
+    assert torch.equal(o["topk_ids"], r["topk_ids"])  # the same fp32 logits give the same ranking

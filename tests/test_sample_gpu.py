@@ -74,7 +74,8 @@ def check_draws(ids_g, lp_g, z, lse, temp, mask, seed, offsets, A, W, what):
     return certified
 
 
-@pytest.mark.parametrize("rows,H,V,k", [(200, 136, 4100, 5), (129, 64, 1000, 0), (17, 64, 2000, 20)])
+@pytest.mark.parametrize("rows,H,V,k", [(200, 136, 4100, 5), (129, 64, 1000, 0), (17, 64, 2000, 20),
+                                        (50, 96, 30000, 8)])
 def test_sampling_with_mask_and_temperatures(lmh, rows, H, V, k):
     hidden, W, ri, g = _case(rows, H, V, rows * 3 + V, w_scale=3.0)
     rng = np.random.default_rng(rows + V)

@@ -57,7 +57,11 @@ struct HeadCfg {
   static constexpr size_t kListBytes = kRegList ? static_cast<size_t>(4) * 64 * 32 * 4
                                                 : static_cast<size_t>(kBM) * KCAP * 8;
   static constexpr size_t kSmem = 1024 /*alignment slack*/ + kStages * (kStageBytesA + kStageBytesB) +
-                                  kListBytes + (2 * kStages + 4) * 8 + 16;
+                                  kListBytes + (2 * kStages + 6) * 8 + 16;
+  // Small batches may split each tile's columns over the epilogue warps (see
+  // HeadArgs::rep); a warp then hands its row state to the leader through its
+  // own staging region: 7 words plus (value, id) per list entry, per lane.
+  static constexpr bool kRepOk = kRegList && 7 + 2 * KCAP <= 64;
 };
 
 struct HeadArgs {
@@ -70,6 +74,11 @@ struct HeadArgs {
   float* logits_out;
   uint32_t* dev_status;
   int epi_quarters;  // TMEM lane quarters that ever hold rows: ceil(rows / 32) below 128 rows, else 4
+  // Column split for batches of at most 64 rows: the A stage holds `rep`
+  // copies of the rows, each spanning rep_nq lane quarters, so every lane
+  // quarter has the rows and epilogue warp q (copy q / rep_nq) reduces only
+  // the 64-column blocks c == copy (mod rep) of each tile.  rep 1: off.
+  int rep, rep_nq;
   float logit_scale;  // head transform: every logit is logit_scale * (A . W) (1: none)
   SampleArgs samp;    // device-side sampling (samp.enabled)
   int final_out;   // one vocabulary split: write the final results (out), not partials
@@ -321,7 +330,9 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;
   uint64_t* acc_empty = acc_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* xchg_full = acc_empty + 2;    // column split: the copies' row states are staged
+  uint64_t* xchg_empty = xchg_full + 1;   // column split: the leader has read them
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xchg_empty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -336,6 +347,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], a.epi_quarters * 32);  // the epilogue warps that read accumulators
     }
+    mbar_init(xchg_full, a.rep > 1 ? (4 - a.rep_nq) * 32 : 1);
+    mbar_init(xchg_empty, a.rep > 1 ? a.rep_nq * 32 : 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -397,16 +410,25 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
           np = j + 1;
         }
       }
+      // the stage's A slice: one box, or with the column split one box per row copy
+      auto load_a = [&](int s, int kb_, int m_tile_) {
+        if (a.rep > 1) {
+          for (int p = 0; p < a.rep; ++p)
+            tma_load_2d(sA + s * kStageBytesA + p * a.rep_nq * 32 * 128, &tmap_a, kb_ * kBK, 0, &full[s]);
+        } else {
+          tma_load_2d(sA + s * kStageBytesA, &tmap_a, kb_ * kBK, m_tile_ * kBM, &full[s]);
+        }
+      };
       pdl_wait();  // the gathered rows are written by the preceding kernel
 #pragma unroll
       for (int j = 0; j < S; ++j)
-        if (j < np) tma_load_2d(sA + j * kStageBytesA, &tmap_a, pk[j] * kBK, pm[j] * kBM, &full[j]);
+        if (j < np) load_a(j, pk[j], pm[j]);
       for (uint32_t it = np; valid; ++it) {
         const int s = it % S;
         const uint32_t ph = (it / S) & 1u;
         if (!wait_or_abort(&empty[s], ph ^ 1u, abort_flag, a.dev_status)) break;
         mbar_arrive_expect_tx(&full[s], a.a_bytes + kStageBytesB);
-        tma_load_2d(sA + s * kStageBytesA, &tmap_a, kb * kBK, m_tile * kBM, &full[s]);
+        load_a(s, kb, m_tile);
         tma_load_2d(sB + s * kStageBytesB, &tmap_b, kb * kBK, n * kBN, &full[s]);
         advance();
       }
@@ -452,10 +474,13 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
     }
   } else {
     // ------------------------- epilogue -------------------------
-    const int q = warp & 3;             // TMEM lane quarter of this warp
-    const int r_local = q * 32 + lane;  // row within the tile
+    const int q = warp & 3;  // TMEM lane quarter of this warp
+    // column split (small batches): this warp's row copy and its first 64-column block
+    const int n_rep = Cfg::kRepOk ? a.rep : 1;
+    const int copy = n_rep > 1 ? q / a.rep_nq : 0;
+    const int r_local = (n_rep > 1 ? q % a.rep_nq : q) * 32 + lane;  // row within the tile
     const float L = kLog2e;
-    uint32_t t = 0;
+    uint32_t t = 0, xu = 0;
     // With fewer than 128 rows (one row tile) the quarters beyond the last
     // row have nothing to read: their warps go straight to the final barrier
     // instead of polling the accumulator barriers (they are not counted there).
@@ -466,7 +491,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
       const int n_end = min(n_begin + a.tiles_per_split, a.n_tiles);
       const int row = m_tile * kBM + r_local;
       const bool valid = row < a.rows;
-      const bool warp_active = (m_tile * kBM + q * 32) < a.rows;
+      const bool warp_active = (m_tile * kBM + (r_local & ~31)) < a.rows;
       int k_row = 0, sel_id = -1;
       if (valid) {
         k_row = a.k_max;
@@ -502,7 +527,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         tc_fence_after();
         if (warp_active) {
 #pragma unroll 1
-          for (int c = 0; c < kBN / kBlock; ++c) {
+          for (int c = copy; c < kBN / kBlock; c += n_rep) {
             const int col0 = n * kBN + c * kBlock;
             if (col0 >= a.V) break;  // uniform across the warp
             float v[kBlock];
@@ -632,6 +657,88 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         mbar_arrive(&acc_empty[b]);
       }
       if (!live) break;
+      // Column split: every copy's warp stages its row state and its sorted list (keys,
+      // lane-interleaved) in its own staging region, now idle; the copy-0 warp of each lane
+      // quarter folds the states into its own and merges the lists while writing them out.
+      constexpr int KC = Cfg::kRegList ? KCAP : 1;
+      const bool split_cols = Cfg::kRepOk && n_rep > 1;
+      if (split_cols) {
+        float* xs = reinterpret_cast<float*>(lists) + q * (kBlock * 32) + lane;
+        uint64_t* xk = reinterpret_cast<uint64_t*>(lists) + q * (kBlock * 16) + 4 * 32 + lane;
+#pragma unroll
+        for (int j = 0; j < KC; ++j) xk[j * 32] = rt.key(j);
+        if (copy > 0) {
+          xs[0] = m;
+          xs[32] = ssum;
+          xs[64] = sel_val;
+          xs[96] = has_sel ? 1.0f : 0.0f;
+          xs[128] = s_best;
+          xs[160] = __int_as_float(s_id);
+          xs[192] = s_z;
+          mbar_arrive(xchg_full);
+          // the staging region is reused only after the leader has read it
+          if (!wait_or_abort(xchg_empty, xu & 1u, abort_flag, a.dev_status)) break;
+          ++xu;
+          continue;
+        }
+        if (!wait_or_abort(xchg_full, xu & 1u, abort_flag, a.dev_status)) break;
+        for (int p = 1; p < n_rep; ++p) {
+          const float* ys = reinterpret_cast<const float*>(lists) + (q + p * a.rep_nq) * (kBlock * 32) + lane;
+          const float mp = ys[0], sp = ys[32];
+          if (mp > m) {
+            ssum = ssum * ex2_approx((m - mp) * L) + sp;
+            m = mp;
+          } else if (mp != -INFINITY) {
+            ssum += sp * ex2_approx((mp - m) * L);
+          }
+          if (ys[96] != 0.0f) {
+            sel_val = ys[64];
+            has_sel = true;
+          }
+          const float sb = ys[128];
+          const int32_t sid = __float_as_int(ys[160]);
+          if (sid >= 0 && (sb > s_best || (sb == s_best && (s_id < 0 || sid < s_id)))) {
+            s_best = sb;
+            s_id = sid;
+            s_z = ys[192];
+          }
+        }
+      }
+      // f(j, key) for the row's best k_row keys, best first (key 0: fewer candidates)
+      auto emit_keys = [&](auto&& f) {
+        if constexpr (Cfg::kRegList) {
+          if (split_cols) {
+            // merge of the copies' sorted lists; keys are unique, so the best head is the one popped
+            const uint64_t* xk = reinterpret_cast<const uint64_t*>(lists) + 4 * 32 + lane;
+            const int w1 = (q + a.rep_nq) * (kBlock * 16), w2 = (q + 2 * a.rep_nq) * (kBlock * 16),
+                      w3 = (q + 3 * a.rep_nq) * (kBlock * 16), w0 = q * (kBlock * 16);
+            const bool four = n_rep > 2;
+            int h0 = 0, h1 = 0, h2 = 0, h3 = 0;
+            uint64_t k0 = xk[w0], k1 = xk[w1], k2 = four ? xk[w2] : 0ull, k3 = four ? xk[w3] : 0ull;
+            for (int j = 0; j < k_row; ++j) {
+              const uint64_t best = max(max(k0, k1), max(k2, k3));
+              f(j, best);
+              if (best == 0ull) continue;
+              if (best == k0) {
+                k0 = (++h0 < KC) ? xk[w0 + h0 * 32] : 0ull;
+              } else if (best == k1) {
+                k1 = (++h1 < KC) ? xk[w1 + h1 * 32] : 0ull;
+              } else if (best == k2) {
+                k2 = (++h2 < KC) ? xk[w2 + h2 * 32] : 0ull;
+              } else {
+                k3 = (++h3 < KC) ? xk[w3 + h3 * 32] : 0ull;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < KC; ++j)
+              if (j < k_row) f(j, rt.key(j));
+          }
+        } else {
+          heap_sort_desc(lists, r_local, st.cnt);
+          for (int j = 0; j < k_row; ++j) f(j, (j < st.cnt) ? lists[j * kBM + r_local] : 0ull);
+        }
+      };
       if (valid && a.final_out) {
         // the whole row went through this thread: lse = m + log(sum), logprob = logit - lse
         const float lse = (m == -INFINITY) ? -INFINITY : m + logf(ssum);
@@ -650,14 +757,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
           ids[j] = key ? key_id(key) : -1;
           lps[j] = key ? key_value(key) - lse : -INFINITY;
         };
-        if constexpr (Cfg::kRegList) {
-#pragma unroll
-          for (int j = 0; j < (Cfg::kRegList ? KCAP : 1); ++j)
-            if (j < k_row) put(j, rt.key(j));
-        } else {
-          heap_sort_desc(lists, r_local, st.cnt);
-          for (int j = 0; j < k_row; ++j) put(j, (j < st.cnt) ? lists[j * kBM + r_local] : 0ull);
-        }
+        emit_keys(put);
         for (int j = k_row; j < a.k_max; ++j) put(j, 0ull);
         if (a.samp.enabled) {
           a.samp.ids_out[row] = s_id;
@@ -668,16 +768,13 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         const int64_t pidx = static_cast<int64_t>(row) * a.splits + split;
         a.parts.part_ms[pidx] = make_float2(m, ssum);
         unsigned long long* out = a.parts.part_keys + pidx * a.k_max;
-        if constexpr (Cfg::kRegList) {
-#pragma unroll
-          for (int j = 0; j < (Cfg::kRegList ? KCAP : 1); ++j)
-            if (j < k_row) out[j] = rt.key(j);
-        } else {
-          heap_sort_desc(lists, r_local, st.cnt);
-          for (int j = 0; j < k_row; ++j) out[j] = (j < st.cnt) ? lists[j * kBM + r_local] : 0ull;
-        }
+        emit_keys([&](int j, uint64_t key) { out[j] = key; });
         if (has_sel) a.parts.sel_logit[row] = sel_val;
         if (a.samp.enabled) a.parts.part_samp[pidx] = make_float4(s_best, __int_as_float(s_id), s_z, 0.0f);
+      }
+      if (split_cols) {  // the copies' staging regions are free again
+        mbar_arrive(xchg_empty);
+        ++xu;
       }
     }
   }
@@ -831,7 +928,17 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   e = make_tmap(&tb, W, static_cast<uint64_t>(H), static_cast<uint64_t>(V), static_cast<uint64_t>(H), kBK, kBN);
   if (e != cudaSuccess) return e;
   HeadArgs a;
-  a.a_bytes = a_box * kBK * 2;
+  // Column split for batches of at most 64 rows (and lists that fit the
+  // exchange): 4 row copies of one lane quarter, or 2 of two.
+  a.rep = 1;
+  a.rep_nq = 4;
+  static_assert(HeadCfg<20>::kRepOk && !HeadCfg<32>::kRepOk, "column split: list capacities up to 20");
+  const bool rep_ok = plan.kcap <= 20;
+  if (rows >= 1 && rows <= 64 && rep_ok) {
+    a.rep_nq = (rows + 31) / 32;
+    a.rep = 4 / a.rep_nq;
+  }
+  a.a_bytes = static_cast<uint32_t>(a.rep) * a_box * kBK * 2;
   a.rows = rows;
   a.H = H;
   a.V = V;
@@ -846,7 +953,7 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   a.parts = parts;
   a.logits_out = logits_out;
   a.dev_status = dev_status;
-  a.epi_quarters = rows < kBM ? (rows + 31) / 32 : 4;
+  a.epi_quarters = a.rep > 1 ? 4 : (rows < kBM ? (rows + 31) / 32 : 4);
   a.logit_scale = logit_scale;
   a.samp = samp ? *samp : SampleArgs{};
   a.final_out = final_out ? 1 : 0;
