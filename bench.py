@@ -383,9 +383,9 @@ def load_peaks():
 
 
 def kernel_source_hash(kernel):
-    src = {"head_logprobs": "head_gemm.cu", "logits_reduce": "logits_reduce.cu"}[kernel]
+    src = {"head_logprobs": ("head_kernel.cuh", "head_gemm.cu"), "logits_reduce": ("logits_reduce.cu",)}[kernel]
     h = hashlib.sha256()
-    for name in (src, "device_common.cuh"):
+    for name in src + ("device_common.cuh",):
         with open(os.path.join(ROOT, "top_reduction_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -144,3 +144,73 @@ def test_sampling_one_split_plan(lmh):
     assert_close(o["lse"].cpu().numpy()[sample], orc["lse"], TOL_FUSED, "one split lse")
     check_draws(o["sampled_ids"].cpu().numpy()[sample], o["sampled_logprob"].cpu().numpy()[sample], z, orc["lse"],
                 temp[sample], None, 99, offsets[sample], A, W, "one split")
+
+
+@pytest.mark.parametrize("rows,H,V,k,w_scale", [(9, 256, 50000, 5, 3.0), (4096, 64, 32768, 0, 1.0),
+                                                (4096, 64, 32768, 3, 6.0)])
+def test_sampling_candidate_filter(lmh, rows, H, V, k, w_scale):
+    """Plans where the head scores only candidate tokens (a raw-word test against the
+    row's best score so far): at most 16 rows per warp, or 128 blocks per row and
+    vocabulary range.  Draws vs the oracle on every row (small batch) or a sample."""
+    hidden, W, ri, g = _case(rows, H, V, rows + V + 1, w_scale=w_scale)
+    rng = np.random.default_rng(rows + H)
+    temp = rng.choice(np.array([0.0, 0.5, 1.0, 2.0], dtype=np.float32), size=rows)
+    mask = _mask(rows, V, rng, p_allow=0.6) if rows < 64 else None
+    offsets = rng.integers(0, 2 ** 62, size=rows, dtype=np.int64)
+    seed = 0xC0FFEE
+    o = lmh.project_logprobs(hidden.cuda(), W.cuda(), row_idx=ri.cuda(), k_max=k,
+                             sampling={"temperature": temp, "seed": seed, "offsets": offsets,
+                                       "mask": None if mask is None else mask.view(np.int32)})
+    torch.cuda.synchronize()
+    sample = np.arange(rows) if rows < 64 else np.unique(np.concatenate([[0, rows - 1], rng.choice(rows, 160, replace=False)]))
+    z = oracle.project(_bits(hidden), _bits(W), row_idx=ri.numpy()[sample])
+    orc = oracle.logprobs(z, k_max=k)
+    A = hidden[ri.long()[torch.as_tensor(sample)]].float().double().numpy()
+    assert_close(o["lse"].cpu().numpy()[sample], orc["lse"], TOL_FUSED, "filter lse")
+    check_draws(o["sampled_ids"].cpu().numpy()[sample], o["sampled_logprob"].cpu().numpy()[sample], z, orc["lse"],
+                temp[sample], None if mask is None else mask[sample], seed, offsets[sample], A, W, "filter")
+
+
+@pytest.mark.parametrize("rows", [64, 16])
+def test_sampling_noise_tail_accuracy(lmh, rows):
+    """Draws decided by the largest noises: per row two allowed tokens whose words are
+    the row's two largest of 65536 (noise near 11, u within about 1e-4 of 1), with
+    logits and temperature set so that their scores differ by 1e-3 -- above the
+    certified near-tie band, so the GPU must pick the oracle's token.  A noise whose
+    logarithm of u loses relative accuracy near u = 1 misses by more than that.  64 rows
+    score every token; 16 rows take the candidate filter."""
+    H, V = 64, 65536
+    seed = 0x5EED_0001
+    cand = np.arange(2 * rows, dtype=np.int64) * 1000003 + 17
+    z0 = np.zeros((cand.size, V))
+    ones = np.ones(cand.size, dtype=np.float32)
+    a, g_a, _ = oracle.sample(z0, temperature=ones, seed=seed, offsets=cand)
+    words = V // 32
+    no_a = np.full((cand.size, words), 0xFFFFFFFF, dtype=np.uint32)
+    no_a[np.arange(cand.size), a // 32] &= ~(np.uint32(1) << (a % 32).astype(np.uint32))
+    b, g_b, _ = oracle.sample(z0, temperature=ones, seed=seed, offsets=cand, mask=no_a)
+    keep = np.nonzero(g_a - g_b > 0.01)[0][:rows]  # offsets whose two largest words differ
+    assert keep.size == rows
+    offsets, a, b, g_a, g_b = cand[keep], a[keep], b[keep], g_a[keep], g_b[keep]
+    assert np.all(g_a > 9.0) and np.all(g_b > 8.0)
+    delta = np.where(np.arange(rows) % 2 == 0, 1e-3, -1e-3)  # b wins on even rows, a on odd rows
+    temp = (1.0 / (g_a - g_b + delta)).astype(np.float32)
+    gap = 1.0 / temp.astype(np.float64) + g_b - g_a  # score(b) - score(a) with the stored temperature
+    assert np.all(np.abs(np.abs(gap) - 1e-3) < 1e-5)
+    hidden = torch.zeros(rows, H)
+    hidden[torch.arange(rows), torch.arange(rows) % H] = 1.0
+    W = torch.zeros(V, H)
+    W[torch.as_tensor(b), torch.arange(rows) % H] = 1.0  # z[i, b_i] = 1, every other logit 0
+    hidden, W = hidden.to(torch.bfloat16), W.to(torch.bfloat16)
+    mask = np.zeros((rows, words), dtype=np.uint32)
+    for i in range(rows):
+        for t in (a[i], b[i]):
+            mask[i, t // 32] |= np.uint32(1) << np.uint32(t % 32)
+    o = lmh.project_logprobs(hidden.cuda(), W.cuda(), k_max=0,
+                             sampling={"temperature": temp, "mask": mask.view(np.int32), "seed": seed,
+                                       "offsets": offsets})
+    torch.cuda.synchronize()
+    z = oracle.project(_bits(hidden), _bits(W))
+    ids_o, _, _ = oracle.sample(z, temperature=temp, mask=mask, seed=seed, offsets=offsets)
+    assert np.array_equal(ids_o, np.where(gap > 0, b, a))
+    assert np.array_equal(o["sampled_ids"].cpu().numpy(), ids_o)
