@@ -200,6 +200,25 @@ def rejected(clocks):
 # our arm
 # ---------------------------------------------------------------------------
 
+def packed(tensors, device, pinned=False):
+    """One byte buffer holding a copy of each named tensor at 256-byte aligned offsets.
+
+    Returns (buffer, {name: view}); with one buffer a step moves its inputs (or its
+    results) in a single copy, as a serving loop packs them.
+    """
+    import torch
+    layout, off = {}, 0
+    for name, t in tensors.items():
+        nbytes = t.numel() * t.element_size()
+        layout[name] = (off, nbytes, t.shape, t.dtype)
+        off = (off + nbytes + 255) // 256 * 256
+    buf = torch.empty(max(off, 256), dtype=torch.uint8, device=device)
+    if pinned:
+        buf = buf.pin_memory()
+    views = {name: buf[o:o + nb].view(dt).view(shape) for name, (o, nb, shape, dt) in layout.items()}
+    return buf, views
+
+
 def step_outputs(rows, k, V, with_sel, device):
     """Preallocated outputs of one call (K -1: [rows, V] logprobs, no ids)."""
     import torch
@@ -306,17 +325,21 @@ def e2e_leg(lmh, b, device, steps):
     Every step copies its inputs host->device (hidden rows, cu_seqlens,
     selected ids; the head weight stays resident like model weights), runs
     the path, copies the compact result device->host and reads it on the
-    host.  Two buffer sets alternate, as in a serving loop: step i+1 is
-    issued before the host waits for step i's result, so the host's own work
-    overlaps the GPU's.
+    host.  Two buffer sets alternate, as in a serving loop, each on its own
+    stream: step i+1 is issued before the host waits for step i's result, so
+    the host's work and step i+1's input copy overlap step i on the GPU.  As
+    a serving loop would, each buffer set's step (the copy in, the API calls
+    and the copy out) is captured once in a CUDA graph and replayed every
+    step; if capture fails the calls run eagerly.
     """
     import torch
     chunk = b["name"] == "logits_chunk"
-    if chunk:
-        h_in = {"logits": b["logits"].pin_memory(), "sel": b["sel"].pin_memory()}
-    else:
-        h_in = {"hidden": b["hidden"].pin_memory(), "cu": b["cu_seqlens"].pin_memory(),
-                "sel": b["sel"].pin_memory()}
+    src = {"logits": b["logits"], "sel": b["sel"]} if chunk else \
+        {"hidden": b["hidden"], "cu": b["cu_seqlens"], "sel": b["sel"]}
+    h_in_buf, h_in = packed(src, "cpu", pinned=True)  # the step's inputs, packed in pinned host memory
+    for key, v in src.items():
+        h_in[key].copy_(v)
+    if not chunk:
         W = b["W"].to(device)
         mask = None if b["all_rows_mask"] is None else b["all_rows_mask"].to(device)
         row_k = None if b["row_k"] is None else b["row_k"].to(device)
@@ -328,20 +351,21 @@ def e2e_leg(lmh, b, device, steps):
         ws_bytes = lmh.workspace_bytes(rows, int(b["H"]), int(b["V"]), k, lmh.PATH_PROJECT)
 
     def buffers():
-        d_in = {key: torch.empty_like(v, device=device) for key, v in h_in.items()}
-        out = step_outputs(rows, k, int(b["V"]), True, device)
-        h_out = {key: torch.empty(v.shape, dtype=v.dtype).pin_memory() for key, v in out.items() if v is not None}
+        d_in_buf, d_in = packed(h_in, device)
+        shapes = {key: v for key, v in step_outputs(rows, k, int(b["V"]), True, "meta").items() if v is not None}
+        d_out_buf, out = packed(shapes, device)
+        h_out_buf, h_out = packed(shapes, "cpu", pinned=True)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
-        return {"d_in": d_in, "out": out, "h_out": h_out, "ws": ws, "ev": torch.cuda.Event()}
+        return {"d_in_buf": d_in_buf, "d_in": d_in, "d_out_buf": d_out_buf, "out": out, "h_out_buf": h_out_buf,
+                "h_out": h_out, "ws": ws, "ev": torch.cuda.Event(), "stream": torch.cuda.Stream()}
 
     bufs = [buffers(), buffers()]
     h2d = sum(v.numel() * v.element_size() for v in h_in.values())
     d2h = sum(v.numel() * v.element_size() for v in bufs[0]["h_out"].values())
 
-    def issue(bf):
+    def step_ops(bf):
         d_in = bf["d_in"]
-        for key, v in h_in.items():
-            d_in[key].copy_(v, non_blocking=True)
+        bf["d_in_buf"].copy_(h_in_buf, non_blocking=True)  # one copy in
         if chunk:
             o = lmh.logprobs_from_logits(d_in["logits"], sel=d_in["sel"], k_max=k, workspace=bf["ws"],
                                          out=bf["out"])
@@ -349,17 +373,40 @@ def e2e_leg(lmh, b, device, steps):
             ri, _ = lmh.select_rows(d_in["cu"], b["num_decode"], mask, max_out_rows=rows)
             o = lmh.project_logprobs(d_in["hidden"], W, row_idx=ri, sel=d_in["sel"], row_k=row_k, k_max=k,
                                      workspace=bf["ws"], out=bf["out"], logit_scale=b.get("logit_scale", 1.0))
-        for key, v in bf["h_out"].items():
-            v.copy_(o[key], non_blocking=True)
-        bf["ev"].record()
+        assert all(o[key].data_ptr() == bf["out"][key].data_ptr() for key in bf["out"])
+        bf["h_out_buf"].copy_(bf["d_out_buf"], non_blocking=True)  # one copy out
+
+    def issue(bf):
+        with torch.cuda.stream(bf["stream"]):
+            if "graph" in bf:
+                bf["graph"].replay()
+            else:
+                step_ops(bf)
+            bf["ev"].record()
 
     def read(bf):  # the host waits for, and touches, the step's result
         bf["ev"].synchronize()
         return float(bf["h_out"]["lse"][0])
 
+    torch.cuda.synchronize()  # the weights and inputs above were placed on the default stream
     for s in range(5):
         issue(bufs[s % 2])
         read(bufs[s % 2])
+    mode = "CUDA graph per buffer set, one stream per buffer set"
+    try:
+        for bf in bufs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step_ops(bf)
+            bf["graph"] = g
+        for s in range(4):
+            issue(bufs[s % 2])
+            read(bufs[s % 2])
+    except Exception as e:  # capture is an optimisation of the loop, not a requirement
+        for bf in bufs:
+            bf.pop("graph", None)
+        mode = "eager, one stream per buffer set (graph capture failed: %s)" % str(e).splitlines()[0][:80]
+        torch.cuda.synchronize()
     t0 = time.perf_counter()
     for s in range(steps):
         issue(bufs[s % 2])
@@ -369,7 +416,7 @@ def e2e_leg(lmh, b, device, steps):
     dt = time.perf_counter() - t0
     return {"value": rows * steps / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": 1e3 * dt / steps,
-            "pipelining": "two buffer sets: step i+1 is issued before step i's result is read"}
+            "pipelining": "two buffer sets: step i+1 is issued before step i's result is read; " + mode}
 
 
 def load_peaks():

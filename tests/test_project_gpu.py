@@ -304,3 +304,36 @@ def test_small_batch_column_split(lmh, rows, H, V, k):
     r = lmh.logprobs_from_logits(logits, sel=sel, row_k=row_k.cuda(), k_max=k)
     torch.cuda.synchronize()
     assert torch.equal(o["topk_ids"], r["topk_ids"])  # the same fp32 logits give the same ranking
+
+
+def test_cuda_graph_capture_and_replay(lmh, tiny):
+    """The whole step (row selection, gather, head, merge) can be captured in a CUDA
+    graph: replays read the inputs' current contents and equal the eager call."""
+    b = tiny
+    hidden_d, W_d = b["hidden"].cuda(), b["W"].cuda()
+    cu = b["cu_seqlens"].cuda()
+    n = int(b["n_sel"])
+    sel = b["sel"].cuda()
+    ws = torch.empty(lmh.workspace_bytes(n, hidden_d.shape[1], W_d.shape[0], 5, lmh.PATH_PROJECT), dtype=torch.uint8,
+                     device="cuda")
+
+    def step():
+        ri, _ = lmh.select_rows(cu, b["num_decode"], None, max_out_rows=n)
+        return lmh.project_logprobs(hidden_d, W_d, row_idx=ri, sel=sel, k_max=5, workspace=ws)
+
+    eager = step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cap = step()
+    g.replay()
+    torch.cuda.synchronize()
+    for key in ("lse", "sel_logprob", "topk_ids", "topk_logprobs"):
+        assert torch.equal(cap[key], eager[key]), key
+    hidden_d.mul_(-1.0)  # new inputs in the same buffers: the replay sees them
+    g.replay()
+    again = step()
+    torch.cuda.synchronize()
+    for key in ("lse", "topk_ids", "topk_logprobs"):
+        assert torch.equal(cap[key], again[key]), key
+    assert not torch.equal(cap["topk_ids"], eager["topk_ids"])
