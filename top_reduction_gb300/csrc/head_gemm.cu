@@ -142,16 +142,21 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   e = make_tmap(&tb, W, static_cast<uint64_t>(H), static_cast<uint64_t>(V), static_cast<uint64_t>(H), kBK, kBN);
   if (e != cudaSuccess) return e;
   HeadArgs a;
-  // Column split for batches of at most 64 rows (and lists that fit the
-  // exchange): 4 row copies of one lane quarter, or 2 of two.
+  // Column split for batches of at most 64 rows with a heavy epilogue (sampling, or
+  // lists of 16 or 20 entries; longer lists do not fit the exchange): 4 row copies of
+  // one lane quarter, or 2 of two.  A light epilogue keeps up with one warp per lane
+  // quarter: batches of at most 32 rows then take the deep layout instead (a deeper
+  // ring of W stages, HeadCfg<KCAP, true>), which pays more on an HBM-bound head.
   a.rep = 1;
   a.rep_nq = 4;
   static_assert(HeadCfg<20>::kRepOk && !HeadCfg<32>::kRepOk, "column split: list capacities up to 20");
-  const bool rep_ok = plan.kcap <= 20;
+  const bool sampling = samp && samp->enabled;
+  const bool rep_ok = plan.kcap <= 20 && (sampling || plan.kcap >= 16);
   if (rows >= 1 && rows <= 64 && rep_ok) {
     a.rep_nq = (rows + 31) / 32;
     a.rep = 4 / a.rep_nq;
   }
+  const bool deep = !sampling && a.rep == 1 && rows <= 32 && plan.kcap <= 32;
   a.a_bytes = static_cast<uint32_t>(a.rep) * a_box * kBK * 2;
   a.rows = rows;
   a.H = H;
@@ -174,7 +179,7 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   a.out = final_out ? *final_out : RowOutputs{nullptr, nullptr, nullptr, nullptr};
   const dim3 grid(plan.grid);
   const bool mat = logits_out != nullptr;
-  if (!a.samp.enabled) return launch_head_mode<kSampNone>(plan.kcap, mat, grid, stream, pdl, ta, tb, a);
+  if (!a.samp.enabled) return launch_head_mode<kSampNone>(plan.kcap, mat, deep, grid, stream, pdl, ta, tb, a);
   // Sampling: the candidate filter pays off when a warp's rows see long vocabulary
   // ranges (its test tightens as the row's best score grows) or when few lanes hold
   // rows (a block's second pass runs for the lanes that have candidates); otherwise
@@ -184,8 +189,8 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   const int lanes = plan.m_tiles == 1 ? (rows < 32 ? rows : 32) : 32;
   const int blocks_per_unit = plan.tiles_per_split * (kBN / 64) / a.rep;
   if (lanes <= 16 || blocks_per_unit >= 64)
-    return launch_head_mode<kSampFiltered>(plan.kcap, mat, grid, stream, pdl, ta, tb, a);
-  return launch_head_mode<kSampAll>(plan.kcap, mat, grid, stream, pdl, ta, tb, a);
+    return launch_head_mode<kSampFiltered>(plan.kcap, mat, false, grid, stream, pdl, ta, tb, a);
+  return launch_head_mode<kSampAll>(plan.kcap, mat, false, grid, stream, pdl, ta, tb, a);
 }
 
 }  // namespace lmh

@@ -48,13 +48,20 @@ constexpr uint32_t kStageBytesB = kBN * kBK * 2;  // 32 KB
 // in registers and uses the shared region to stage candidate blocks (4 warps x
 // 64 columns x 32 lanes x 4 bytes); KCAP 128 keeps a min-heap per row in
 // shared memory (slot-major) and has room for only 2 pipeline stages.
-template <int KCAP>
+//
+// kDeep: the layout of batches of at most 32 rows whose epilogue is one warp (no column
+// split): A slices of 32 rows (4 KB; the MMA still reads 128 rows from a slice's base, and
+// the rows past it only reach accumulator lanes no warp reads), one warp's staging region,
+// and 6 stages in place of 4, so more of W is in flight.
+template <int KCAP, bool kDeep = false>
 struct HeadCfg {
   static constexpr bool kRegList = KCAP <= 32;
-  static constexpr int kStages = kRegList ? 4 : 2;
-  static constexpr size_t kListBytes = kRegList ? static_cast<size_t>(4) * 64 * 32 * 4
-                                                : static_cast<size_t>(kBM) * KCAP * 8;
-  static constexpr size_t kSmem = 1024 /*alignment slack*/ + kStages * (kStageBytesA + kStageBytesB) +
+  static constexpr int kStages = kDeep ? 6 : (kRegList ? 4 : 2);
+  static constexpr uint32_t kStageA = kDeep ? 32 * kBK * 2 : kStageBytesA;
+  static constexpr size_t kListBytes = kDeep ? static_cast<size_t>(64) * 32 * 4
+                                       : kRegList ? static_cast<size_t>(4) * 64 * 32 * 4
+                                                  : static_cast<size_t>(kBM) * KCAP * 8;
+  static constexpr size_t kSmem = 1024 /*alignment slack*/ + kStages * (kStageA + kStageBytesB) +
                                   kListBytes + (2 * kStages + 6) * 8 + 16;
   // Small batches may split each tile's columns over the epilogue warps (see
   // HeadArgs::rep); a warp then hands its row state to the leader through its
@@ -338,17 +345,18 @@ __device__ __forceinline__ uint32_t noise_word_limit(float t) {
 // (kSampAll) or only the tokens whose Philox word passes the candidate test (kSampFiltered).
 constexpr int kSampNone = 0, kSampAll = 1, kSampFiltered = 2;
 
-template <int KCAP, bool kMaterialize, int kSamp>
+template <int KCAP, bool kMaterialize, int kSamp, bool kDeep = false>
 __global__ void __launch_bounds__(kHeadThreads, 1)
     head_logprobs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const HeadArgs a) {
-  using Cfg = HeadCfg<KCAP>;
+  using Cfg = HeadCfg<KCAP, kDeep>;
+  static_assert(!kDeep || (Cfg::kRegList && kSamp == 0), "the deep layout: register lists, no sampling");
   constexpr int S = Cfg::kStages;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   unsigned char* sA = smem;
-  unsigned char* sB = sA + S * kStageBytesA;
+  unsigned char* sB = sA + S * Cfg::kStageA;
   uint64_t* lists = reinterpret_cast<uint64_t*>(sB + S * kStageBytesB);
   uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(lists) + Cfg::kListBytes);
   uint64_t* empty = full + S;
@@ -438,29 +446,35 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
       auto load_a = [&](int s, int kb_, int m_tile_) {
         if (a.rep > 1) {
           for (int p = 0; p < a.rep; ++p)
-            tma_load_2d(sA + s * kStageBytesA + p * a.rep_nq * 32 * 128, &tmap_a, kb_ * kBK, 0, &full[s]);
+            tma_load_2d(sA + s * Cfg::kStageA + p * a.rep_nq * 32 * 128, &tmap_a, kb_ * kBK, 0, &full[s]);
         } else {
-          tma_load_2d(sA + s * kStageBytesA, &tmap_a, kb_ * kBK, m_tile_ * kBM, &full[s]);
+          tma_load_2d(sA + s * Cfg::kStageA, &tmap_a, kb_ * kBK, m_tile_ * kBM, &full[s]);
         }
       };
       pdl_wait();  // the gathered rows are written by the preceding kernel
 #pragma unroll
       for (int j = 0; j < S; ++j)
         if (j < np) load_a(j, pk[j], pm[j]);
-      for (uint32_t it = np; valid; ++it) {
-        const int s = it % S;
-        const uint32_t ph = (it / S) & 1u;
+      int s = np == S ? 0 : np;
+      uint32_t ph = np == S ? 1u : 0u;
+      while (valid) {
         if (!wait_or_abort(&empty[s], ph ^ 1u, abort_flag, a.dev_status)) break;
         mbar_arrive_expect_tx(&full[s], a.a_bytes + kStageBytesB);
         load_a(s, kb, m_tile);
         tma_load_2d(sB + s * kStageBytesB, &tmap_b, kb * kBK, n * kBN, &full[s]);
         advance();
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
     }
   } else if (warp == 1) {
     // ------------------------- MMA issuer -------------------------
     if (lane == 0) {
-      uint32_t it = 0, t = 0;
+      uint32_t t = 0;
+      int s = 0;
+      uint32_t ph = 0;
       bool live = true;
       for (int u = blockIdx.x; u < a.num_units && live; u += gridDim.x) {
         const int split = u / a.m_tiles;
@@ -474,15 +488,13 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + b * kBN;
-          for (int kb = 0; kb < k_blocks; ++kb, ++it) {
-            const int s = it % S;
-            const uint32_t ph = (it / S) & 1u;
+          for (int kb = 0; kb < k_blocks; ++kb) {
             if (!wait_or_abort(&full[s], ph, abort_flag, a.dev_status)) {
               live = false;
               break;
             }
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(sA + s * kStageBytesA);
+            const uint32_t a_addr = smem_u32(sA + s * Cfg::kStageA);
             const uint32_t b_addr = smem_u32(sB + s * kStageBytesB);
 #pragma unroll
             for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
@@ -491,6 +503,10 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
               umma_bf16(d_tmem, ad, bd, (kb > 0 || kk > 0) ? 1u : 0u);
             }
             umma_commit(&empty[s]);
+            if (++s == S) {
+              s = 0;
+              ph ^= 1u;
+            }
           }
           if (live) umma_commit(&acc_full[b]);
         }
@@ -877,13 +893,44 @@ cudaError_t head_attr_mode() {
   LMH_HEAD_ATTR(32)
   LMH_HEAD_ATTR(128)
 #undef LMH_HEAD_ATTR
+  if constexpr (kSamp == kSampNone) {
+#define LMH_HEAD_ATTR_DEEP(KC)                                                 \
+  set(head_logprobs_kernel<KC, false, kSamp, true>, HeadCfg<KC, true>::kSmem); \
+  set(head_logprobs_kernel<KC, true, kSamp, true>, HeadCfg<KC, true>::kSmem);
+    LMH_HEAD_ATTR_DEEP(1)
+    LMH_HEAD_ATTR_DEEP(5)
+    LMH_HEAD_ATTR_DEEP(8)
+    LMH_HEAD_ATTR_DEEP(32)
+#undef LMH_HEAD_ATTR_DEEP
+  }
   return e;
 }
 
 template <int kSamp>
-cudaError_t launch_head_mode(int kcap, bool materialize, dim3 grid, cudaStream_t stream, bool pdl,
+cudaError_t launch_head_mode(int kcap, bool materialize, bool deep, dim3 grid, cudaStream_t stream, bool pdl,
                              const CUtensorMap& ta, const CUtensorMap& tb, const HeadArgs& a) {
   const dim3 block(kHeadThreads);
+  if constexpr (kSamp == kSampNone) {
+    if (deep) {
+      switch (kcap) {
+#define LMH_HEAD_CASE_DEEP(KC)                                                                                   \
+  case KC:                                                                                                       \
+    return materialize ? launch_kernel(head_logprobs_kernel<KC, true, kSamp, true>, grid, block,                 \
+                                       HeadCfg<KC, true>::kSmem, stream, pdl, ta, tb, a)                         \
+                       : launch_kernel(head_logprobs_kernel<KC, false, kSamp, true>, grid, block,                \
+                                       HeadCfg<KC, true>::kSmem, stream, pdl, ta, tb, a);
+        LMH_HEAD_CASE_DEEP(1)
+        LMH_HEAD_CASE_DEEP(5)
+        LMH_HEAD_CASE_DEEP(8)
+        LMH_HEAD_CASE_DEEP(32)
+#undef LMH_HEAD_CASE_DEEP
+        default:
+          return cudaErrorInvalidValue;
+      }
+    }
+  } else if (deep) {
+    return cudaErrorInvalidValue;
+  }
   switch (kcap) {
 #define LMH_HEAD_CASE(KC)                                                                                      \
   case KC:                                                                                                     \
@@ -906,7 +953,7 @@ cudaError_t launch_head_mode(int kcap, bool materialize, dim3 grid, cudaStream_t
 
 #define LMH_HEAD_MODE_DECL(EXT, MODE)                                                                           \
   EXT template cudaError_t head_attr_mode<MODE>();                                                              \
-  EXT template cudaError_t launch_head_mode<MODE>(int, bool, dim3, cudaStream_t, bool, const CUtensorMap&,     \
+  EXT template cudaError_t launch_head_mode<MODE>(int, bool, bool, dim3, cudaStream_t, bool, const CUtensorMap&, \
                                                   const CUtensorMap&, const HeadArgs&);
 
 }  // namespace lmh
