@@ -89,7 +89,7 @@ __device__ __noinline__ void cta_sample(const MergeArgs& a, int row, int nslots,
   }
 }
 
-constexpr int kMergeItemsPerThread = 8;  // a row's keys held in registers per thread (first round)
+constexpr int kMergeItemsPerThread = 12;  // a row's keys held in registers per thread (first round)
 
 __global__ void __launch_bounds__(kMergeThreads, 4) merge_partials_kernel(const MergeArgs a) {
   __shared__ uint64_t cand[kMergeCap];
@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_partials_kernel(const 
   __shared__ uint32_t misc[4];  // [0] candidates, [1..2] select broadcast
   __shared__ float red[32];
   __shared__ uint64_t red64[32];
+  __shared__ uint32_t lbw[kMergeThreads / 32];  // per-warp bounds (read once, after one barrier)
   pdl_wait();  // the partials come from the kernel launched just before
   pdl_launch_dependents();  // a following kernel may be scheduled; it waits for this grid before using its results
   const int row = blockIdx.x;
@@ -174,44 +175,50 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_partials_kernel(const 
   }
 
   // ---- lb: a lower bound of the row's k-th key ----
-  // U = the q best keys of every slot, q = ceil(k / nslots), so |U| >= k and
-  // the k-th largest key of U is reached by k keys of the row.  (Taking the
-  // largest k-th key of a single slot is also a bound, but with many slots
-  // far more keys pass it.)  Keys are unique; empty entries (0) rank last.
+  // The first k entries of a slot's list are logits of the row (the slot's best k; the
+  // entries past the row's K are not written).  Every warp takes the q-th largest value
+  // among such keys its threads hold (q = ceil(k / warps): q rounds of a warp-wide max,
+  // one holder of the maximum dropping out each round); the minimum t over the warps is
+  // reached by q * warps >= k logits of the row, so the row's k-th key has a value >= t
+  // and every top-k key is >= (t, any id).  A warp holding fewer than q keys gives t = 0:
+  // no pruning.
   uint64_t lb = 0;
-  const int q = (k + nslots - 1) / nslots;
-  const int nu = q * nslots;
-  if (nu <= kMergeCap) {
-    auto put_u = [&](int i, uint64_t key) {
-      const int j = i / a.k_max, r = i - j * a.k_max;
-      if (r < q) cand[j * q + r] = key;
-    };
+  {
+    constexpr int kWarps = kMergeThreads / 32;
+    const int q = (k + kWarps - 1) / kWarps;
+    uint32_t uv[kMergeItemsPerThread];  // ordered values of the held keys (0: none)
     int j = j0, r = r0;
 #pragma unroll
     for (int u = 0; u < kMergeItemsPerThread; ++u) {
-      if (tid + u * kMergeThreads < n_items && r < q) cand[j * q + r] = kv[u];
+      uv[u] = r < k ? static_cast<uint32_t>(kv[u] >> 32) : 0u;  // kv is 0 past the row's items
       next(j, r);
     }
-    for (int i = tid + kMergeItemsPerThread * kMergeThreads; i < n_items; i += kMergeThreads) put_u(i, keys[i]);
-    __syncthreads();
-    for (int i = tid; i < nu; i += kMergeThreads) {
-      const uint64_t key = cand[i];
-      int rank = 0;  // by key desc, then position asc
-      for (int j = 0; j < nu; ++j) {
-        const uint64_t o = cand[j];
-        rank += (o > key) | ((o == key) & (j < i));
+    const int lane = tid & 31;
+    uint32_t t = 0;
+    for (int round = 0; round < q; ++round) {
+      uint32_t mine = 0;
+#pragma unroll
+      for (int u = 0; u < kMergeItemsPerThread; ++u) mine = max(mine, uv[u]);
+      const uint32_t wmax = __reduce_max_sync(0xffffffffu, mine);
+      t = wmax;
+      if (wmax == 0u) break;  // fewer than q held keys in this warp
+      const unsigned holders = __ballot_sync(0xffffffffu, mine == wmax);
+      if (lane == __ffs(holders) - 1) {  // drop one instance of the maximum
+        bool done = false;
+#pragma unroll
+        for (int u = 0; u < kMergeItemsPerThread; ++u) {
+          const bool hit = !done && uv[u] == wmax;
+          uv[u] = hit ? 0u : uv[u];
+          done = done || hit;
+        }
       }
-      if (rank == k - 1) red64[0] = key;
     }
+    if (lane == 0) lbw[tid >> 5] = t;
     __syncthreads();
-    lb = red64[0];
-    __syncthreads();  // cand is reused below
-  } else {
-    for (int j = tid; j < nslots; j += kMergeThreads) {
-      const uint64_t kk = keys[static_cast<int64_t>(j) * a.k_max + (k - 1)];
-      lb = kk > lb ? kk : lb;
-    }
-    lb = block_max_u64(lb, red64);
+    uint32_t tmin = 0xFFFFFFFFu;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) tmin = min(tmin, lbw[w]);
+    lb = static_cast<uint64_t>(tmin) << 32;
   }
 
   // ---- candidates: the keys >= lb among the first k of every slot ----
