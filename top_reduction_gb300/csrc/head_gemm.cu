@@ -53,6 +53,8 @@ cudaError_t launch_gather_rows(const void* hidden, int64_t hidden_stride, int nu
 // host side: plan, tensor maps, launch
 // ---------------------------------------------------------------------------
 
+constexpr int kRepMaxH = 2048;  // hidden sizes from which lists of 16-20 need no column split
+
 HeadPlan head_plan(int rows, int H, int V, int k_max, int num_sms) {
   (void)H;
   HeadPlan p;
@@ -142,16 +144,18 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   e = make_tmap(&tb, W, static_cast<uint64_t>(H), static_cast<uint64_t>(V), static_cast<uint64_t>(H), kBK, kBN);
   if (e != cudaSuccess) return e;
   HeadArgs a;
-  // Column split for batches of at most 64 rows with a heavy epilogue (sampling, or
-  // lists of 16 or 20 entries; longer lists do not fit the exchange): 4 row copies of
-  // one lane quarter, or 2 of two.  A light epilogue keeps up with one warp per lane
-  // quarter: batches of at most 32 rows then take the deep layout instead (a deeper
-  // ring of W stages, HeadCfg<KCAP, true>), which pays more on an HBM-bound head.
+  // Column split for batches of at most 64 rows with a heavy epilogue: sampling, or
+  // lists of 16 or 20 entries on short tiles (H below kRepMaxH: the tile's W streams in
+  // less time than one warp needs for the lists of its early blocks); longer lists do
+  // not fit the exchange.  4 row copies of one lane quarter, or 2 of two.  Otherwise
+  // one warp per lane quarter keeps up, and batches of at most 32 rows take the deep
+  // layout (a deeper ring of W stages, HeadCfg<KCAP, true>), which pays more on an
+  // HBM-bound head.
   a.rep = 1;
   a.rep_nq = 4;
   static_assert(HeadCfg<20>::kRepOk && !HeadCfg<32>::kRepOk, "column split: list capacities up to 20");
   const bool sampling = samp && samp->enabled;
-  const bool rep_ok = plan.kcap <= 20 && (sampling || plan.kcap >= 16);
+  const bool rep_ok = plan.kcap <= 20 && (sampling || (plan.kcap >= 16 && H < kRepMaxH));
   if (rows >= 1 && rows <= 64 && rep_ok) {
     a.rep_nq = (rows + 31) / 32;
     a.rep = 4 / a.rep_nq;

@@ -900,6 +900,8 @@ cudaError_t head_attr_mode() {
     LMH_HEAD_ATTR_DEEP(1)
     LMH_HEAD_ATTR_DEEP(5)
     LMH_HEAD_ATTR_DEEP(8)
+    LMH_HEAD_ATTR_DEEP(16)
+    LMH_HEAD_ATTR_DEEP(20)
     LMH_HEAD_ATTR_DEEP(32)
 #undef LMH_HEAD_ATTR_DEEP
   }
@@ -922,6 +924,8 @@ cudaError_t launch_head_mode(int kcap, bool materialize, bool deep, dim3 grid, c
         LMH_HEAD_CASE_DEEP(1)
         LMH_HEAD_CASE_DEEP(5)
         LMH_HEAD_CASE_DEEP(8)
+        LMH_HEAD_CASE_DEEP(16)
+        LMH_HEAD_CASE_DEEP(20)
         LMH_HEAD_CASE_DEEP(32)
 #undef LMH_HEAD_CASE_DEEP
         default:
