@@ -280,13 +280,14 @@ def test_full_vocabulary_output(lmh, rows, H, V):
 
 @pytest.mark.parametrize("rows,H,V,k", [(40, 128, 200, 20), (50, 256, 40000, 16), (32, 64, 70001, 5),
                                         (33, 192, 3000, 8), (9, 1024, 151936, 20), (2, 64, 513, 1),
-                                        (20, 128, 5000, 25)])
+                                        (20, 128, 5000, 25), (24, 2048, 20000, 20), (16, 2560, 9000, 16)])
 def test_small_batch_column_split(lmh, rows, H, V, k):
     """Batches of at most 64 rows: with lists of 16 or 20 entries each tile's
     columns are split over the epilogue warps (4 copies of 32 rows, or 2 of 64)
     and the copies' lse, top-k and selected logit are folded per row; lighter
     lists on at most 32 rows take the deep-ring layout (4 KB A slices, 6
-    stages).  Per-row K, selected ids in every block position, a one-split plan
+    stages; lists of 16-20 on hidden sizes of 2048 and more take it too).  Per-row K,
+    selected ids in every block position, a one-split plan
     (V 200) and equal logits in different blocks (duplicated W rows) must all
     match the oracle."""
     g = torch.Generator().manual_seed(rows * 131 + V)
