@@ -565,7 +565,11 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
           break;
         }
         tc_fence_after();
+        // The accumulator is handed back to the MMA as soon as this warp's last block of
+        // the tile is in registers, so the next tile can start while that block is reduced.
+        bool released = false;
         if (warp_active) {
+          const int last_c = copy + ((kBN / kBlock - 1 - copy) / n_rep) * n_rep;
 #pragma unroll 1
           for (int c = copy; c < kBN / kBlock; c += n_rep) {
             const int col0 = n * kBN + c * kBlock;
@@ -573,7 +577,12 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             float v[kBlock];
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kBN + c * kBlock;
             __syncwarp();
-            tmem_ld64(taddr, v);
+            tmem_ld64(taddr, v);  // waits for the load (tcgen05.wait::ld)
+            if (c == last_c) {
+              tc_fence_before();
+              mbar_arrive(&acc_empty[b]);
+              released = true;
+            }
             if (a.logit_scale != 1.0f) {  // head transform, applied before everything else reads the logits
 #pragma unroll
               for (int j = 0; j < kBlock; ++j) v[j] *= a.logit_scale;
@@ -737,8 +746,10 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             }
           }
         }
-        tc_fence_before();
-        mbar_arrive(&acc_empty[b]);
+        if (!released) {
+          tc_fence_before();
+          mbar_arrive(&acc_empty[b]);
+        }
       }
       if (!live) break;
       // Column split: every copy's warp stages its row state and its sorted list (keys,
