@@ -38,7 +38,7 @@
  *       bitmask applied in the compacted layout (vllm-metal release,
  *       "Testing": bitmask application under the compacted layout).
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings where the pages are silent:
  *   - decode sequences keep all their rows [cu[s], cu[s+1]);
  *   - an empty prefill segment, a non-monotone cu_seqlens or cu[0] != 0
  *     is rejected (return code ORACLE_ERR_BAD_CU);
