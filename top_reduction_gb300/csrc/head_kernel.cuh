@@ -22,9 +22,14 @@
 //   * Persistent CTAs walk "units" = (128-row tile, vocabulary range); the
 //     per-row state lives across the n-tiles of a unit and is flushed as one
 //     partial per (row, range) that merge_partials.cu combines.
-//   * Batches of at most 64 rows split each tile's columns over the four
-//     epilogue warps: the A stage holds a copy of the rows in every lane
-//     quarter that the warps then share out (HeadArgs::rep).
+//   * Batches of at most 64 rows with a heavy epilogue (sampling, or longer
+//     lists on short tiles) split each tile's columns over the four epilogue
+//     warps: the A stage holds a copy of the rows in every lane quarter that
+//     the warps then share out (HeadArgs::rep).  Batches of at most 32 rows
+//     with a light epilogue take the deep layout instead (HeadCfg<KCAP, true>):
+//     small A slices and 6 stages, so more of W is in flight.
+//   * An epilogue warp hands the accumulator back to the MMA as soon as its
+//     last block of the tile is in registers.
 #pragma once
 
 #include <cuda.h>
