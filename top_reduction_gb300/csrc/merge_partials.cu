@@ -64,8 +64,9 @@ __device__ __forceinline__ void samp_write(const MergeArgs& a, int row, float4 b
 //         M = max_j m_j (lse = -inf when every logit is -inf);
 //   top-k = the k best keys of the union of the slots' sorted top-k lists.
 //         Every slot list holds that piece's k best, so the union holds the
-//         row's k best.  A lower bound L of the row's k-th key (the k-th
-//         largest of the slots' leading keys) limits the gather to keys >= L;
+//         row's k best.  A lower bound L of the row's k-th key (the minimum
+//         over the warps of each warp's q-th largest held list value, q =
+//         ceil(k / warps)) limits the gather to keys >= L;
 //         they are ordered by rank.
 // The best of a row's slot partials, by the whole CTA (kept out of line so
 // that its registers do not add to the merge's).
