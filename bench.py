@@ -52,6 +52,8 @@ def parse_args():
                    help="override the workload's K (-1: the full-vocabulary output, every id's logprob)")
     p.add_argument("--logit-scale", type=float, default=1.0,
                    help="head transform: every logit scaled by this factor (head workloads)")
+    p.add_argument("--w-hv", action="store_true",
+                   help="the head weight stored [H x V] (vocabulary contiguous) instead of lm_head.weight's [V x H]")
     p.add_argument("--sample", action="store_true",
                    help="device-side Gumbel-max sampling of every row at temperature 1 (head workloads)")
     return p.parse_args()
@@ -87,6 +89,8 @@ def apply_options(b, args):
         b = dict(b, logit_scale=args.logit_scale)
     if getattr(args, "sample", False) and b["name"] != "logits_chunk":
         b = dict(b, sample=True)
+    if getattr(args, "w_hv", False) and b["name"] != "logits_chunk":
+        b = dict(b, w_hv=True)
     return b
 
 
@@ -102,6 +106,8 @@ def workload_config(b):
         cfg["logit_scale"] = b["logit_scale"]
     if b.get("sample"):
         cfg["sampling"] = "Gumbel-max, temperature 1, every row"
+    if b.get("w_hv"):
+        cfg["w_layout"] = "[H x V] (vocabulary contiguous)"
     return cfg
 
 
@@ -253,7 +259,8 @@ class Step:
             self.sampling = {"temperature": torch.ones(int(b["n_sel"]), dtype=torch.float32, device=device),
                              "seed": 1234, "offsets": torch.arange(int(b["n_sel"]), dtype=torch.int64, device=device)}
         self.hidden = b["hidden"].to(device)
-        self.W = b["W"].to(device)
+        self.w_layout = lmh.W_HV if b.get("w_hv") else lmh.W_VH
+        self.W = (b["W"].t().contiguous() if b.get("w_hv") else b["W"]).to(device)
         self.cu = b["cu_seqlens"].to(device)
         self.mask = None if b["all_rows_mask"] is None else b["all_rows_mask"].to(device)
         self.sel = b["sel"].to(device)
@@ -282,12 +289,12 @@ class Step:
         if self.full:
             return lmh.project_logprobs(self.hidden, self.W, sel=self.sel, row_k=self.row_k, k_max=self.k,
                                         workspace=self.ws, out=self.out, dev_status=self.status,
-                                        logit_scale=self.scale, sampling=self.sampling)
+                                        logit_scale=self.scale, sampling=self.sampling, w_layout=self.w_layout)
         ri, _ = lmh.select_rows(self.cu, self.b["num_decode"], self.mask, max_out_rows=self.rows,
                                 dev_status=self.status)
         return lmh.project_logprobs(self.hidden, self.W, row_idx=ri, sel=self.sel, row_k=self.row_k,
                                     k_max=self.k, workspace=self.ws, out=self.out, dev_status=self.status,
-                                    logit_scale=self.scale, sampling=self.sampling)
+                                    logit_scale=self.scale, sampling=self.sampling, w_layout=self.w_layout)
 
 
 def max_over_ranks(ms, dist, device):
@@ -340,7 +347,8 @@ def e2e_leg(lmh, b, device, steps):
     for key, v in src.items():
         h_in[key].copy_(v)
     if not chunk:
-        W = b["W"].to(device)
+        w_layout = lmh.W_HV if b.get("w_hv") else lmh.W_VH
+        W = (b["W"].t().contiguous() if b.get("w_hv") else b["W"]).to(device)
         mask = None if b["all_rows_mask"] is None else b["all_rows_mask"].to(device)
         row_k = None if b["row_k"] is None else b["row_k"].to(device)
     rows = b["rows"] if chunk else int(b["n_sel"])
@@ -372,7 +380,8 @@ def e2e_leg(lmh, b, device, steps):
         else:
             ri, _ = lmh.select_rows(d_in["cu"], b["num_decode"], mask, max_out_rows=rows)
             o = lmh.project_logprobs(d_in["hidden"], W, row_idx=ri, sel=d_in["sel"], row_k=row_k, k_max=k,
-                                     workspace=bf["ws"], out=bf["out"], logit_scale=b.get("logit_scale", 1.0))
+                                     workspace=bf["ws"], out=bf["out"], logit_scale=b.get("logit_scale", 1.0),
+                                     w_layout=w_layout)
         assert all(o[key].data_ptr() == bf["out"][key].data_ptr() for key in bf["out"])
         bf["h_out_buf"].copy_(bf["d_out_buf"], non_blocking=True)  # one copy out
 

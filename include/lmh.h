@@ -69,7 +69,7 @@ typedef enum lmh_dtype { LMH_BF16 = 0, LMH_F16 = 1, LMH_F32 = 2 } lmh_dtype;
 /* Storage of the head weight W, whose math shape is [H x V]. */
 typedef enum lmh_w_layout {
     LMH_W_VH = 0, /* stored [V x H] row-major: PyTorch lm_head.weight (H contiguous) */
-    LMH_W_HV = 1  /* stored [H x V] row-major (not implemented: LMH_ERR_UNSUPPORTED)  */
+    LMH_W_HV = 1  /* stored [H x V] row-major (V contiguous; V % 8 == 0)            */
 } lmh_w_layout;
 
 /* Which entry point a workspace is sized for. */
@@ -156,7 +156,11 @@ size_t lmh_workspace_bytes(int32_t rows, int32_t hidden, int32_t vocab, int32_t 
  *   num_tokens        rows of `hidden` (bounds for row_idx).
  *   row_idx           device int32 [rows] or NULL.
  *   rows, H, V        sizes; H % 8 == 0.
- *   W                 device bf16, layout w_layout (LMH_W_VH only), 16-byte aligned.
+ *   W                 device bf16, layout w_layout, 16-byte aligned; with
+ *                     LMH_W_HV, V % 8 == 0 (rows of V elements are 16-byte
+ *                     multiples).  Both layouts run the same kernels at the
+ *                     same speed: the [H x V] slices enter the tensor cores
+ *                     vocabulary-major.
  *   sel_ids           device int32 [rows] or NULL; -1 = no selected token (NaN).
  *   row_k             device int32 [rows] or NULL (= k_max); values clamped to [0, k_max].
  *   k_max             0..LMH_K_MAX and <= V, or LMH_K_FULL.
@@ -174,7 +178,7 @@ size_t lmh_workspace_bytes(int32_t rows, int32_t hidden, int32_t vocab, int32_t 
  *   workspace         device, >= lmh_workspace_bytes(rows, H, V, k_max,
  *                     LMH_PATH_PROJECT) bytes, 256-byte aligned.
  * Errors: LMH_ERR_INVALID_ARG, LMH_ERR_UNSUPPORTED (k_max < -1 or > LMH_K_MAX,
- * W layout LMH_W_HV, H % 8 != 0, misaligned pointers),
+ * LMH_W_HV with V % 8 != 0, H % 8 != 0, misaligned pointers),
  * LMH_ERR_WORKSPACE_TOO_SMALL, LMH_ERR_CUDA.  Device: LMH_DS_SEL_OUT_OF_RANGE,
  * LMH_DS_ROW_IDX_OUT_OF_RANGE, LMH_DS_TIMEOUT.
  */

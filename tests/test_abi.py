@@ -106,7 +106,8 @@ def test_project_argument_checks_return_before_launch(lib):
     assert _call_project(lib, sel=ctypes.c_void_p(0x6000)) == E.ERR_INVALID_ARG  # sel without sel_logprob
     assert _call_project(lib, stride=32) == E.ERR_INVALID_ARG        # stride < H
     assert _call_project(lib, rows=9) == E.ERR_INVALID_ARG           # rows > num_tokens, no row_idx
-    assert _call_project(lib, layout=1) == E.ERR_UNSUPPORTED         # [H x V] storage
+    assert _call_project(lib, layout=1, V=4100) == E.ERR_UNSUPPORTED  # [H x V] storage needs V % 8 == 0
+    assert _call_project(lib, layout=2) == E.ERR_INVALID_ARG
     assert _call_project(lib, layout=7) == E.ERR_INVALID_ARG
     assert _call_project(lib, H=60, stride=60) == E.ERR_UNSUPPORTED  # H % 8
     assert _call_project(lib, W=0x2002) == E.ERR_UNSUPPORTED         # misaligned W

@@ -341,3 +341,32 @@ def test_cuda_graph_capture_and_replay(lmh, tiny):
     for key in ("lse", "topk_ids", "topk_logprobs"):
         assert torch.equal(cap[key], again[key]), key
     assert not torch.equal(cap["topk_ids"], eager["topk_ids"])
+
+
+@pytest.mark.parametrize("rows,H,V,k,scale", [(32, 2560, 151936, 5, 1.0), (200, 136, 4104, 20, 1.0),
+                                              (9, 1024, 20000, 20, 1.0), (129, 64, 1000, 128, 1.0),
+                                              (40, 512, 33000, 8, 0.25)])
+def test_w_stored_h_by_v(lmh, rows, H, V, k, scale):
+    """W stored [H x V] (vocabulary contiguous, LMH_W_HV): the W slices enter the tensor
+    cores vocabulary-major.  Parity with the oracle's [H x V] projection, and the same
+    results as the [V x H] call on the transposed weight."""
+    from top_reduction_gb300 import lmh as L
+    g = torch.Generator().manual_seed(rows + H + V)
+    T = rows + 3
+    hidden = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    W_vh = (torch.randn(V, H, generator=g) * (2.0 / H ** 0.5)).to(torch.bfloat16)
+    W_hv = W_vh.t().contiguous()
+    ri = torch.randperm(T, generator=g)[:rows].to(torch.int32)
+    sel = torch.randint(-1, V, (rows,), generator=g, dtype=torch.int32)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = lmh.project_logprobs(hidden.cuda(), W_hv.cuda(), row_idx=ri.cuda(), sel=sel, k_max=k, dev_status=st,
+                             logit_scale=scale, w_layout=L.W_HV)
+    ref = lmh.project_logprobs(hidden.cuda(), W_vh.cuda(), row_idx=ri.cuda(), sel=sel, k_max=k, logit_scale=scale)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    z = oracle.project(_bits(hidden), _bits(W_hv), row_idx=ri.numpy(), w_layout=1) * scale
+    orc = oracle.logprobs(z, sel=sel.numpy(), k_max=k)
+    A = hidden[ri.long()].float().double().numpy()
+    check_fused(o, orc, z, A, W_vh, k, what="W [H x V] %s" % ((rows, H, V, k),), scale=scale)
+    for key in ("lse", "sel_logprob", "topk_ids", "topk_logprobs"):
+        assert torch.equal(o[key], ref[key]), key

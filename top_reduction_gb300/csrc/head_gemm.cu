@@ -131,7 +131,7 @@ cudaError_t head_setup() {
 cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const void* W, int V, const HeadPlan& plan,
                         const int32_t* sel, const int32_t* row_k, int k_max, Partials parts, float* logits_out,
                         uint32_t* dev_status, cudaStream_t stream, bool pdl, const RowOutputs* final_out,
-                        float logit_scale, const SampleArgs* samp) {
+                        float logit_scale, const SampleArgs* samp, bool w_hv) {
   if (final_out && plan.splits != 1) return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
   // With fewer than 128 rows (one row tile) the A box covers only the real
@@ -141,7 +141,9 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   cudaError_t e = make_tmap(&ta, A, static_cast<uint64_t>(H), static_cast<uint64_t>(rows),
                             static_cast<uint64_t>(a_stride), kBK, a_box);
   if (e != cudaSuccess) return e;
-  e = make_tmap(&tb, W, static_cast<uint64_t>(H), static_cast<uint64_t>(V), static_cast<uint64_t>(H), kBK, kBN);
+  // W [V x H]: [256 x 64] boxes along H; W [H x V]: [64 x 64] boxes, vocabulary innermost
+  e = w_hv ? make_tmap(&tb, W, static_cast<uint64_t>(V), static_cast<uint64_t>(H), static_cast<uint64_t>(V), 64, kBK)
+           : make_tmap(&tb, W, static_cast<uint64_t>(H), static_cast<uint64_t>(V), static_cast<uint64_t>(H), kBK, kBN);
   if (e != cudaSuccess) return e;
   HeadArgs a;
   // Column split for batches of at most 64 rows with a heavy epilogue: sampling, or
@@ -162,6 +164,7 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   }
   const bool deep = !sampling && a.rep == 1 && rows <= 32 && plan.kcap <= 32;
   a.a_bytes = static_cast<uint32_t>(a.rep) * a_box * kBK * 2;
+  a.w_hv = w_hv ? 1 : 0;
   a.rows = rows;
   a.H = H;
   a.V = V;

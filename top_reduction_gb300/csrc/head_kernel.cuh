@@ -89,6 +89,7 @@ struct HeadArgs {
   // quarter has the rows and epilogue warp q (copy q / rep_nq) reduces only
   // the 64-column blocks c == copy (mod rep) of each tile.  rep 1: off.
   int rep, rep_nq;
+  int w_hv;  // W stored [H x V] (vocabulary contiguous): 4 boxes of 64 columns per W slice, MN-major MMA operand
   float logit_scale;  // head transform: every logit is logit_scale * (A . W) (1: none)
   SampleArgs samp;    // device-side sampling (kernels with kSamp != 0)
   int final_out;   // one vocabulary split: write the final results (out), not partials
@@ -124,20 +125,38 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N = kBN, M = kBM.
+// Shared-memory matrix descriptor: vocabulary-major (MN-major) W slice of a
+// [H x V] head, 128-byte swizzle.  The slice is 4 blocks of 64 vocabulary
+// columns (128-byte rows) x 64 hidden rows, 8 KB apart; within a block, groups
+// of 8 hidden rows are 1024 bytes apart.  One MMA reads 16 hidden rows: its
+// start address advances by 2048 bytes per K step.
+constexpr uint32_t kHvBlockBytes = 64 * kBK * 2;  // 8 KB: 64 vocabulary columns x 64 hidden rows
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(kHvBlockBytes >> 4) << 16;  // between 64-column blocks (MN direction)
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;          // between 8-row groups (K direction)
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major,
+// B K-major (kIdesc) or MN-major (kIdescBmn, bit 16), N = kBN, M = kBM.
 constexpr uint32_t kIdesc = (1u << 4)                                   // D format: f32
                             | (1u << 7)                                 // A format: bf16
                             | (1u << 10)                                // B format: bf16
                             | (static_cast<uint32_t>(kBN >> 3) << 17)   // N / 8
                             | (static_cast<uint32_t>(kBM >> 4) << 24);  // M / 16
+constexpr uint32_t kIdescBmn = kIdesc | (1u << 16);
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate,
+                                          uint32_t idesc = kIdesc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -433,6 +452,17 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
           }
         }
       };
+      // the stage's W slice: one [256 x 64] box, or with W stored [H x V] four [64 x 64]
+      // boxes (64 vocabulary columns x 64 hidden rows each)
+      auto load_b = [&](int s, int kb_, int n_) {
+        if (a.w_hv) {
+#pragma unroll
+          for (int j = 0; j < kBN / 64; ++j)
+            tma_load_2d(sB + s * kStageBytesB + j * kHvBlockBytes, &tmap_b, n_ * kBN + 64 * j, kb_ * kBK, &full[s]);
+        } else {
+          tma_load_2d(sB + s * kStageBytesB, &tmap_b, kb_ * kBK, n_ * kBN, &full[s]);
+        }
+      };
       start_unit();
       int pm[S], pk[S];
       int np = 0;
@@ -442,7 +472,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
           pm[j] = m_tile;
           pk[j] = kb;
           mbar_arrive_expect_tx(&full[j], a.a_bytes + kStageBytesB);
-          tma_load_2d(sB + j * kStageBytesB, &tmap_b, kb * kBK, n * kBN, &full[j]);
+          load_b(j, kb, n);
           advance();
           np = j + 1;
         }
@@ -466,7 +496,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         if (!wait_or_abort(&empty[s], ph ^ 1u, abort_flag, a.dev_status)) break;
         mbar_arrive_expect_tx(&full[s], a.a_bytes + kStageBytesB);
         load_a(s, kb, m_tile);
-        tma_load_2d(sB + s * kStageBytesB, &tmap_b, kb * kBK, n * kBN, &full[s]);
+        load_b(s, kb, n);
         advance();
         if (++s == S) {
           s = 0;
@@ -504,8 +534,13 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
               const uint64_t ad = sw128_kmajor_desc(a_addr + kk * kUmmaK * 2);
-              const uint64_t bd = sw128_kmajor_desc(b_addr + kk * kUmmaK * 2);
-              umma_bf16(d_tmem, ad, bd, (kb > 0 || kk > 0) ? 1u : 0u);
+              if (a.w_hv) {  // W stored [H x V]: the slice is vocabulary-major
+                const uint64_t bd = sw128_mnmajor_desc(b_addr + kk * kUmmaK * 128);
+                umma_bf16(d_tmem, ad, bd, (kb > 0 || kk > 0) ? 1u : 0u, kIdescBmn);
+              } else {
+                const uint64_t bd = sw128_kmajor_desc(b_addr + kk * kUmmaK * 2);
+                umma_bf16(d_tmem, ad, bd, (kb > 0 || kk > 0) ? 1u : 0u);
+              }
             }
             umma_commit(&empty[s]);
             if (++s == S) {

@@ -249,7 +249,8 @@ static lmh_status project_impl(const void* hidden, int64_t hidden_row_stride, in
     return LMH_ERR_INVALID_ARG;
   if (hidden_row_stride < H) return LMH_ERR_INVALID_ARG;
   if (!row_idx && rows > num_tokens) return LMH_ERR_INVALID_ARG;
-  if (w_layout == LMH_W_HV) return LMH_ERR_UNSUPPORTED;
+  // W [H x V] rows are V elements: the tensor map wants them a multiple of 16 bytes
+  if (w_layout == LMH_W_HV && (V % 8) != 0) return LMH_ERR_UNSUPPORTED;
   if ((H % 8) != 0 || !aligned(hidden, 16) || !aligned(W, 16) || (logits_out && !aligned(logits_out, 16)))
     return LMH_ERR_UNSUPPORTED;
   if (rows == 0) return LMH_OK;
@@ -279,7 +280,7 @@ static lmh_status project_impl(const void* hidden, int64_t hidden_row_stride, in
   if (e == cudaSuccess) {
     Traced tr(kTraceHead, stream);
     e = launch_head(A, a_stride, rows, H, W, V, plan, sel_ids, row_k, k_max, parts, z_out, dev_status, stream,
-                    /*pdl=*/gather, one_split ? &outs : nullptr, logit_scale, samp);
+                    /*pdl=*/gather, one_split ? &outs : nullptr, logit_scale, samp, w_layout == LMH_W_HV);
   }
   if (e == cudaSuccess && !one_split) {
     Traced tr(kTraceMerge, stream);

@@ -126,7 +126,7 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
                         const HeadPlan& plan, const int32_t* sel, const int32_t* row_k, int k_max,
                         Partials parts, float* logits_out, uint32_t* dev_status, cudaStream_t stream,
                         bool pdl = false, const RowOutputs* final_out = nullptr, float logit_scale = 1.0f,
-                        const SampleArgs* samp = nullptr);
+                        const SampleArgs* samp = nullptr, bool w_hv = false);
 
 // Launch `kernel` on `stream`; with pdl = true it carries the programmatic
 // stream serialization attribute, so it may start while its predecessor in the

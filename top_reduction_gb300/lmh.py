@@ -188,10 +188,11 @@ def _workspace(workspace, nbytes, device):
 
 def project_logprobs(hidden, W, row_idx=None, rows=None, sel=None, row_k=None, k_max=0,
                      logits_out=None, workspace=None, dev_status=None, out=None, stream=None, logit_scale=1.0,
-                     sampling=None):
+                     sampling=None, w_layout=W_VH):
     """Selective head projection + per-row lse / selected logprob / top-k.
 
-    hidden: bf16 [T, H] (rows may be strided); W: bf16 [V, H] (lm_head.weight);
+    hidden: bf16 [T, H] (rows may be strided); W: bf16 [V, H] (lm_head.weight), or
+    [H, V] with w_layout=W_HV (V a multiple of 8);
     row_idx: int32 [rows] device tensor or None (rows 0..rows-1).
     logit_scale: head transform, every logit is logit_scale * (A . W)
     (lmh_project_logprobs_scaled); 1.0 is the plain projection.
@@ -204,8 +205,9 @@ def project_logprobs(hidden, W, row_idx=None, rows=None, sel=None, row_k=None, k
     assert hidden.stride(1) == 1
     assert W.is_cuda and W.dtype == torch.bfloat16 and W.dim() == 2 and W.is_contiguous()
     T, H = hidden.shape
-    V = W.shape[0]
-    assert W.shape[1] == H
+    assert w_layout in (W_VH, W_HV)
+    V = W.shape[0] if w_layout == W_VH else W.shape[1]
+    assert W.shape[1 if w_layout == W_VH else 0] == H
     dev = hidden.device
     if row_idx is not None:
         rows = row_idx.numel() if rows is None else rows
@@ -216,7 +218,7 @@ def project_logprobs(hidden, W, row_idx=None, rows=None, sel=None, row_k=None, k
     rk_t = _dev_i32(row_k, dev, rows, "row_k")
     o = out if out is not None else _outputs(rows, k_max, sel_t is not None, dev, V)
     ws = _workspace(workspace, workspace_bytes(rows, H, V, k_max, PATH_PROJECT), dev)
-    args = (_p(hidden), hidden.stride(0) if T > 1 else H, T, _p(row_idx), int(rows), H, _p(W), W_VH, V,
+    args = (_p(hidden), hidden.stride(0) if T > 1 else H, T, _p(row_idx), int(rows), H, _p(W), int(w_layout), V,
             _p(sel_t), _p(rk_t), int(k_max), _p(o["lse"]), _p(o["sel_logprob"]), _p(o["topk_ids"]),
             _p(o["topk_logprobs"]), _p(logits_out), _p(ws), ws.numel() * ws.element_size(), _p(dev_status))
     if sampling is not None:
