@@ -5,7 +5,7 @@ deep ring, the column split, plain row tiles and several row tiles), H (a multip
 V (ragged), K (0..40, per-row K on some cases), a logit scale and, on some cases,
 sampling with a mask and mixed temperatures.  Everything must match the oracle as the
 targeted tests require: lse and logprobs within 2e-2, ids exact or certified near-ties,
-draws exact or certified near-ties."""
+draws exact or certified near-ties.  A quarter of the head cases store W as [H x V]."""
 import numpy as np
 import pytest
 import torch
@@ -31,6 +31,10 @@ def test_random_head_configurations(lmh, case):
     if sampled:
         scale = 1.0  # the draw's near-tie bound is stated for unscaled logits
     with_row_k = bool(rng.random() < 0.3) and k > 0
+    hv = bool(rng.random() < 0.25)  # W stored [H x V]: V a multiple of 8
+    if hv:
+        V = max(8, V // 8 * 8)
+        k = min(k, V)
     g = torch.Generator().manual_seed(case)
     T = rows + 4
     hidden = torch.randn(T, H, generator=g).to(torch.bfloat16)
@@ -46,18 +50,19 @@ def test_random_head_configurations(lmh, case):
         sampling = {"temperature": temp, "seed": 77 + case, "offsets": offsets,
                     "mask": None if mask is None else mask.view(np.int32)}
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    o = lmh.project_logprobs(hidden.cuda(), W.cuda(), row_idx=ri.cuda(), sel=sel,
+    from top_reduction_gb300 import lmh as L
+    W_arg = W.t().contiguous() if hv else W
+    o = lmh.project_logprobs(hidden.cuda(), W_arg.cuda(), row_idx=ri.cuda(), sel=sel,
                              row_k=None if row_k is None else row_k.cuda(), k_max=k, dev_status=st,
-                             logit_scale=scale, sampling=sampling)
+                             logit_scale=scale, sampling=sampling, w_layout=L.W_HV if hv else L.W_VH)
     torch.cuda.synchronize()
     status = int(st.item())
-    from top_reduction_gb300 import lmh as L
     assert status & ~L.DS_NO_ALLOWED_TOKEN == 0, status
     z = oracle.project(_bits(hidden), _bits(W), row_idx=ri.numpy()) * scale
     rk = None if row_k is None else row_k.numpy()
     orc = oracle.logprobs(z, sel=sel.numpy(), row_k=rk, k_max=k)
     A = hidden[ri.long()].float().double().numpy()
-    what = "case %d %s" % (case, (rows, H, V, k, scale, sampled, with_row_k))
+    what = "case %d %s" % (case, (rows, H, V, k, scale, sampled, with_row_k, hv))
     check_fused(o, orc, z, A, W, k, row_k=rk, what=what, scale=scale)
     if sampled:
         check_draws(o["sampled_ids"].cpu().numpy(), o["sampled_logprob"].cpu().numpy(), z, orc["lse"],

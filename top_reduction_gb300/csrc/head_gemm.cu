@@ -9,14 +9,18 @@
 // finite k the [rows x vocab] logits are never written to memory.
 
 #include <mutex>
+#include <type_traits>
 
 #include "head_kernel.cuh"
 
 namespace lmh {
 
-LMH_HEAD_MODE_DECL(extern, kSampNone)
-LMH_HEAD_MODE_DECL(extern, kSampAll)
-LMH_HEAD_MODE_DECL(extern, kSampFiltered)
+LMH_HEAD_MODE_DECL(extern, kSampNone, false)
+LMH_HEAD_MODE_DECL(extern, kSampAll, false)
+LMH_HEAD_MODE_DECL(extern, kSampFiltered, false)
+LMH_HEAD_MODE_DECL(extern, kSampNone, true)
+LMH_HEAD_MODE_DECL(extern, kSampAll, true)
+LMH_HEAD_MODE_DECL(extern, kSampFiltered, true)
 
 // ---------------------------------------------------------------------------
 // row gather (K2): out[i, :] = hidden[row_idx[i], :]
@@ -122,9 +126,12 @@ static cudaError_t make_tmap(CUtensorMap* map, const void* base, uint64_t inner,
 }
 
 cudaError_t head_setup() {
-  cudaError_t e = head_attr_mode<kSampNone>();
-  if (e == cudaSuccess) e = head_attr_mode<kSampAll>();
-  if (e == cudaSuccess) e = head_attr_mode<kSampFiltered>();
+  cudaError_t e = head_attr_mode<kSampNone, false>();
+  if (e == cudaSuccess) e = head_attr_mode<kSampAll, false>();
+  if (e == cudaSuccess) e = head_attr_mode<kSampFiltered, false>();
+  if (e == cudaSuccess) e = head_attr_mode<kSampNone, true>();
+  if (e == cudaSuccess) e = head_attr_mode<kSampAll, true>();
+  if (e == cudaSuccess) e = head_attr_mode<kSampFiltered, true>();
   return e;
 }
 
@@ -164,7 +171,6 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   }
   const bool deep = !sampling && a.rep == 1 && rows <= 32 && plan.kcap <= 32;
   a.a_bytes = static_cast<uint32_t>(a.rep) * a_box * kBK * 2;
-  a.w_hv = w_hv ? 1 : 0;
   a.rows = rows;
   a.H = H;
   a.V = V;
@@ -186,7 +192,13 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   a.out = final_out ? *final_out : RowOutputs{nullptr, nullptr, nullptr, nullptr};
   const dim3 grid(plan.grid);
   const bool mat = logits_out != nullptr;
-  if (!a.samp.enabled) return launch_head_mode<kSampNone>(plan.kcap, mat, deep, grid, stream, pdl, ta, tb, a);
+  // the kernels for each weight layout: [V x H] (kHV false) or [H x V] (kHV true)
+  auto launch = [&](auto mode, bool deep_) {
+    constexpr int M = decltype(mode)::value;
+    return w_hv ? launch_head_mode<M, true>(plan.kcap, mat, deep_, grid, stream, pdl, ta, tb, a)
+                : launch_head_mode<M, false>(plan.kcap, mat, deep_, grid, stream, pdl, ta, tb, a);
+  };
+  if (!a.samp.enabled) return launch(std::integral_constant<int, kSampNone>{}, deep);
   // Sampling: the candidate filter pays off when a warp's rows see long vocabulary
   // ranges (its test tightens as the row's best score grows) or when few lanes hold
   // rows (a block's second pass runs for the lanes that have candidates); otherwise
@@ -196,8 +208,8 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   const int lanes = plan.m_tiles == 1 ? (rows < 32 ? rows : 32) : 32;
   const int blocks_per_unit = plan.tiles_per_split * (kBN / 64) / a.rep;
   if (lanes <= 16 || blocks_per_unit >= 64)
-    return launch_head_mode<kSampFiltered>(plan.kcap, mat, false, grid, stream, pdl, ta, tb, a);
-  return launch_head_mode<kSampAll>(plan.kcap, mat, false, grid, stream, pdl, ta, tb, a);
+    return launch(std::integral_constant<int, kSampFiltered>{}, false);
+  return launch(std::integral_constant<int, kSampAll>{}, false);
 }
 
 }  // namespace lmh

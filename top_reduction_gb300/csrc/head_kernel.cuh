@@ -89,7 +89,6 @@ struct HeadArgs {
   // quarter has the rows and epilogue warp q (copy q / rep_nq) reduces only
   // the 64-column blocks c == copy (mod rep) of each tile.  rep 1: off.
   int rep, rep_nq;
-  int w_hv;  // W stored [H x V] (vocabulary contiguous): 4 boxes of 64 columns per W slice, MN-major MMA operand
   float logit_scale;  // head transform: every logit is logit_scale * (A . W) (1: none)
   SampleArgs samp;    // device-side sampling (kernels with kSamp != 0)
   int final_out;   // one vocabulary split: write the final results (out), not partials
@@ -369,7 +368,9 @@ __device__ __forceinline__ uint32_t noise_word_limit(float t) {
 // (kSampAll) or only the tokens whose Philox word passes the candidate test (kSampFiltered).
 constexpr int kSampNone = 0, kSampAll = 1, kSampFiltered = 2;
 
-template <int KCAP, bool kMaterialize, int kSamp, bool kDeep = false>
+// kHV: W stored [H x V] (vocabulary contiguous): 4 boxes of 64 columns per W slice and a
+// vocabulary-major (MN-major) MMA operand.
+template <int KCAP, bool kMaterialize, int kSamp, bool kDeep = false, bool kHV = false>
 __global__ void __launch_bounds__(kHeadThreads, 1)
     head_logprobs_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const HeadArgs a) {
@@ -455,7 +456,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
       // the stage's W slice: one [256 x 64] box, or with W stored [H x V] four [64 x 64]
       // boxes (64 vocabulary columns x 64 hidden rows each)
       auto load_b = [&](int s, int kb_, int n_) {
-        if (a.w_hv) {
+        if constexpr (kHV) {
 #pragma unroll
           for (int j = 0; j < kBN / 64; ++j)
             tma_load_2d(sB + s * kStageBytesB + j * kHvBlockBytes, &tmap_b, n_ * kBN + 64 * j, kb_ * kBK, &full[s]);
@@ -534,7 +535,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
               const uint64_t ad = sw128_kmajor_desc(a_addr + kk * kUmmaK * 2);
-              if (a.w_hv) {  // W stored [H x V]: the slice is vocabulary-major
+              if constexpr (kHV) {  // W stored [H x V]: the slice is vocabulary-major
                 const uint64_t bd = sw128_mnmajor_desc(b_addr + kk * kUmmaK * 128);
                 umma_bf16(d_tmem, ad, bd, (kb > 0 || kk > 0) ? 1u : 0u, kIdescBmn);
               } else {
@@ -927,15 +928,15 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
 // ---------------------------------------------------------------------------
 // per-mode entry points (instantiated in head_inst_*.cu)
 // ---------------------------------------------------------------------------
-template <int kSamp>
+template <int kSamp, bool kHV>
 cudaError_t head_attr_mode() {
   cudaError_t e = cudaSuccess;
   auto set = [&](auto kernel, size_t smem) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   };
 #define LMH_HEAD_ATTR(KC)                                                      \
-  set(head_logprobs_kernel<KC, false, kSamp>, HeadCfg<KC>::kSmem);             \
-  set(head_logprobs_kernel<KC, true, kSamp>, HeadCfg<KC>::kSmem);
+  set(head_logprobs_kernel<KC, false, kSamp, false, kHV>, HeadCfg<KC>::kSmem); \
+  set(head_logprobs_kernel<KC, true, kSamp, false, kHV>, HeadCfg<KC>::kSmem);
   LMH_HEAD_ATTR(1)
   LMH_HEAD_ATTR(5)
   LMH_HEAD_ATTR(8)
@@ -946,8 +947,8 @@ cudaError_t head_attr_mode() {
 #undef LMH_HEAD_ATTR
   if constexpr (kSamp == kSampNone) {
 #define LMH_HEAD_ATTR_DEEP(KC)                                                 \
-  set(head_logprobs_kernel<KC, false, kSamp, true>, HeadCfg<KC, true>::kSmem); \
-  set(head_logprobs_kernel<KC, true, kSamp, true>, HeadCfg<KC, true>::kSmem);
+  set(head_logprobs_kernel<KC, false, kSamp, true, kHV>, HeadCfg<KC, true>::kSmem); \
+  set(head_logprobs_kernel<KC, true, kSamp, true, kHV>, HeadCfg<KC, true>::kSmem);
     LMH_HEAD_ATTR_DEEP(1)
     LMH_HEAD_ATTR_DEEP(5)
     LMH_HEAD_ATTR_DEEP(8)
@@ -959,7 +960,7 @@ cudaError_t head_attr_mode() {
   return e;
 }
 
-template <int kSamp>
+template <int kSamp, bool kHV>
 cudaError_t launch_head_mode(int kcap, bool materialize, bool deep, dim3 grid, cudaStream_t stream, bool pdl,
                              const CUtensorMap& ta, const CUtensorMap& tb, const HeadArgs& a) {
   const dim3 block(kHeadThreads);
@@ -968,9 +969,9 @@ cudaError_t launch_head_mode(int kcap, bool materialize, bool deep, dim3 grid, c
       switch (kcap) {
 #define LMH_HEAD_CASE_DEEP(KC)                                                                                   \
   case KC:                                                                                                       \
-    return materialize ? launch_kernel(head_logprobs_kernel<KC, true, kSamp, true>, grid, block,                 \
+    return materialize ? launch_kernel(head_logprobs_kernel<KC, true, kSamp, true, kHV>, grid, block,            \
                                        HeadCfg<KC, true>::kSmem, stream, pdl, ta, tb, a)                         \
-                       : launch_kernel(head_logprobs_kernel<KC, false, kSamp, true>, grid, block,                \
+                       : launch_kernel(head_logprobs_kernel<KC, false, kSamp, true, kHV>, grid, block,           \
                                        HeadCfg<KC, true>::kSmem, stream, pdl, ta, tb, a);
         LMH_HEAD_CASE_DEEP(1)
         LMH_HEAD_CASE_DEEP(5)
@@ -989,10 +990,10 @@ cudaError_t launch_head_mode(int kcap, bool materialize, bool deep, dim3 grid, c
   switch (kcap) {
 #define LMH_HEAD_CASE(KC)                                                                                      \
   case KC:                                                                                                     \
-    return materialize ? launch_kernel(head_logprobs_kernel<KC, true, kSamp>, grid, block, HeadCfg<KC>::kSmem, \
-                                       stream, pdl, ta, tb, a)                                                 \
-                       : launch_kernel(head_logprobs_kernel<KC, false, kSamp>, grid, block, HeadCfg<KC>::kSmem, \
-                                       stream, pdl, ta, tb, a);
+    return materialize ? launch_kernel(head_logprobs_kernel<KC, true, kSamp, false, kHV>, grid, block,          \
+                                       HeadCfg<KC>::kSmem, stream, pdl, ta, tb, a)                             \
+                       : launch_kernel(head_logprobs_kernel<KC, false, kSamp, false, kHV>, grid, block,         \
+                                       HeadCfg<KC>::kSmem, stream, pdl, ta, tb, a);
     LMH_HEAD_CASE(1)
     LMH_HEAD_CASE(5)
     LMH_HEAD_CASE(8)
@@ -1006,9 +1007,9 @@ cudaError_t launch_head_mode(int kcap, bool materialize, bool deep, dim3 grid, c
   }
 }
 
-#define LMH_HEAD_MODE_DECL(EXT, MODE)                                                                           \
-  EXT template cudaError_t head_attr_mode<MODE>();                                                              \
-  EXT template cudaError_t launch_head_mode<MODE>(int, bool, bool, dim3, cudaStream_t, bool, const CUtensorMap&, \
-                                                  const CUtensorMap&, const HeadArgs&);
+#define LMH_HEAD_MODE_DECL(EXT, MODE, HV)                                                                       \
+  EXT template cudaError_t head_attr_mode<MODE, HV>();                                                          \
+  EXT template cudaError_t launch_head_mode<MODE, HV>(int, bool, bool, dim3, cudaStream_t, bool,               \
+                                                      const CUtensorMap&, const CUtensorMap&, const HeadArgs&);
 
 }  // namespace lmh
