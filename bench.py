@@ -1,14 +1,24 @@
-"""Benchmark of the LM-head logprob path: rows/s and the head kernel's roofline.
+"""Benchmark of the LM-head logprob path: rows/s and each dominant kernel's roofline.
 
 One step = one pass of the whole hot path over one batch: lmh_select_rows on
 the batch's cu_seqlens, then lmh_project_logprobs on the selected rows (row
 gather, tcgen05 head GEMM with the fused lse / selected-logprob / top-k
-epilogue, partial merge).  The default workload is the decode batch (32 rows,
-H 2560, V 151936, K 5; synthetic seeded inputs, see workloads.py).  The
-2560 x 151936 bf16 head (778 MB) is larger than L2, so every step streams it
-from HBM.
+epilogue, partial merge); for the prompt-scoring chunk, one
+lmh_logprobs_from_logits call.  A pure-decode batch (every sequence one
+decode row) passes no row indices, as the pages' pure-decode case does: the
+selection is the identity and the head reads the hidden rows in place.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode_batch]
+The headline workload is the mixed serving step (Llama-3-8B head shape: H
+4096, V 128256; 64 decode rows, 4 prefill segments of 512 and one
+1024-position scoring segment: 1092 selected rows), the largest selective
+configuration.  The same JSON line carries a "workloads" object with the
+other configurations (decode batch K 5 and K 1, selective prefill, the
+16384-row full projection arm, the 256 x 248320 logits chunk), each with its
+own value, roofline, CPU baseline and id check.  Inputs are seeded synthetic
+tensors (workloads.py) resident in HBM; every head is larger than L2, so each
+step streams it from HBM, and the chunk rotates four copies.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mixed_batch]
     python bench.py --impl reference ...   # the CPU oracle on the same workload
 
 Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its
@@ -36,16 +46,21 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
+HEADLINE = "mixed_batch"
+SUB_WORKLOADS = ("decode_batch", "decode_batch_k1", "prefill_batch", "prefill_full", "logits_chunk")
+WORKLOADS = (HEADLINE,) + SUB_WORKLOADS
+SUB_TIMED_S = 1.0  # about this much device time per extra workload's timed region
+
+
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=8000)
-    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="decode_batch",
-                   choices=["decode_batch", "decode_batch_k1", "prefill_batch", "prefill_full", "mixed_batch",
-                            "logits_chunk"])
+    p.add_argument("--workload", default=HEADLINE, choices=list(WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-sub", action="store_true", help="only the headline workload (profiling runs)")
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     p.add_argument("--k", type=int, default=None,
@@ -109,6 +124,12 @@ def workload_config(b):
     if b.get("w_hv"):
         cfg["w_layout"] = "[H x V] (vocabulary contiguous)"
     return cfg
+
+
+def pure_decode(b):
+    """Every sequence is one decode row: the selection is the identity and no indices are passed."""
+    return b["name"] != "logits_chunk" and not b.get("full") and int(b["num_decode"]) == b["cu_seqlens"].numel() - 1 \
+        and int(b["n_sel"]) == int(b["hidden"].shape[0])
 
 
 def algorithmic(b):
@@ -267,6 +288,7 @@ class Step:
         self.row_k = None if b["row_k"] is None else b["row_k"].to(device)
         self.k = int(b["k"])
         self.rows = int(b["n_sel"])
+        self.pure = pure_decode(b)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.ws = torch.empty(lmh.workspace_bytes(self.rows, b["H"], b["V"], self.k, lmh.PATH_PROJECT),
                               dtype=torch.uint8, device=device)
@@ -275,18 +297,13 @@ class Step:
     def _outputs(self, rows, k, with_sel):
         return step_outputs(rows, k, int(self.b["V"]), with_sel, self.dev)
 
-    def launches_per_step(self):
-        if self.chunk:
-            return 2
-        return 2 if self.full else 4
-
     def run(self):
         lmh = self.lmh
         if self.chunk:
             x = self.logits[self.i & 3]
             self.i += 1
             return lmh.logprobs_from_logits(x, sel=self.sel, k_max=self.k, workspace=self.ws, out=self.out)
-        if self.full:
+        if self.full or self.pure:
             return lmh.project_logprobs(self.hidden, self.W, sel=self.sel, row_k=self.row_k, k_max=self.k,
                                         workspace=self.ws, out=self.out, dev_status=self.status,
                                         logit_scale=self.scale, sampling=self.sampling, w_layout=self.w_layout)
@@ -332,15 +349,20 @@ def e2e_leg(lmh, b, device, steps):
     Every step copies its inputs host->device (hidden rows, cu_seqlens,
     selected ids; the head weight stays resident like model weights), runs
     the path, copies the compact result device->host and reads it on the
-    host.  Two buffer sets alternate, as in a serving loop, each on its own
-    stream: step i+1 is issued before the host waits for step i's result, so
-    the host's work and step i+1's input copy overlap step i on the GPU.  As
-    a serving loop would, each buffer set's step (the copy in, the API calls
-    and the copy out) is captured once in a CUDA graph and replayed every
-    step; if capture fails the calls run eagerly.
+    host.  As a serving loop would, each step (the copy in, the API calls and
+    the copy out) is captured once in a CUDA graph and replayed every step;
+    if capture fails the calls run eagerly.  Two buffer sets alternate and
+    step i+1 is issued before the host waits for step i's result.
+
+    The value is the loop with both buffer sets on one stream, as an
+    autoregressive loop over one batch runs: each step's GPU work follows the
+    previous step's.  The "pipelined" record repeats it with one stream per
+    buffer set (two independent batches in flight); there two heads run at
+    once and share W's reads in L2, so it is context, not the metric.
     """
     import torch
     chunk = b["name"] == "logits_chunk"
+    pure = pure_decode(b)
     src = {"logits": b["logits"], "sel": b["sel"]} if chunk else \
         {"hidden": b["hidden"], "cu": b["cu_seqlens"], "sel": b["sel"]}
     h_in_buf, h_in = packed(src, "cpu", pinned=True)  # the step's inputs, packed in pinned host memory
@@ -378,7 +400,9 @@ def e2e_leg(lmh, b, device, steps):
             o = lmh.logprobs_from_logits(d_in["logits"], sel=d_in["sel"], k_max=k, workspace=bf["ws"],
                                          out=bf["out"])
         else:
-            ri, _ = lmh.select_rows(d_in["cu"], b["num_decode"], mask, max_out_rows=rows)
+            ri = None
+            if not pure:
+                ri, _ = lmh.select_rows(d_in["cu"], b["num_decode"], mask, max_out_rows=rows)
             o = lmh.project_logprobs(d_in["hidden"], W, row_idx=ri, sel=d_in["sel"], row_k=row_k, k_max=k,
                                      workspace=bf["ws"], out=bf["out"], logit_scale=b.get("logit_scale", 1.0),
                                      w_layout=w_layout)
@@ -425,17 +449,18 @@ def e2e_leg(lmh, b, device, steps):
         read(bufs[(n - 1) % 2])
         return time.perf_counter() - t0
 
-    dt = timed(steps)
-    # The same loop with both buffer sets on one stream: each step's GPU work waits for the
-    # previous step's, as an autoregressive loop over a single batch would.
+    dt_pipe = timed(steps)
+    # the metric: both buffer sets on one stream, each step's GPU work after the previous step's
+    two_streams = bufs[1]["stream"]
     bufs[1]["stream"] = bufs[0]["stream"]
-    dt_serial = timed(steps)
+    dt = timed(steps)
+    bufs[1]["stream"] = two_streams
     return {"value": rows * steps / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": 1e3 * dt / steps,
-            "pipelining": "two independent batches in flight (two buffer sets): step i+1 is issued before "
-                          "step i's result is read; " + mode,
-            "one_stream": {"value": rows * steps / dt_serial, "ms_per_step": 1e3 * dt_serial / steps,
-                           "note": "both buffer sets on one stream: no overlap between steps on the GPU"}}
+            "mode": "one stream, steps back to back; " + mode.replace(", one stream per buffer set", ""),
+            "pipelined": {"value": rows * steps / dt_pipe, "ms_per_step": 1e3 * dt_pipe / steps,
+                          "note": "two buffer sets on two streams: two independent batches in flight, whose "
+                                  "heads share W's reads in L2 (context only)"}}
 
 
 def load_peaks():
@@ -473,17 +498,19 @@ def recorded_traffic(kernel, workload):
 class OracleStep:
     """One step of the oracle, as it stands, on the same workload.
 
-    A step is one batch of selected rows (as many as there are host cores, so
-    the oracle's threads are all busy): row selection, f64 projection and the
+    A step is one batch of selected rows (as many as the oracle has threads,
+    so they are all busy): row selection, f64 projection and the
     full-vocabulary f64 log-softmax + full sort.  Rows cycle through the
-    workload's selected rows.
+    workload's selected rows.  The last step's rows and results are kept for
+    the id check against the GPU's output.
     """
 
-    def __init__(self, b):
+    def __init__(self, b, threads=0):
         import numpy as np
         import oracle
         import workloads
         self.oracle, self.b = oracle, b
+        self.req_threads = int(threads)
         self.cores = oracle.cores()
         if b["name"] == "logits_chunk":
             self.x = workloads.bits(b["logits"])
@@ -495,9 +522,10 @@ class OracleStep:
                 self.ri = np.arange(b["hidden"].shape[0], dtype=np.int32)
             self.hid, self.W = workloads.bits(b["hidden"]), workloads.bits(b["W"])
             self.n = len(self.ri)
-        self.per = max(1, min(self.n, self.cores))
+        self.per = max(1, min(self.n, self.req_threads or self.cores))
         self.pos = 0
-        self.threads = self.cores
+        self.threads = self.req_threads or self.cores
+        self.last = None
 
     def run(self):
         import numpy as np
@@ -505,13 +533,18 @@ class OracleStep:
         idx = (self.pos + np.arange(self.per)) % self.n
         self.pos = (self.pos + self.per) % self.n
         sel = b["sel"].numpy()[idx]
+        k = max(int(b["k"]), 0)
         if b["name"] == "logits_chunk":
-            r = o.logprobs(self.x[idx], dtype=o.BF16, sel=sel, k_max=max(int(b["k"]), 0), return_threads=True)
+            r = o.logprobs(self.x[idx], dtype=o.BF16, sel=sel, k_max=k, threads=self.req_threads,
+                           return_threads=True)
             self.threads = r["threads"]
+            self.last = (idx, r, None)
         else:
             rk = None if b["row_k"] is None else b["row_k"].numpy()[idx]
-            z, self.threads = o.project(self.hid, self.W, row_idx=self.ri[idx], return_threads=True)
-            o.logprobs(z, sel=sel, row_k=rk, k_max=max(int(b["k"]), 0))
+            z, self.threads = o.project(self.hid, self.W, row_idx=self.ri[idx], threads=self.req_threads,
+                                        return_threads=True)
+            r = o.logprobs(z, sel=sel, row_k=rk, k_max=k, threads=self.req_threads)
+            self.last = (idx, r, z)
         return self.per
 
     def describe(self):
@@ -521,17 +554,154 @@ class OracleStep:
         return "%d %s of %s per step" % (self.per, what, self.b["name"])
 
 
-def cpu_baseline(b, budget_s=12.0):
-    """The oracle on a bounded sample of the workload (about budget_s seconds of work)."""
+class IdCheck:
+    """The GPU's top-k ids against the oracle's on the rows the oracle scored.
+
+    From given logits the ids must be identical (the logits widen exactly).
+    For the fused head a differing rank counts as a certified near-tie swap
+    only when the oracle's values at the two ids differ by at most 2 * delta,
+    delta = gamma_H * sum_h |A_h * W_hv| (the fp32 dot-product bound, gamma_H
+    = H u / (1 - H u), u = 2^-24); anything else is an uncertified mismatch.
+    The named workloads expect 0 of both.
+    """
+
+    def __init__(self, b, gpu_ids):
+        self.b, self.ids = b, gpu_ids
+        self.rows = self.ranks = self.mismatched = self.certified = 0
+        self.max_gap = 0.0  # the largest oracle gap |z_gpu_id - z_oracle_id| among certified swaps
+
+    def add(self, st):
+        import numpy as np
+        if self.ids is None or st.last is None:
+            return
+        idx, orc, z = st.last
+        b = self.b
+        k_max = max(int(b["k"]), 0)
+        if k_max == 0:
+            return
+        ks = np.full(len(idx), k_max) if b.get("row_k") is None else np.clip(b["row_k"].numpy()[idx], 0, k_max)
+        for j, r in enumerate(idx):
+            k = int(ks[j])
+            g, o = self.ids[r, :k], orc["topk_ids"][j, :k]
+            self.rows += 1
+            self.ranks += k
+            for q in np.nonzero(g != o)[0]:
+                self.mismatched += 1
+                if z is None or g[q] < 0:
+                    continue
+                H = int(b["H"])
+                u = 2.0 ** -24
+                gamma = H * u / (1 - H * u)
+                a = b["hidden"][int(st.ri[r])].float().double().numpy()
+                Wc = b["W"][[int(g[q]), int(o[q])]].float().double().numpy()
+                delta = b.get("logit_scale", 1.0) * gamma * np.abs(Wc * a[None, :]).sum(axis=1).max()
+                gap = abs(z[j, g[q]] - z[j, o[q]])
+                if gap <= 2 * delta:
+                    self.certified += 1
+                    self.max_gap = max(self.max_gap, float(gap))
+
+    def summary(self):
+        return {"rows_checked": self.rows, "ranks_checked": self.ranks, "certified_swaps": self.certified,
+                "max_certified_gap": self.max_gap, "uncertified_mismatches": self.mismatched - self.certified}
+
+
+def cpu_baseline(b, budget_s=12.0, single_s=4.0, gpu_ids=None):
+    """The oracle on a bounded sample of the workload: about budget_s seconds on every
+    host core, then about single_s seconds on one thread.  The rows it scores also
+    check the GPU's ids (IdCheck)."""
+    chk = IdCheck(b, gpu_ids)
+
+    def timed(st, budget):
+        t0 = time.perf_counter()
+        rows, steps = 0, 0
+        while steps == 0 or time.perf_counter() - t0 < budget:
+            rows += st.run()
+            steps += 1
+            chk.add(st)
+        return rows, steps, time.perf_counter() - t0
+
     st = OracleStep(b)
-    t0 = time.perf_counter()
-    rows, steps = 0, 0
-    while steps == 0 or time.perf_counter() - t0 < budget_s:
-        rows += st.run()
-        steps += 1
-    dt = time.perf_counter() - t0
+    rows, steps, dt = timed(st, budget_s)
+    one = OracleStep(b, threads=1)
+    rows1, steps1, dt1 = timed(one, single_s)
     return {"value": rows / dt, "unit": UNIT, "cores": int(st.threads), "kind": "oracle",
-            "sample": "%d steps of %s (%.1f s)" % (steps, st.describe(), dt)}
+            "sample": "%d steps of %s (%.1f s)" % (steps, st.describe(), dt),
+            "single_thread": {"value": rows1 / dt1, "unit": UNIT, "cores": 1,
+                              "sample": "%d steps of %s (%.1f s)" % (steps1, one.describe(), dt1)},
+            "id_check": chk.summary()}
+
+
+def roofline(b, per_kernel, ms_per_step, peaks, peak_src):
+    """The dominant kernel's roofline record: algorithmic amount over its traced launch time
+    (for the logits chunk the whole call, counter reset and stream with its fused select,
+    over the step's event time)."""
+    bound, amount, unit = algorithmic(b)
+    kernel = dominant_kernel(b)
+    if b["name"] == "logits_chunk" and b["k"] >= 0:
+        us = 1e3 * ms_per_step
+        kernel_label = "logits_reduce whole call (counters_reset + logits_stream_tma with the fused select)"
+    else:
+        us = per_kernel.get(kernel, {}).get("avg_us")
+        kernel_label = kernel
+    if bound == "hbm":
+        peak = peaks["hbm_gbs"]
+        achieved = amount / (us * 1e-6) / 1e9 if us else None
+    else:
+        peak = peaks["bf16_tflops"]
+        achieved = amount / (us * 1e-6) / 1e12 if us else None
+    roof = {"kernel": kernel_label, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": (achieved / peak) if achieved else None, "peak_source": peak_src + " (burst)",
+            "algorithmic_per_launch": amount, "avg_launch_us": us,
+            "traffic": recorded_traffic(kernel, b["name"])}
+    if bound == "tensor" and achieved:
+        roof["frac_of_sustained"] = achieved / peaks.get("bf16_tflops_sustained", peak)
+    return roof
+
+
+def measure(lmh, b, device, steps, warmup, dist, world, local, retry_clocks):
+    """Warm-up, the timed region (the value), then the same steps traced per kernel."""
+    import torch
+    step = Step(lmh, b, device)
+    for _ in range(max(warmup, 3)):
+        step.run()
+    torch.cuda.synchronize()
+    if steps is None:  # size the region to about SUB_TIMED_S of device time
+        t = timed_region(step, 10, dist, world) / 10
+        steps = int(min(20000, max(20, SUB_TIMED_S * 1e3 / max(t, 1e-3))))
+    # Region 1 (the value): plain launches, no per-kernel events, so consecutive kernels of a
+    # call can overlap their launch through programmatic dependent launch.
+    # Region 2 (the roofline): the same steps with an event pair recorded around every launch
+    # on the launching stream; its per-kernel averages give each kernel's duration.
+    result = None
+    for attempt in range(2 if retry_clocks else 1):
+        with ClockSampler(local) as cs:
+            ms = timed_region(step, steps, dist, world)
+        clocks = cs.summary()
+        result = (ms, clocks)
+        if not rejected(clocks):
+            break
+    ms, clocks = result
+    lmh.trace_reset()
+    lmh.trace_enable(True)
+    ms_traced = timed_region(step, steps, dist, world)
+    lmh.trace_enable(False)
+    launches = 0
+    per_kernel = {}
+    for kname in lmh.lmh.TRACE_KERNELS:
+        n, t = lmh.trace_read(kname)
+        launches += n
+        if n:
+            per_kernel[kname] = {"launches": n, "avg_us": 1e3 * t / n}
+    status = int(step.status.item()) if hasattr(step, "status") else 0
+    if status:
+        raise RuntimeError("device status %#x during the benchmark of %s" % (status, b["name"]))
+    out = step.out
+    gpu_ids = None if out.get("topk_ids") is None else out["topk_ids"].cpu().numpy()
+    return {"step": step, "steps": steps, "ms": ms, "ms_traced": ms_traced, "clocks": clocks,
+            "per_kernel": per_kernel, "launches": launches, "gpu_ids": gpu_ids}
+
+
+_SHARED = {"decode_batch_k1": "decode_batch", "prefill_full": "prefill_batch"}
 
 
 def run_ours(args):
@@ -548,67 +718,58 @@ def run_ours(args):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     _build.build()
-    b = apply_options(make_workload(args.workload, rank), args)
-    step = Step(lmh, b, device)
-    for _ in range(max(args.warmup, 3)):
-        step.run()
-    torch.cuda.synchronize()
-
-    bound, amount, unit = algorithmic(b)
-    kernel = dominant_kernel(b)
-    # Region 1 (the value): plain launches, no per-kernel events, so consecutive kernels of a
-    # call can overlap their launch through programmatic dependent launch.
-    # Region 2 (the roofline): the same steps with an event pair recorded around every launch
-    # on the launching stream; its per-kernel averages give each kernel's duration.
-    result = None
-    for attempt in range(2):
-        with ClockSampler(local) as cs:
-            ms = timed_region(step, args.steps, dist, world)
-        clocks = cs.summary()
-        result = (ms, clocks)
-        if not rejected(clocks):
-            break
-    ms, clocks = result
-    lmh.trace_reset()
-    lmh.trace_enable(True)
-    ms_traced = timed_region(step, args.steps, dist, world)
-    lmh.trace_enable(False)
-    launches = 0
-    per_kernel = {}
-    for kname in lmh.lmh.TRACE_KERNELS:
-        n, t = lmh.trace_read(kname)
-        launches += n
-        if n:
-            per_kernel[kname] = {"launches": n, "avg_us": 1e3 * t / n}
-    status = int(step.status.item()) if hasattr(step, "status") else 0
-    if status:
-        raise RuntimeError("device status %#x during the benchmark" % status)
-
-    value = job_value(step.rows, args.steps, world, ms)
     peaks, peak_src = load_peaks()
-    avg_us = per_kernel.get(kernel, {}).get("avg_us")
-    if bound == "hbm":
-        peak = peaks["hbm_gbs"]
-        achieved = amount / (avg_us * 1e-6) / 1e9 if avg_us else None
-    else:
-        peak = peaks["bf16_tflops_sustained" if args.steps * (avg_us or 0) > 1e6 else "bf16_tflops"]
-        achieved = amount / (avg_us * 1e-6) / 1e12 if avg_us else None
-    roof = {"kernel": kernel, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": (achieved / peak) if achieved else None, "peak_source": peak_src,
-            "algorithmic_per_launch": amount, "avg_launch_us": avg_us,
-            "traffic": recorded_traffic(kernel, b["name"])}
+
+    b = apply_options(make_workload(args.workload, rank), args)
+    m = measure(lmh, b, device, args.steps, args.warmup, dist, world, local, retry_clocks=True)
+    value = job_value(m["step"].rows, args.steps, world, m["ms"])
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": m["ms"] / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(b), "roofline": roof, "kernels": per_kernel,
-            "traced_ms_per_step": ms_traced / args.steps,
+            "config": workload_config(b),
+            "roofline": roofline(b, m["per_kernel"], m["ms"] / args.steps, peaks, peak_src),
+            "kernels": m["per_kernel"], "traced_ms_per_step": m["ms_traced"] / args.steps,
             # launches counted by the event trace over the second region, which runs the same steps
-            "gpu_launches": launches, "clocks": clocks}
+            "gpu_launches": m["launches"], "clocks": m["clocks"]}
+    if rank == 0 and not args.no_e2e:
+        line["e2e"] = e2e_leg(lmh, b, device, args.e2e_steps or max(200, min(args.steps, 2000)))
+    head_ids = m["gpu_ids"]
+    del m
+    torch.cuda.empty_cache()
+
+    # the other configurations, one at a time, each on its own inputs
+    subs = {}
+    cache = {}
+    for name in ([] if args.no_sub else [w for w in WORKLOADS if w != args.workload]):
+        base = _SHARED.get(name, name)
+        if base not in cache:
+            cache.clear()
+            cache[base] = make_workload(base, rank)
+        src = cache[base]
+        if name == base:
+            sb = src
+        elif name == "decode_batch_k1":  # the decode batch's tensors at K 1
+            sb = dict(src, name=name, k=1)
+        else:  # the prefill batch's tensors, every packed row through the head
+            sb = dict(src, name="prefill_full", num_decode=0, all_rows_mask=None, full=True,
+                      n_sel=src["hidden"].shape[0], sel=src["sel_all"])
+        sm = measure(lmh, sb, device, None, 10, dist, world, local, retry_clocks=False)
+        rec = {"value": job_value(sm["step"].rows, sm["steps"], world, sm["ms"]), "unit": UNIT,
+               "steps": sm["steps"], "ms_per_step": sm["ms"] / sm["steps"], "config": workload_config(sb),
+               "roofline": roofline(sb, sm["per_kernel"], sm["ms"] / sm["steps"], peaks, peak_src),
+               "kernels": sm["per_kernel"], "gpu_launches": sm["launches"], "clocks": sm["clocks"]}
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            rec["cpu_baseline"] = cpu_baseline(sb, budget_s=4.0, single_s=2.0, gpu_ids=sm["gpu_ids"])
+            rec["certified_swaps"] = rec["cpu_baseline"]["id_check"]["certified_swaps"]
+        subs[name] = rec
+        del sm
+        torch.cuda.empty_cache()
+    if subs:
+        line["workloads"] = subs
     if rank == 0:
-        if not args.no_e2e:
-            line["e2e"] = e2e_leg(lmh, b, device, args.e2e_steps or max(200, min(args.steps, 2000)))
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(b)
+            line["cpu_baseline"] = cpu_baseline(b, gpu_ids=head_ids)
+            line["certified_swaps"] = line["cpu_baseline"]["id_check"]["certified_swaps"]
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()

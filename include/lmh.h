@@ -14,6 +14,9 @@
  *   3. lmh_logprobs_from_logits the same reduction for logits that already
  *                               exist (prompt scoring of logits chunks).
  *
+ * lmh_project_partials and lmh_merge_records split step 2 over GPUs that each
+ * hold a share of the vocabulary (a vocabulary-parallel head).
+ *
  * The O(k+1) result of a row is: lse (fp32 log-sum-exp over the vocabulary),
  * the selected token's logprob, and the exact top-k (ids and logprobs),
  * sorted by logit descending with exact ties ordered by ascending token id.
@@ -344,8 +347,11 @@ lmh_status lmh_logprobs_from_logits(const void* logits, lmh_dtype dtype, int32_t
  * Arguments, results and errors are those of lmh_logprobs_from_logits,
  * minus workspace/workspace_bytes, with two differences:
  * - sizes whose partials need more than the 8 MiB are rejected with
- *   LMH_ERR_WORKSPACE_TOO_SMALL, and nothing is launched.  For example,
- *   256 rows x 248320 at k_max 128 needs about 0.8 MB and fits.
+ *   LMH_ERR_WORKSPACE_TOO_SMALL, and nothing is launched.  The partials take
+ *   about rows * (4 * ceil(V / 64) + 8 * slots + 8) bytes, with slots =
+ *   4 * ceil(ceil(V / 64) / 64) (whatever k_max and dtype): 256 rows x
+ *   248320 need about 4.5 MB and fit; the largest batch is 479 rows at
+ *   V = 248320 and 782 rows at V = 151936.
  * - the first call on each device does a one-time set-up with that device
  *   current: kernel attributes, and the array's device address via
  *   cudaGetSymbolAddress.  Make that first call before any stream capture.
@@ -359,6 +365,75 @@ lmh_status lmh_logprobs_from_logits_static(const void* logits, lmh_dtype dtype, 
                                            float* sel_logprob, int32_t* topk_ids,
                                            float* topk_logprobs, uint32_t* dev_status,
                                            cudaStream_t stream);
+
+/*
+ * Vocabulary-parallel head: several GPUs, each holding a share of the head's
+ * vocabulary, together compute the same O(k+1) result as lmh_project_logprobs.
+ *
+ * Defined by openinfer issue #719, "Suggested direction" (a numerically sound
+ * multi-stage reduction: per-part max and sum of exponentials combine exactly
+ * into the log-sum-exp) and MTPLX PR #532, "Change" (the exact top-k of a row
+ * lies among the union of the parts' own top-k lists; exact ties by ascending
+ * token id).  Each rank calls lmh_project_partials on its share, the ranks
+ * all-gather their records (any collective that concatenates equal-sized byte
+ * buffers in rank order, e.g. an NCCL all-gather into the caller's device
+ * memory), and every rank (or one) calls lmh_merge_records on the gathered
+ * buffer.  The library itself makes no collective call.
+ *
+ * A record is lmh_record_bytes(k_max) bytes per row, 8-byte aligned:
+ *   float m            the share's largest logit of the row (-inf: none)
+ *   float s            sum over the share of exp(logit - m)
+ *   float sel_logit    the selected token's logit, when it lies in the share
+ *   uint32 flags       bit 0: sel_logit is set
+ *   uint64 keys[k_max] the share's best k entries, best first: a key is
+ *                      (order-preserving bits of the fp32 logit << 32) |
+ *                      ~token_id, with global token ids; 0 = no entry.
+ */
+size_t lmh_record_bytes(int32_t k_max);
+
+/*
+ * lmh_project_partials -- one share of a vocabulary-parallel head.
+ *
+ * As lmh_project_logprobs (same hidden / row_idx / rows / H / sel_ids /
+ * row_k / k_max meanings, the same fp32 accumulation and the same per-row
+ * reduction), over the share's tokens [v_begin, v_begin + v_count) only:
+ *   W_share    device bf16 [v_count x H], rows v_begin.. of lm_head.weight
+ *              (LMH_W_VH; other layouts: LMH_ERR_UNSUPPORTED).
+ *   V          the full vocabulary (sel_ids and returned ids are global).
+ *   records    device [rows] records (lmh_record_bytes(k_max) each), out.
+ *   workspace  >= lmh_workspace_bytes(rows, H, v_count, k_max, LMH_PATH_PROJECT).
+ * k_max in [0, LMH_K_MAX] and <= v_count.  No logits are written.
+ * Errors: as lmh_project_logprobs; LMH_ERR_INVALID_ARG also when the share is
+ * empty or leaves [0, V).
+ */
+lmh_status lmh_project_partials(const void* hidden, int64_t hidden_row_stride, int32_t num_tokens,
+                                const int32_t* row_idx, int32_t rows, int32_t H, const void* W_share,
+                                lmh_w_layout w_layout, int32_t v_begin, int32_t v_count, int32_t V,
+                                const int32_t* sel_ids, const int32_t* row_k, int32_t k_max, void* records,
+                                void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                cudaStream_t stream);
+
+/* Workspace of lmh_merge_records (bytes; 0 for invalid arguments). */
+size_t lmh_merge_workspace_bytes(int32_t rows, int32_t num_parts, int32_t k_max);
+
+/*
+ * lmh_merge_records -- the rows' final results from the gathered records.
+ *
+ *   records     device [num_parts][rows] records, part p's rows contiguous
+ *               (the layout of an all-gather of each rank's record buffer).
+ *               The parts' shares must partition [0, V).
+ *   V, sel_ids, row_k, k_max, lse, sel_logprob, topk_ids, topk_logprobs:
+ *               as for lmh_project_logprobs (k_max must equal the k_max the
+ *               records were made with).
+ *   workspace   >= lmh_merge_workspace_bytes(rows, num_parts, k_max).
+ * lse = M + log(sum_p s_p exp(m_p - M)), M = max_p m_p; the top-k is the best
+ * k keys of the parts' lists; logprob = logit - lse.
+ * Errors: as lmh_project_logprobs.
+ */
+lmh_status lmh_merge_records(const void* records, int32_t num_parts, int32_t rows, int32_t V,
+                             const int32_t* sel_ids, const int32_t* row_k, int32_t k_max, float* lse,
+                             float* sel_logprob, int32_t* topk_ids, float* topk_logprobs, void* workspace,
+                             size_t workspace_bytes, uint32_t* dev_status, cudaStream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* lmh_status_string(lmh_status status);
@@ -375,8 +450,10 @@ int32_t lmh_version(void);
  * lmh_trace_read waits for the recorded events, then reports the launches
  * and total milliseconds of the named kernel ("select_rows", "gather_rows",
  * "head_logprobs", "merge_partials", "logits_reduce" (the streaming pass of
- * lmh_logprobs_from_logits), "logits_select" (its per-row selection),
- * "ticket_reset" (the chunk-counter reset before the streaming pass),
+ * lmh_logprobs_from_logits; with 16-byte aligned rows it also selects every
+ * row), "logits_select" (the per-row selection after the plain-load pass),
+ * "counters_reset" (the reset of the chunk and row counters before the
+ * streaming pass),
  * "full_logprobs" (the pass that writes the k_max = LMH_K_FULL output)) since
  * the last reset.
  * lmh_trace_reset clears the totals.
@@ -384,6 +461,22 @@ int32_t lmh_version(void);
 lmh_status lmh_trace_enable(int32_t enable);
 lmh_status lmh_trace_read(const char* kernel, int64_t* launches, double* total_ms);
 void lmh_trace_reset(void);
+
+/*
+ * lmh_debug_set_wait_limit -- test hook for the timeout path; not for
+ * production use.  The pages have no counterpart.
+ *
+ * Inside a kernel, every wait on another role of the same CTA (a shared-memory
+ * stage, an accumulator, a chunk) gives up after this limit: the kernel sets
+ * LMH_DS_TIMEOUT in *dev_status, stops its loops, lets its copies and tensor-
+ * core work in flight finish (those drain waits keep a fixed 2 s limit), frees
+ * its tensor memory and returns, so the context stays usable.  The default is
+ * 2 s, far above any legitimate wait; a test sets a limit shorter than the
+ * latency of one load so that the first wait runs out, then calls with 0 to
+ * restore the default.  The value applies to kernels launched after the call,
+ * from any thread.  Always LMH_OK.
+ */
+lmh_status lmh_debug_set_wait_limit(uint64_t limit_ns);
 
 #ifdef __cplusplus
 }

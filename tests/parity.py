@@ -10,7 +10,13 @@ Acceptance (stated once, used by every parity test):
     delta = gamma_H * sum_h |A[h] * W[h][v]| and gamma_H = H*u/(1 - H*u),
     u = 2^-24 (the fp32 dot-product error bound, Higham, "Accuracy and
     Stability of Numerical Algorithms", section 3.1): such a swap is a
-    certified near-tie and is counted, any other mismatch fails.
+    certified near-tie and is counted, any other mismatch fails.  The named
+    workloads (tiny, decode, selective prefill, mixed step, full arm) assert
+    that the count is 0: their smallest adjacent top-k gaps are far above the
+    fp32 accumulation error, so a correct kernel reproduces the ids exactly.
+    With a head transform (logit scale s != 1) the kernel rounds s * z once
+    more, so the window there also takes 2^-23 * |z| (one fp32 rounding of the
+    product).
 """
 import numpy as np
 
@@ -119,7 +125,9 @@ def check_fused(gpu, orc, z_oracle, A_f64, W_bf16_vh, k_max, row_k=None, atol=TO
             cols = np.array([g[r], o[r]])
             Wc = W_bf16_vh[cols].float().double().numpy()
             zmax = max(abs(z_oracle[i, g[r]]), abs(z_oracle[i, o[r]]))
-            d = scale * higham_delta(A_f64[i], Wc).max() + 2.0 ** -23 * zmax
+            d = scale * higham_delta(A_f64[i], Wc).max()
+            if scale != 1.0:  # the epilogue's product scale * z is rounded once more
+                d += 2.0 ** -23 * zmax
             gap = abs(z_oracle[i, g[r]] - z_oracle[i, o[r]])
             if gap > 2 * d:
                 raise AssertionError(

@@ -63,7 +63,8 @@ def test_random_head_configurations(lmh, case):
     orc = oracle.logprobs(z, sel=sel.numpy(), row_k=rk, k_max=k)
     A = hidden[ri.long()].float().double().numpy()
     what = "case %d %s" % (case, (rows, H, V, k, scale, sampled, with_row_k, hv))
-    check_fused(o, orc, z, A, W, k, row_k=rk, what=what, scale=scale)
+    swaps = check_fused(o, orc, z, A, W, k, row_k=rk, what=what, scale=scale)
+    print("%s: %d certified near-tie swaps" % (what, swaps))
     if sampled:
         check_draws(o["sampled_ids"].cpu().numpy(), o["sampled_logprob"].cpu().numpy(), z, orc["lse"],
                     sampling["temperature"], None if sampling["mask"] is None else sampling["mask"].view(np.uint32),

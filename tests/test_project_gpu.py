@@ -1,7 +1,9 @@
 """lmh_project_logprobs (row gather + tcgen05 head + fused reduction) vs the oracle.
 
 Fused-head acceptance (tests/parity.py): logits, lse and logprobs within 2e-2
-absolute of the f64 oracle; top-k ids bit-exact or a certified near-tie.
+absolute of the f64 oracle; top-k ids bit-exact on the named workloads (no
+certified near-tie swap allowed there), bit-exact or a certified near-tie on
+the random shapes.
 Workloads: the tiny packed batch, the decode batch (K 5 and 1), the
 selective prefill batch, the mixed Llama-3-8B-shaped step and the full
 16384-row projection arm (sampled rows), plus ragged shapes and invariants.
@@ -86,7 +88,7 @@ def test_decode_batch(lmh, decode, k):
     o, st, _ = gpu_project(lmh, b["hidden_d"], b["W_d"], sel=b["sel"], k=k)
     assert st == 0
     z, orc, A = oracle_rows(b, np.arange(32), b["sel"], k)
-    check_fused(o, orc, z, A, b["W"], k, what="decode K=%d" % k)
+    assert check_fused(o, orc, z, A, b["W"], k, what="decode K=%d" % k) == 0
 
 
 def test_prefill_selective(lmh, prefill):
@@ -96,7 +98,7 @@ def test_prefill_selective(lmh, prefill):
     assert st == 0
     assert ri.cpu().tolist() == [2048 * (j + 1) - 1 for j in range(8)]
     z, orc, A = oracle_rows(b, ri.cpu().numpy(), b["sel"], 20)
-    check_fused(o, orc, z, A, b["W"], 20, what="prefill selective")
+    assert check_fused(o, orc, z, A, b["W"], 20, what="prefill selective") == 0
 
 
 def test_full_projection_arm_sampled(lmh, prefill):
@@ -108,7 +110,7 @@ def test_full_projection_arm_sampled(lmh, prefill):
     sample = np.unique(np.concatenate([[0, 127, 128, 2047, 16383], rng.choice(16384, 11, replace=False)]))
     z, orc, A = oracle_rows(b, sample, b["sel_all"][sample], 20)
     sub = {key: v[torch.as_tensor(sample)] for key, v in o.items() if v is not None}
-    check_fused(sub, orc, z, A, b["W"], 20, what="full arm")
+    assert check_fused(sub, orc, z, A, b["W"], 20, what="full arm") == 0
 
 
 def test_mixed_step_sampled(lmh):
@@ -123,7 +125,7 @@ def test_mixed_step_sampled(lmh):
     rk = b["row_k"][sample].numpy()
     z, orc, A = oracle_rows(b, want_ri[sample], b["sel"][sample], 20, row_k=rk)
     sub = {key: v[torch.as_tensor(sample)] for key, v in o.items() if v is not None}
-    check_fused(sub, orc, z, A, b["W"], 20, row_k=rk, what="mixed")
+    assert check_fused(sub, orc, z, A, b["W"], 20, row_k=rk, what="mixed") == 0
 
 
 @pytest.mark.parametrize("rows,H,V,k", [(200, 136, 4100, 20), (129, 64, 1000, 128), (3, 520, 70000, 0),

@@ -39,13 +39,17 @@ def _ptr(t):
 
 
 def call_static(lmh, x, sel, k_max):
-    """One call of the workspace-free entry point; outputs start as garbage on purpose."""
+    """One call of the workspace-free entry point; outputs start as garbage on purpose.
+
+    k_max = K_FULL (-1) asks for every id's logprob: topk_logprobs is [rows, V], no ids.
+    """
     rows, V = x.shape
     dev = x.device
+    full = k_max == lmh.K_FULL
     out = {"lse": torch.full((rows,), float("nan"), device=dev),
            "sel_logprob": torch.full((rows,), float("nan"), device=dev),
-           "topk_ids": torch.full((rows, k_max), -7, dtype=torch.int32, device=dev),
-           "topk_logprobs": torch.full((rows, k_max), float("nan"), device=dev)}
+           "topk_ids": None if full else torch.full((rows, k_max), -7, dtype=torch.int32, device=dev),
+           "topk_logprobs": torch.full((rows, V if full else k_max), float("nan"), device=dev)}
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     rc = _entry(lmh.load())(_ptr(x), lmh.BF16, rows, V, x.stride(0), _ptr(sel), None, k_max, _ptr(out["lse"]),
                             _ptr(out["sel_logprob"]), _ptr(out["topk_ids"]), _ptr(out["topk_logprobs"]),
@@ -56,16 +60,44 @@ def call_static(lmh, x, sel, k_max):
     return out
 
 
+def _same(got, ref, what):
+    if got["topk_ids"] is not None:
+        assert torch.equal(got["topk_ids"], ref["topk_ids"]), what
+    for key in ("lse", "sel_logprob", "topk_logprobs"):
+        diff = (got[key] - ref[key]).abs().max().item()
+        assert diff <= TOL, (what, key, diff)
+
+
 def test_static_matches_workspace_entry_point_on_two_calls(lmh):
     for dist, seed, k in (("normal", 11, 20), ("ties", 12, 128)):
         c = workloads.logits_chunk(dist, seed=seed, rows=64, V=50000)
         x, sel = c["logits"].cuda(), c["sel"].cuda()
         ref = lmh.logprobs_from_logits(x, sel=sel, k_max=k)
         got = call_static(lmh, x, sel, k)
-        assert torch.equal(got["topk_ids"], ref["topk_ids"]), dist
-        for key in ("lse", "sel_logprob", "topk_logprobs"):
-            diff = (got[key] - ref[key]).abs().max().item()
-            assert diff <= TOL, (dist, key, diff)
+        _same(got, ref, dist)
+
+
+def test_static_plain_load_path_and_full_vocabulary(lmh):
+    """Rows whose stride is not a multiple of 16 bytes take the plain-load stream and the
+    select kernel; k_max = K_FULL returns every id's logprob.  Two calls in a row."""
+    c = workloads.logits_chunk("normal", seed=13, rows=40, V=30000)
+    padded = torch.full((40, 30001), -1.0, dtype=torch.bfloat16)
+    padded[:, :30000] = c["logits"]
+    x = padded.cuda()[:, :30000]  # row stride 30001 elements: odd
+    sel = c["sel"].cuda()
+    for k in (20, lmh.K_FULL):
+        ref = lmh.logprobs_from_logits(x, sel=sel, k_max=k)
+        got = call_static(lmh, x, sel, k)
+        _same(got, ref, "odd stride, k %d" % k)
+
+
+def test_static_documented_size_fits(lmh):
+    """The 256 x 248320 prompt-scoring chunk at k_max 128 fits the array (about 4.5 MB)."""
+    c = workloads.logits_chunk("gumbel", seed=14)
+    x, sel = c["logits"].cuda(), c["sel"].cuda()
+    ref = lmh.logprobs_from_logits(x, sel=sel, k_max=128)
+    got = call_static(lmh, x, sel, 128)
+    _same(got, ref, "256 x 248320")
 
 
 def test_static_rejects_requests_beyond_its_scratch(lmh):

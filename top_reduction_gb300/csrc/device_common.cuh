@@ -114,15 +114,37 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
+// Non-blocking test of a phase's completion (mbarrier.test_wait).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Limits below this are test settings (lmh_debug_set_wait_limit): such a wait
+// polls with test_wait, because try_wait itself may suspend the thread until
+// the phase completes and so outlast a limit shorter than its own window.
+constexpr uint64_t kPollLimitNs = 1000000ull;
+
 // Wait on an mbarrier unless the CTA has aborted (another thread gave up
-// first); on a timeout, mark the abort and report LMH_DS_TIMEOUT.
+// first); after limit_ns, mark the abort and report LMH_DS_TIMEOUT.  The
+// kernels pass the library's wait limit (2 s unless a test shortened it);
+// the waits that drain a CTA's copies in flight after an abort use mbar_wait
+// and keep the full limit.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                              uint32_t* dev_status) {
-  if (mbar_try_wait(bar, parity)) return true;
+                                              uint32_t* dev_status, uint64_t limit_ns = kWaitLimitNs) {
+  const bool poll = limit_ns < kPollLimitNs;
+  if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!(poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity))) {
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       set_status(dev_status, LMH_DS_TIMEOUT);
       return false;
@@ -237,7 +259,30 @@ __device__ __forceinline__ float ex2_approx(float x) {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
-// CTA radix select: the k-th largest 64-bit key of an item set
+// named barriers (a subset of a CTA's warps synchronising among themselves)
+// ---------------------------------------------------------------------------
+// bar.sync / bar.red on barrier `id` for `n` threads (n a multiple of 32; every
+// thread of the participating warps arrives).  Barrier 0 is __syncthreads'.
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Barrier that also returns the OR of every participating thread's `pred`.
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+// ---------------------------------------------------------------------------
+// radix select: the k-th largest 64-bit key of an item set
 // ---------------------------------------------------------------------------
 //
 // Items are enumerated by index 0..n-1 through `get(i, &key)`, which returns
@@ -248,17 +293,18 @@ constexpr float kLog2e = 1.4426950408889634f;
 // (< k); items with prefix == T fill the ranks n_above..k-1 (and maybe more).
 // With bits = 64 and unique keys exactly k items have key >= T.
 // Requires k >= 1 and at least k items in the set.  `hist` is 256 uint32 of
-// shared memory, `bcast` 2 uint32 of shared memory.  All threads call it.
-template <typename Get>
-__device__ uint64_t cta_radix_select(Get get, int n, int k, int bits, uint32_t* hist, uint32_t* bcast,
-                                     int* n_above) {
+// shared memory, `bcast` 2 uint32 of shared memory.  Run by a group of `nt`
+// threads (whole warps) with ranks tid = 0..nt-1, synchronised by `sync()`.
+template <typename Get, typename Sync>
+__device__ uint64_t group_radix_select(Get get, int n, int k, int bits, uint32_t* hist, uint32_t* bcast,
+                                       int* n_above, int tid, int nt, Sync sync) {
   uint64_t prefix = 0, mask = 0;
   int need = k, above = 0;
   for (int shift = 56; shift >= 64 - bits; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    for (int base = 0; base < n; base += blockDim.x) {
-      const int i = base + threadIdx.x;
+    for (int i = tid; i < 256; i += nt) hist[i] = 0;
+    sync();
+    for (int base = 0; base < n; base += nt) {
+      const int i = base + tid;
       uint64_t key = 0;
       bool in = (i < n) && get(i, &key) && ((key & mask) == prefix);
       const uint32_t digit = in ? static_cast<uint32_t>(key >> shift) & 0xFFu : 0x100u;
@@ -266,13 +312,13 @@ __device__ uint64_t cta_radix_select(Get get, int n, int k, int bits, uint32_t* 
       const unsigned active = __ballot_sync(0xffffffffu, in);
       if (in) {
         const unsigned peers = __match_any_sync(active, digit);
-        if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
+        if ((tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
       }
     }
-    __syncthreads();
-    if (threadIdx.x < 32) {
+    sync();
+    if (tid < 32) {
       // find digit d with count(> d) < need <= count(>= d), scanning from 255 down
-      const int lane = threadIdx.x;
+      const int lane = tid;
       uint32_t c[8];
       uint32_t mine = 0;
 #pragma unroll
@@ -302,10 +348,10 @@ __device__ uint64_t cta_radix_select(Get get, int n, int k, int bits, uint32_t* 
         }
       }
     }
-    __syncthreads();
+    sync();
     const uint32_t d = bcast[0];
     const uint32_t gt = bcast[1];
-    __syncthreads();
+    sync();
     need -= static_cast<int>(gt);
     above += static_cast<int>(gt);
     prefix |= static_cast<uint64_t>(d) << shift;
@@ -313,6 +359,14 @@ __device__ uint64_t cta_radix_select(Get get, int n, int k, int bits, uint32_t* 
   }
   *n_above = above;
   return prefix;
+}
+
+// The same over all threads of the CTA (synchronised by __syncthreads).
+template <typename Get>
+__device__ uint64_t cta_radix_select(Get get, int n, int k, int bits, uint32_t* hist, uint32_t* bcast,
+                                     int* n_above) {
+  return group_radix_select(get, n, k, bits, hist, bcast, n_above, static_cast<int>(threadIdx.x),
+                            static_cast<int>(blockDim.x), [] { __syncthreads(); });
 }
 
 // ---------------------------------------------------------------------------

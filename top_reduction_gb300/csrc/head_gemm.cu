@@ -138,7 +138,7 @@ cudaError_t head_setup() {
 cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const void* W, int V, const HeadPlan& plan,
                         const int32_t* sel, const int32_t* row_k, int k_max, Partials parts, float* logits_out,
                         uint32_t* dev_status, cudaStream_t stream, bool pdl, const RowOutputs* final_out,
-                        float logit_scale, const SampleArgs* samp, bool w_hv) {
+                        float logit_scale, const SampleArgs* samp, bool w_hv, int id_off) {
   if (final_out && plan.splits != 1) return cudaErrorInvalidValue;
   CUtensorMap ta, tb;
   // With fewer than 128 rows (one row tile) the A box covers only the real
@@ -190,6 +190,8 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
   a.samp = samp ? *samp : SampleArgs{};
   a.final_out = final_out ? 1 : 0;
   a.out = final_out ? *final_out : RowOutputs{nullptr, nullptr, nullptr, nullptr};
+  a.wait_ns = wait_limit_ns();
+  a.id_off = id_off;
   const dim3 grid(plan.grid);
   const bool mat = logits_out != nullptr;
   // the kernels for each weight layout: [V x H] (kHV false) or [H x V] (kHV true)

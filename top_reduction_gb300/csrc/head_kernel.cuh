@@ -67,7 +67,7 @@ struct HeadCfg {
                                        : kRegList ? static_cast<size_t>(4) * 64 * 32 * 4
                                                   : static_cast<size_t>(kBM) * KCAP * 8;
   static constexpr size_t kSmem = 1024 /*alignment slack*/ + kStages * (kStageA + kStageBytesB) +
-                                  kListBytes + (2 * kStages + 6) * 8 + 16;
+                                  kListBytes + (2 * kStages + 7) * 8 + 16;
   // Small batches may split each tile's columns over the epilogue warps (see
   // HeadArgs::rep); a warp then hands its row state to the leader through its
   // own staging region: 7 words plus (value, id) per list entry, per lane.
@@ -93,6 +93,8 @@ struct HeadArgs {
   SampleArgs samp;    // device-side sampling (kernels with kSamp != 0)
   int final_out;   // one vocabulary split: write the final results (out), not partials
   RowOutputs out;
+  uint64_t wait_ns;  // limit of a bounded wait on another role of the CTA
+  int id_off;  // vocabulary-parallel share: token id of W's first row (0: the whole head)
 };
 
 // ---------------------------------------------------------------------------
@@ -389,7 +391,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* xchg_full = acc_empty + 2;    // column split: the copies' row states are staged
   uint64_t* xchg_empty = xchg_full + 1;   // column split: the leader has read them
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xchg_empty + 1);
+  uint64_t* mma_drain = xchg_empty + 1;   // the MMA thread's work in flight has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -406,6 +409,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
     }
     mbar_init(xchg_full, a.rep > 1 ? (4 - a.rep_nq) * 32 : 1);
     mbar_init(xchg_empty, a.rep > 1 ? a.rep_nq * 32 : 1);
+    mbar_init(mma_drain, 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -467,6 +471,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
       start_unit();
       int pm[S], pk[S];
       int np = 0;
+      uint32_t n_issued = 0;  // stage loads issued: load i went to stage i % S, phase (i / S) & 1
 #pragma unroll
       for (int j = 0; j < S; ++j) {
         if (valid) {  // a fresh ring: the empty barriers need no wait yet
@@ -476,6 +481,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
           load_b(j, kb, n);
           advance();
           np = j + 1;
+          ++n_issued;
         }
       }
       // the stage's A slice: one box, or with the column split one box per row copy
@@ -494,16 +500,21 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
       int s = np == S ? 0 : np;
       uint32_t ph = np == S ? 1u : 0u;
       while (valid) {
-        if (!wait_or_abort(&empty[s], ph ^ 1u, abort_flag, a.dev_status)) break;
+        if (!wait_or_abort(&empty[s], ph ^ 1u, abort_flag, a.dev_status, a.wait_ns)) break;
         mbar_arrive_expect_tx(&full[s], a.a_bytes + kStageBytesB);
         load_a(s, kb, m_tile);
         load_b(s, kb, n);
         advance();
+        ++n_issued;
         if (++s == S) {
           s = 0;
           ph ^= 1u;
         }
       }
+      // Every stage's last load lands before the CTA exits (after an abort some may
+      // still be in flight; otherwise these waits return at once).  Full limit.
+      for (uint32_t i = n_issued > static_cast<uint32_t>(S) ? n_issued - S : 0u; i < n_issued; ++i)
+        mbar_wait(&full[i % S], (i / S) & 1u);
     }
   } else if (warp == 1) {
     // ------------------------- MMA issuer -------------------------
@@ -518,14 +529,14 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
         const int n_end = min(n_begin + a.tiles_per_split, a.n_tiles);
         for (int n = n_begin; n < n_end && live; ++n, ++t) {
           const uint32_t b = t & 1u, aph = (t >> 1) & 1u;
-          if (!wait_or_abort(&acc_empty[b], aph ^ 1u, abort_flag, a.dev_status)) {
+          if (!wait_or_abort(&acc_empty[b], aph ^ 1u, abort_flag, a.dev_status, a.wait_ns)) {
             live = false;
             break;
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + b * kBN;
           for (int kb = 0; kb < k_blocks; ++kb) {
-            if (!wait_or_abort(&full[s], ph, abort_flag, a.dev_status)) {
+            if (!wait_or_abort(&full[s], ph, abort_flag, a.dev_status, a.wait_ns)) {
               live = false;
               break;
             }
@@ -552,6 +563,10 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
           if (live) umma_commit(&acc_full[b]);
         }
       }
+      // Every MMA this thread issued has completed before the tensor memory is freed
+      // (after an abort some may still run; otherwise the wait returns at once).
+      umma_commit(mma_drain);
+      mbar_wait(mma_drain, 0);
     }
   } else {
     // ------------------------- epilogue -------------------------
@@ -601,7 +616,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
       rt.reset();
       for (int n = n_begin; n < n_end; ++n, ++t) {
         const uint32_t b = t & 1u, aph = (t >> 1) & 1u;
-        if (!wait_or_abort(&acc_full[b], aph, abort_flag, a.dev_status)) {
+        if (!wait_or_abort(&acc_full[b], aph, abort_flag, a.dev_status, a.wait_ns)) {
           live = false;
           break;
         }
@@ -663,7 +678,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
               acc1 += ex2_approx(fmaf(v[j + 1], L, -mL));
             }
             ssum += acc0 + acc1;
-            const unsigned rel = static_cast<unsigned>(sel_id - col0);
+            const int gcol0 = col0 + a.id_off;  // token id of the block's first logit
+            const unsigned rel = static_cast<unsigned>(sel_id - gcol0);
             if (rel < static_cast<unsigned>(kBlock)) {
               float sv = 0.0f;
 #pragma unroll
@@ -774,7 +790,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                   const int j = __ffsll(static_cast<long long>(cm)) - 1;
                   cm &= cm - 1;
                   const float x = stg[j * 32 + lane];
-                  if (x > rt.tau) rt.insert(x, col0 + j);
+                  if (x > rt.tau) rt.insert(x, gcol0 + j);
                 }
                 __syncwarp(valid_mask);
               }
@@ -782,7 +798,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
               if (k_row > 0 && bm > st.tau) {
 #pragma unroll
                 for (int j = 0; j < kBlock; ++j)
-                  if (v[j] > st.tau) st = heap_push(lists, r_local, st, a.k_max, make_key(v[j], col0 + j));
+                  if (v[j] > st.tau) st = heap_push(lists, r_local, st, a.k_max, make_key(v[j], gcol0 + j));
               }
             }
           }
@@ -813,11 +829,11 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
           xs[192] = s_z;
           mbar_arrive(xchg_full);
           // the staging region is reused only after the leader has read it
-          if (!wait_or_abort(xchg_empty, xu & 1u, abort_flag, a.dev_status)) break;
+          if (!wait_or_abort(xchg_empty, xu & 1u, abort_flag, a.dev_status, a.wait_ns)) break;
           ++xu;
           continue;
         }
-        if (!wait_or_abort(xchg_full, xu & 1u, abort_flag, a.dev_status)) break;
+        if (!wait_or_abort(xchg_full, xu & 1u, abort_flag, a.dev_status, a.wait_ns)) break;
         for (int p = 1; p < n_rep; ++p) {
           const float* ys = reinterpret_cast<const float*>(lists) + (q + p * a.rep_nq) * (kBlock * 32) + lane;
           const float mp = ys[0], sp = ys[32];

@@ -3,6 +3,7 @@
 //
 // Nothing here computes results: every step of the path runs in the kernels
 // of select_rows.cu, head_gemm.cu, logits_reduce.cu and merge_partials.cu.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -43,6 +44,10 @@ static cudaError_t device_setup(int* num_sms) {
 
 static inline size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
+// limit of the kernels' bounded waits (read at every launch)
+static std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
 size_t partials_bytes(int rows, int splits, int k_max) {
   const size_t rs = static_cast<size_t>(rows) * static_cast<size_t>(splits);
   return align256(rs * 8) + align256(rs * static_cast<size_t>(k_max) * 8) + align256(static_cast<size_t>(rows) * 4) +
@@ -62,6 +67,7 @@ Partials carve_partials(void* base, int rows, int splits, int k_max) {
   out.part_samp = reinterpret_cast<float4*>(p);
   out.bmax = nullptr;
   out.ticket = nullptr;
+  out.row_done = nullptr;
   return out;
 }
 
@@ -70,7 +76,7 @@ Partials carve_partials(void* base, int rows, int splits, int k_max) {
 // ---------------------------------------------------------------------------
 static const char* const kTraceNames[kTraceCount] = {"select_rows",   "gather_rows",    "head_logprobs",
                                                      "logits_reduce", "merge_partials", "logits_select",
-                                                     "ticket_reset",  "full_logprobs"};
+                                                     "counters_reset", "full_logprobs"};
 
 struct TraceRecord {
   int kernel;
@@ -285,7 +291,7 @@ static lmh_status project_impl(const void* hidden, int64_t hidden_row_stride, in
   if (e == cudaSuccess && !one_split) {
     Traced tr(kTraceMerge, stream);
     e = launch_merge(rows, plan.splits, V, k_max, parts, sel_ids, row_k, lse, sel_logprob, topk_ids, topk_logprobs,
-                     dev_status, stream, /*pdl=*/true, samp);
+                     dev_status, stream, /*pdl=*/true, samp, sms);
   }
   if (e == cudaSuccess && full)
     e = launch_full_logprobs(z_out, LMH_F32, V, rows, V, lse, topk_logprobs, stream);
@@ -391,6 +397,100 @@ lmh_status lmh_probe_selective(const void* hidden, int64_t hidden_row_stride, in
   if (st != LMH_OK) return st;
   return from_cuda(launch_probe_compare(ours, ref_logits, static_cast<int64_t>(rows) * V, tolerance, mismatches, sms,
                                         stream));
+}
+
+size_t lmh_record_bytes(int32_t k_max) {
+  if (k_max < 0 || k_max > LMH_K_MAX) return 0;
+  return record_bytes(k_max);
+}
+
+// One rank's share of a vocabulary-parallel head: the gather, the head over the
+// share's rows of W (token ids offset by v_begin) and the merge of its vocabulary
+// ranges into one record per row.
+lmh_status lmh_project_partials(const void* hidden, int64_t hidden_row_stride, int32_t num_tokens,
+                                const int32_t* row_idx, int32_t rows, int32_t H, const void* W_share,
+                                lmh_w_layout w_layout, int32_t v_begin, int32_t v_count, int32_t V,
+                                const int32_t* sel_ids, const int32_t* row_k, int32_t k_max, void* records,
+                                void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                cudaStream_t stream) {
+  if (rows < 0 || H <= 0 || V <= 0 || num_tokens < 0 || v_begin < 0 || v_count <= 0 ||
+      static_cast<int64_t>(v_begin) + v_count > V)
+    return LMH_ERR_INVALID_ARG;
+  if (k_max < 0 || k_max > LMH_K_MAX) return LMH_ERR_UNSUPPORTED;
+  if (k_max > v_count) return LMH_ERR_INVALID_ARG;
+  if (w_layout != LMH_W_VH) return LMH_ERR_UNSUPPORTED;
+  if (!hidden || !W_share || !records || hidden_row_stride < H || (!row_idx && rows > num_tokens))
+    return LMH_ERR_INVALID_ARG;
+  if ((H % 8) != 0 || !aligned(hidden, 16) || !aligned(W_share, 16) || !aligned(records, 8))
+    return LMH_ERR_UNSUPPORTED;
+  if (rows == 0) return LMH_OK;
+  int sms = 0;
+  if (device_setup(&sms) != cudaSuccess) return LMH_ERR_CUDA;
+  const HeadPlan plan = head_plan(rows, H, v_count, k_max, sms);
+  const size_t gather_bytes = align256(static_cast<size_t>(rows) * static_cast<size_t>(H) * 2);
+  const size_t need = gather_bytes + partials_bytes(rows, plan.splits, k_max);
+  if (!workspace || !aligned(workspace, 256)) return LMH_ERR_INVALID_ARG;
+  if (workspace_bytes < need) return LMH_ERR_WORKSPACE_TOO_SMALL;
+  char* ws = static_cast<char*>(workspace);
+  const Partials parts = carve_partials(ws + gather_bytes, rows, plan.splits, k_max);
+  const bool gather = row_idx != nullptr || (hidden_row_stride % 8) != 0;
+  const void* A = hidden;
+  int64_t a_stride = hidden_row_stride;
+  cudaError_t e = cudaSuccess;
+  if (gather) {
+    Traced tr(kTraceGather, stream);
+    e = launch_gather_rows(hidden, hidden_row_stride, num_tokens, row_idx, rows, H, ws, dev_status, stream);
+    A = ws;
+    a_stride = H;
+  }
+  if (e == cudaSuccess) {
+    Traced tr(kTraceHead, stream);
+    e = launch_head(A, a_stride, rows, H, W_share, v_count, plan, sel_ids, row_k, k_max, parts, nullptr, dev_status,
+                    stream, /*pdl=*/gather, nullptr, 1.0f, nullptr, false, v_begin);
+  }
+  if (e == cudaSuccess) {
+    const RecordOut rec{static_cast<unsigned char*>(records), v_begin, v_count};
+    Traced tr(kTraceMerge, stream);
+    e = launch_merge(rows, plan.splits, V, k_max, parts, sel_ids, row_k, nullptr, nullptr, nullptr, nullptr,
+                     dev_status, stream, /*pdl=*/true, nullptr, sms, &rec);
+  }
+  return from_cuda(e);
+}
+
+size_t lmh_merge_workspace_bytes(int32_t rows, int32_t num_parts, int32_t k_max) {
+  if (rows < 0 || num_parts <= 0 || k_max < 0 || k_max > LMH_K_MAX) return 0;
+  if (rows == 0) return 256;
+  return partials_bytes(rows, num_parts, k_max);
+}
+
+lmh_status lmh_merge_records(const void* records, int32_t num_parts, int32_t rows, int32_t V,
+                             const int32_t* sel_ids, const int32_t* row_k, int32_t k_max, float* lse,
+                             float* sel_logprob, int32_t* topk_ids, float* topk_logprobs, void* workspace,
+                             size_t workspace_bytes, uint32_t* dev_status, cudaStream_t stream) {
+  if (rows < 0 || num_parts <= 0 || V <= 0) return LMH_ERR_INVALID_ARG;
+  if (k_max < 0 || k_max > LMH_K_MAX) return LMH_ERR_UNSUPPORTED;
+  if (k_max > V) return LMH_ERR_INVALID_ARG;
+  if (!records || !lse || (sel_ids && !sel_logprob) || (k_max > 0 && (!topk_ids || !topk_logprobs)))
+    return LMH_ERR_INVALID_ARG;
+  if (!aligned(records, 8)) return LMH_ERR_UNSUPPORTED;
+  if (rows == 0) return LMH_OK;
+  int sms = 0;
+  if (device_setup(&sms) != cudaSuccess) return LMH_ERR_CUDA;
+  if (!workspace || !aligned(workspace, 256)) return LMH_ERR_INVALID_ARG;
+  if (workspace_bytes < partials_bytes(rows, num_parts, k_max)) return LMH_ERR_WORKSPACE_TOO_SMALL;
+  const Partials parts = carve_partials(workspace, rows, num_parts, k_max);
+  cudaError_t e = launch_unpack_records(records, num_parts, rows, k_max, parts, stream);
+  if (e == cudaSuccess) {
+    Traced tr(kTraceMerge, stream);
+    e = launch_merge(rows, num_parts, V, k_max, parts, sel_ids, row_k, lse, sel_logprob, topk_ids, topk_logprobs,
+                     dev_status, stream, /*pdl=*/true, nullptr, sms);
+  }
+  return from_cuda(e);
+}
+
+lmh_status lmh_debug_set_wait_limit(uint64_t limit_ns) {
+  g_wait_limit_ns.store(limit_ns == 0 ? 2000000000ull : limit_ns, std::memory_order_relaxed);
+  return LMH_OK;
 }
 
 lmh_status lmh_trace_enable(int32_t enable) {

@@ -39,6 +39,7 @@ struct Partials {
   unsigned int* ticket;  // standalone reduction: chunk counter of the dynamic schedule (else unused)
   float4* part_samp;     // head path: per-(row, split) sampling partial (best score, id bits, z, -)
   float* bmax;  // standalone reduction: block maxima [rows * nblk] (else unused)
+  unsigned int* row_done;  // standalone reduction: chunks of each row completed (else unused)
 };
 
 // Device-side sampling on the head path (lmh_project_logprobs_sample): Gumbel-max
@@ -54,6 +55,28 @@ struct SampleArgs {
   float* lp_out;           // [rows] z[id] - lse, or null
 };
 
+// Vocabulary-parallel head: one rank's result for one row over its share of the
+// vocabulary, as exchanged between ranks (include/lmh.h, lmh_record_bytes):
+// the share's max m and sum exp(z - m), the selected token's logit when the
+// token lies in the share (flags bit 0), then k_max sortable keys, best first,
+// with global token ids (0: no entry).
+struct VocabRecord {
+  float m;
+  float s;
+  float sel_logit;
+  uint32_t flags;
+};
+constexpr uint32_t kRecordHasSel = 1u;
+__host__ __device__ inline size_t record_bytes(int k_max) {
+  return sizeof(VocabRecord) + 8 * static_cast<size_t>(k_max > 0 ? k_max : 0);
+}
+
+// Where the merge writes a vocabulary-parallel record instead of final results.
+struct RecordOut {
+  unsigned char* base;  // [rows] records of record_bytes(k_max)
+  int v_begin, v_count;  // the share: token ids [v_begin, v_begin + v_count)
+};
+
 // Final per-row results (the outputs of lmh_project_logprobs / lmh_logprobs_from_logits).
 struct RowOutputs {
   float* lse;
@@ -64,6 +87,10 @@ struct RowOutputs {
 
 size_t partials_bytes(int rows, int splits, int k_max);
 Partials carve_partials(void* base, int rows, int splits, int k_max);
+
+// Limit of the kernels' bounded waits on another role of their own CTA (2 s;
+// lmh_debug_set_wait_limit changes it for tests of the timeout path).
+uint64_t wait_limit_ns();
 
 // One-time per-device set-up (kernel attributes).  Returns cudaSuccess or the error.
 cudaError_t logits_reduce_setup();
@@ -77,11 +104,13 @@ cudaError_t launch_select_rows(const int32_t* cu, int num_seqs, int num_decode, 
                                cudaStream_t stream);
 
 // Workspace of the standalone reduction: part_ms [rows * slots], sel_logit
-// [rows], bmax [rows * nblk], the chunk counter.
+// [rows], bmax [rows * nblk], the chunk counter, the per-row chunk counters.
 size_t stream_partials_bytes(int rows, const VocabSplit& vs);
 Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs);
 
-// Stream kernel then per-row select kernel (the results go straight to the outputs).
+// Counter reset and the stream kernel, which selects each row in the CTA that
+// completes it (16-byte aligned rows), or the register-path stream kernel and a
+// per-row select kernel; the results go straight to the outputs.
 cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t row_stride, int rows, int V,
                                  VocabSplit split, const int32_t* sel, const int32_t* row_k, int k_max,
                                  Partials parts, float* lse, float* sel_logprob, int32_t* topk_ids,
@@ -91,7 +120,12 @@ cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t ro
 cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts, const int32_t* sel,
                          const int32_t* row_k, float* lse, float* sel_logprob, int32_t* topk_ids,
                          float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream, bool pdl = false,
-                         const SampleArgs* samp = nullptr);
+                         const SampleArgs* samp = nullptr, int num_sms = 0, const RecordOut* rec = nullptr);
+
+// Scatters the gathered records [num_parts][rows] into the merge's partials
+// (one slot per part): (m, s), keys, and the selected logit from the part that holds it.
+cudaError_t launch_unpack_records(const void* records, int num_parts, int rows, int k_max, Partials parts,
+                                  cudaStream_t stream);
 
 // Full-vocabulary output: out[r][v] = fp32(x[r][v]) - lse[r] (x may alias out for f32).
 cudaError_t launch_full_logprobs(const void* x, lmh_dtype dtype, int64_t row_stride, int rows, int V, const float* lse,
@@ -126,7 +160,7 @@ cudaError_t launch_head(const void* A, int64_t a_stride, int rows, int H, const 
                         const HeadPlan& plan, const int32_t* sel, const int32_t* row_k, int k_max,
                         Partials parts, float* logits_out, uint32_t* dev_status, cudaStream_t stream,
                         bool pdl = false, const RowOutputs* final_out = nullptr, float logit_scale = 1.0f,
-                        const SampleArgs* samp = nullptr, bool w_hv = false);
+                        const SampleArgs* samp = nullptr, bool w_hv = false, int id_off = 0);
 
 // Launch `kernel` on `stream`; with pdl = true it carries the programmatic
 // stream serialization attribute, so it may start while its predecessor in the

@@ -5,7 +5,7 @@
 // largest maxima, followed by an exact top-k among their entries; exact ties
 // by ascending token id.
 //
-// GB300 design, two kernels:
+// GB300 design:
 //   * a stream kernel reads every logit once, as a persistent grid over the
 //     whole chunk, so the work per CTA does not depend on the row length.
 //     For every 64-block it writes the block's maximum to the workspace, and
@@ -19,17 +19,22 @@
 //         (cp.async.bulk, completion on mbarriers); four consumer warps read
 //         them, each thread owning 128 contiguous bytes (one bf16/f16 block,
 //         half an f32 block), so a block's maximum needs no exchange between
-//         lanes; one (m, s) pair per warp and chunk.
+//         lanes; one (m, s) pair per warp and chunk.  After each chunk the
+//         CTA counts it against its row; the CTA that counts a row's last
+//         chunk selects that row at once (select_row, below), while the other
+//         CTAs keep streaming, so only the last rows' selections follow the
+//         stream.  A small kernel before it zeroes the counters.
 //       - logits_stream_regs_kernel (any element-aligned layout; two CTAs
 //         per SM): the flattened (row, 64-block) space is cut into equal
 //         contiguous ranges, one per CTA; every thread loads 16-byte vectors
 //         (or elements at unaligned rows) straight into registers, two
 //         chunks in flight; the lanes of a block combine their maxima by
-//         shuffles; one (m, s) pair per row piece.
-//   * logits_select_kernel -- one CTA per row: lse from the row's (m, s)
-//     pairs (one warp); a lower bound t on the row's k-th largest logit from
-//     the block maxima; candidates = entries >= t of the blocks whose maximum
-//     is >= t, re-read from memory by the warp that owns the block; their
+//         shuffles; one (m, s) pair per row piece.  logits_select_kernel then
+//         selects every row, one CTA per row.
+//   * select_row -- lse from the row's (m, s) pairs (one warp); a lower bound
+//     t on the row's k-th largest logit from the block maxima; candidates =
+//     entries >= t of the blocks whose maximum is >= t, re-read from memory
+//     (L2 for a row just streamed) by the warp that owns the block; their
 //     exact top-k by key (value desc, id asc), ordered by rank.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -54,7 +59,7 @@ constexpr int kTChunkBytes = kTConsumers * 128;  // 128 contiguous bytes per con
 constexpr int kTStages = 3;
 constexpr int kTCtasPerSm = 4;
 constexpr int kTDescBytes = 32;
-constexpr int kTSmem = kTStages * kTChunkBytes + kTStages * kTDescBytes + 2 * kTStages * 8 + 16;
+constexpr int kTSmemRing = kTStages * kTChunkBytes + kTStages * kTDescBytes + 2 * kTStages * 8 + 16;
 
 template <typename T>
 struct Vec16;  // 16-byte vector of T widened to fp32
@@ -197,6 +202,13 @@ struct ReduceArgs {
   int k_max;
   Partials parts;
   uint32_t* dev_status;
+  uint64_t wait_ns;  // limit of a bounded wait on another role of the CTA
+  // TMA path: the CTA that completes a row's last chunk selects the row and
+  // writes these outputs itself
+  float* lse;
+  float* sel_logprob;
+  int32_t* topk_ids;
+  float* topk_logprobs;
 };
 
 // One chunk of a CTA's work: up to CH blocks of one row inside one range.
@@ -262,6 +274,355 @@ __device__ __forceinline__ int64_t piece_slot(const ReduceArgs& a, int row, int 
 }
 
 // ---------------------------------------------------------------------------
+// per-row selection
+// ---------------------------------------------------------------------------
+// select_row() finishes one row from the stream kernel's results: lse from the
+// row's (m, s) slots, the selected token's logprob, and the exact top-k.  It is
+// run by a group of NT threads (whole warps, ranks tid = 0..NT-1) synchronised
+// on named barrier kSelBar: the four consumer warps of the stream CTA that
+// completed the row's last chunk (TMA path), or a CTA of its own per row
+// (logits_select_kernel, register path).  The block maxima, (m, s) slots and
+// selected logit were written by other CTAs of the same grid, so they are read
+// through L2 (ld.global.cg), never from a possibly stale L1 line.
+constexpr int kSelBar = 1;      // named barrier of the selecting group
+constexpr int kSThreads = 256;  // logits_select_kernel
+constexpr int kSCandCap = 512;  // candidate keys held in shared memory
+constexpr int kSWarpKept = 64;  // kept blocks listed per warp
+constexpr int kSGather = 4;     // candidate vectors per lane in flight
+
+template <int NT>
+struct SelectSmem {
+  static constexpr int kWarps = NT / 32;
+  uint64_t cand[kSCandCap];
+  uint32_t hist[256];
+  uint32_t misc[4];  // [0] candidates, [1..2] select broadcast, [3] kept-list overflow
+  float wq[kWarps];
+  int wkept[kWarps][kSWarpKept];
+  float lse;
+  int flag;  // stream kernel: the row this CTA's last count completed, or -1
+};
+
+// Lower bound on the k-th largest logit of a row from its block maxima.
+// (m1, m2) are the two largest block maxima of a thread's share of the blocks
+// (two distinct blocks); in every warp the q-th largest of the 64 such values
+// (q = ceil(k / warps) <= 32) is a value that q distinct blocks of the warp
+// reach, so the minimum t over the warps is reached by q * warps >= k distinct
+// blocks, each holding a logit >= t: the k-th largest logit is >= t, every
+// top-k logit is >= t and lies in a block whose maximum is >= t.  (Two values
+// per thread keep t tight when a group of four warps asks for 128.)
+template <int NT>
+__device__ __forceinline__ float topk_lower_bound(float m1, float m2, int k, float* wq, int tid) {
+  constexpr int W = NT / 32;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int q = (k + W - 1) / W;
+  // the q-th largest of the warp's values: q rounds of (warp max, one holder pops its best)
+  uint32_t k1 = f32_ord(m1), k2 = f32_ord(m2);  // > 0 for every value that is not NaN; k1 >= k2
+  uint32_t m = 0;
+  for (int r = 0; r < q; ++r) {
+    m = __reduce_max_sync(0xffffffffu, k1);
+    const unsigned holders = __ballot_sync(0xffffffffu, k1 == m);
+    if (lane == __ffs(holders) - 1) {
+      k1 = k2;
+      k2 = 0;  // 0: nothing left in this lane
+    }
+  }
+  if (lane == 0) wq[warp] = ord_f32(m);
+  named_bar_sync(kSelBar, NT);
+  float t = wq[0];
+#pragma unroll
+  for (int w = 1; w < W; ++w) t = fminf(t, wq[w]);
+  return t;
+}
+
+// KB block maxima per thread per round: rows of at most KB * NT blocks take one round,
+// their maxima held in registers.
+template <typename T, int NT, int KB>
+__device__ void select_row(const ReduceArgs& a, int row, int tid, SelectSmem<NT>& sm, float* lse_out,
+                           float* sel_logprob, int32_t* topk_ids, float* topk_logprobs) {
+  using VT = Vec16<T>;
+  constexpr int EPV = VT::N;
+  constexpr int VPB = kBlock / EPV;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int64_t b0 = static_cast<int64_t>(row) * a.nblk;
+  // Every independent load first, so that their latencies overlap: the row's
+  // block maxima (kept in registers when one round covers the row), its K,
+  // the selected token and its logit, and (warp 0) the (m, s) slots.
+  const int nb = a.nblk;
+  const float* bm = a.parts.bmax + b0;
+  const bool one_round = nb <= KB * NT;
+  float bv[KB];
+  if (one_round) {
+#pragma unroll
+    for (int i = 0; i < KB; ++i) {
+      const int b = tid + i * NT;
+      bv[i] = b < nb ? __ldcg(bm + b) : -INFINITY;
+    }
+  }
+  const int k_row = a.row_k ? a.row_k[row] : a.k_max;
+  int sel_t = -1;
+  float sel_x = 0.0f;
+  if (tid == 0 && a.sel) {
+    sel_t = a.sel[row];
+    sel_x = __ldcg(a.parts.sel_logit + row);  // meaningful only when sel_t is in range
+  }
+  // (m, s) slots: warp 0 loads them now and folds them into the lse later,
+  // off the path to the first barrier (rows of <= 128 slots: one round)
+  const int nslots = a.cpr > 0 ? a.cpr * kTConsumerWarps
+                               : static_cast<int>((b0 + a.nblk - 1) / a.per - b0 / a.per + 1);
+  const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.P;
+  float2 msv[4];
+  if (warp == 0) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = u * 32 + lane;
+      msv[u] = j < nslots ? __ldcg(ms + j) : make_float2(-INFINITY, 0.0f);
+    }
+  }
+  // lse = M + log(sum_j s_j exp(m_j - M)); warp 0 writes it (and the selected
+  // token's logprob) and leaves it in sm.lse
+  auto row_lse = [&]() {
+    // two passes over the slots (max, then the rescaled sum): short, parallel dependency chains
+    float tm = fmaxf(fmaxf(msv[0].x, msv[1].x), fmaxf(msv[2].x, msv[3].x));
+    for (int j = 4 * 32 + lane; j < nslots; j += 32) tm = fmaxf(tm, __ldcg(ms + j).x);
+    const float M = warp_max(tm);
+    float ts = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) ts += msv[u].x == -INFINITY ? 0.0f : msv[u].y * expf(msv[u].x - M);
+      for (int j = 4 * 32 + lane; j < nslots; j += 32) {
+        const float2 p = __ldcg(ms + j);
+        ts += p.x == -INFINITY ? 0.0f : p.y * expf(p.x - M);
+      }
+    }
+    const float S = warp_sum(ts);
+    const float lse = (M == -INFINITY) ? -INFINITY : M + logf(S);
+    if (lane == 0) {
+      sm.lse = lse;
+      lse_out[row] = lse;
+      if (a.sel) {
+        float v = __int_as_float(0x7fc00000);  // NaN: no selected token / out of range
+        if (sel_t >= 0 && sel_t < a.V)
+          v = sel_x - lse;
+        else if (sel_t != -1)
+          set_status(a.dev_status, LMH_DS_SEL_OUT_OF_RANGE);
+        sel_logprob[row] = v;
+      }
+    }
+  };
+  if (tid == 0) {
+    sm.misc[0] = 0;
+    sm.misc[3] = 0;
+  }
+  const int k = min(max(k_row, 0), a.k_max);
+  if (k == 0) {
+    if (warp == 0) row_lse();
+    if (a.k_max == 0) return;
+    int32_t* out_ids = topk_ids + static_cast<int64_t>(row) * a.k_max;
+    float* out_lp = topk_logprobs + static_cast<int64_t>(row) * a.k_max;
+    for (int r = tid; r < a.k_max; r += NT) {
+      out_ids[r] = -1;
+      out_lp[r] = -INFINITY;
+    }
+    return;
+  }
+
+  // ---- t <= the k-th largest logit ----
+  // the thread's two largest block maxima (never NaN: fmaxf / fminf drop NaN)
+  float m1 = -INFINITY, m2 = -INFINITY;
+  auto top2 = [&](float v) {
+    m2 = fmaxf(m2, fminf(m1, v));
+    m1 = fmaxf(m1, v);
+  };
+  if (one_round) {
+#pragma unroll
+    for (int i = 0; i < KB; ++i) top2(bv[i]);
+  } else {
+    for (int base = 0; base < nb; base += KB * NT) {
+      float v[KB];
+#pragma unroll
+      for (int i = 0; i < KB; ++i) {
+        const int b = base + tid + i * NT;
+        v[i] = b < nb ? __ldcg(bm + b) : -INFINITY;
+      }
+#pragma unroll
+      for (int i = 0; i < KB; ++i) top2(v[i]);
+    }
+  }
+  const float t = topk_lower_bound<NT>(m1, m2, k, sm.wq, tid);  // (its barrier also publishes misc[0] and misc[3])
+  int32_t* out_ids = topk_ids + static_cast<int64_t>(row) * a.k_max;
+  float* out_lp = topk_logprobs + static_cast<int64_t>(row) * a.k_max;
+
+  // ---- kept blocks (maximum >= t), listed per warp; the warp gathers their entries >= t ----
+  const T* rowp = reinterpret_cast<const T*>(a.logits) + static_cast<int64_t>(row) * a.row_stride;
+  int* wk = sm.wkept[warp];
+  int nk = 0;  // the warp's kept blocks (uniform across the warp)
+  if (one_round) {
+    // this thread's kept blocks as a bit mask; positions by a warp prefix sum of the counts
+    uint32_t kmask = 0;
+#pragma unroll
+    for (int i = 0; i < KB; ++i) kmask |= ((tid + i * NT < nb && bv[i] >= t) ? 1u : 0u) << i;
+    const int mine = __popc(kmask);
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    nk = __shfl_sync(0xffffffffu, incl, 31);
+    int pos = incl - mine;
+    while (kmask) {
+      const int i = __ffs(kmask) - 1;
+      kmask &= kmask - 1;
+      if (pos < kSWarpKept) wk[pos] = tid + i * NT;
+      ++pos;
+    }
+  } else {
+    for (int base = 0; base < nb; base += KB * NT) {
+      float v[KB];
+#pragma unroll
+      for (int i = 0; i < KB; ++i) {
+        const int b = base + tid + i * NT;
+        v[i] = b < nb ? __ldcg(bm + b) : -INFINITY;
+      }
+#pragma unroll
+      for (int i = 0; i < KB; ++i) {
+        const int b = base + tid + i * NT;
+        const bool keep = b < nb && v[i] >= t;
+        const unsigned m = __ballot_sync(0xffffffffu, keep);
+        if (keep) {
+          const int pos = nk + __popc(m & ((1u << lane) - 1u));
+          if (pos < kSWarpKept) wk[pos] = b;
+        }
+        nk += __popc(m);
+      }
+    }
+  }
+  __syncwarp();
+  if (nk > kSWarpKept) {
+    if (lane == 0) sm.misc[3] = 1;  // more kept blocks than the list holds: exact path below
+  } else if (a.vec_ok) {
+    // 16-byte vectors of the kept blocks, kSGather per lane in flight; none straddles the row end.
+    // The warp's candidates are placed with one shared atomic: per-lane bit masks and a prefix sum.
+    const int n_vec = nk * VPB;
+    for (int base = 0; base < n_vec; base += kSGather * 32) {
+      uint4 w[kSGather];
+      int e0[kSGather];
+#pragma unroll
+      for (int u = 0; u < kSGather; ++u) {
+        const int j = base + u * 32 + lane;
+        e0[u] = -1;
+        if (j < n_vec) {
+          const int e = wk[j / VPB] * kBlock + (j % VPB) * EPV;
+          if (e < a.V) {
+            e0[u] = e;
+            w[u] = *reinterpret_cast<const uint4*>(rowp + e);
+          }
+        }
+      }
+      uint32_t cmask = 0;  // bit u * EPV + e: element e of vector u reaches t
+#pragma unroll
+      for (int u = 0; u < kSGather; ++u) {
+        float x[EPV];
+        VT::unpack(w[u], x);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) cmask |= ((e0[u] >= 0 && x[e] >= t) ? 1u : 0u) << (u * EPV + e);
+      }
+      const int mine = __popc(cmask);
+      int incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int total = __shfl_sync(0xffffffffu, incl, 31);
+      uint32_t wbase = 0;
+      if (lane == 31 && total > 0) wbase = atomicAdd(&sm.misc[0], static_cast<uint32_t>(total));
+      wbase = __shfl_sync(0xffffffffu, wbase, 31);
+      uint32_t pos = wbase + static_cast<uint32_t>(incl - mine);
+#pragma unroll
+      for (int u = 0; u < kSGather; ++u) {
+        uint32_t mu = (cmask >> (u * EPV)) & ((1u << EPV) - 1u);
+        if (!mu) continue;
+        float x[EPV];
+        VT::unpack(w[u], x);
+        while (mu) {
+          const int e = __ffs(mu) - 1;
+          mu &= mu - 1;
+          float v = x[0];  // x[e] without dynamic register indexing
+#pragma unroll
+          for (int ee = 1; ee < EPV; ++ee) v = (e == ee) ? x[ee] : v;
+          if (pos < kSCandCap) sm.cand[pos] = make_key(v, e0[u] + e);
+          ++pos;
+        }
+      }
+    }
+  } else {
+    const int n_el = nk * kBlock;
+    for (int j = lane; j < n_el; j += 32) {
+      const int e = wk[j / kBlock] * kBlock + (j % kBlock);
+      if (e < a.V) {
+        const float x = VT::at(rowp, e);
+        if (x >= t) {
+          const uint32_t pos = atomicAdd(&sm.misc[0], 1u);
+          if (pos < kSCandCap) sm.cand[pos] = make_key(x, e);
+        }
+      }
+    }
+  }
+  if (warp == 0) row_lse();
+  named_bar_sync(kSelBar, NT);
+  int cnt = static_cast<int>(sm.misc[0]);
+  const float lse = sm.lse;
+  if (cnt > kSCandCap || sm.misc[3] != 0) {
+    // too many entries reach t (ties, rows of -inf): the exact k-th key over
+    // them, then the k keys at or above it
+    auto in_set = [&](int i, uint64_t* key) -> bool {
+      if (i >= a.V || !(__ldcg(bm + i / kBlock) >= t)) return false;
+      const float x = VT::at(rowp, i);
+      if (!(x >= t)) return false;
+      *key = make_key(x, i);
+      return true;
+    };
+    auto sync = [] { named_bar_sync(kSelBar, NT); };
+    int above;
+    const int n_items = nb * kBlock;
+    const uint64_t T64 = group_radix_select(in_set, n_items, k, 64, sm.hist, sm.misc + 1, &above, tid, NT, sync);
+    sync();
+    if (tid == 0) sm.misc[0] = 0;
+    sync();
+    for (int i = tid; i < n_items; i += NT) {
+      uint64_t key = 0;
+      if (in_set(i, &key) && key >= T64) {
+        const uint32_t pos = atomicAdd(&sm.misc[0], 1u);  // exactly k of them
+        if (pos < kSCandCap) sm.cand[pos] = key;
+      }
+    }
+    sync();
+    cnt = min(k, static_cast<int>(sm.misc[0]));
+  }
+  // ---- exact order by rank (keys are unique): G threads per candidate ----
+  int G = 1;  // a power of two <= 32 with G * cnt <= NT, at least 1
+  while (G < 32 && 2 * G * cnt <= NT) G *= 2;
+  const int groups = NT / G;
+  for (int base = 0; base < cnt; base += groups) {
+    const int i = base + tid / G, sub = tid % G;
+    const uint64_t key = i < cnt ? sm.cand[i] : 0ull;
+    int rank = 0;
+    if (i < cnt)
+      for (int j = sub; j < cnt; j += G) rank += sm.cand[j] > key;
+    for (int o = G / 2; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+    if (i < cnt && sub == 0 && rank < k) {
+      out_ids[rank] = key_id(key);
+      out_lp[rank] = key_value(key) - lse;
+    }
+  }
+  for (int r = min(cnt, k) + tid; r < a.k_max; r += NT) {  // ranks without a candidate, and ranks >= k
+    out_ids[r] = -1;
+    out_lp[r] = -INFINITY;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // stream kernel, TMA path
 // ---------------------------------------------------------------------------
 struct StreamDesc {  // one per stage, written by the producer before the copy is issued
@@ -273,6 +634,9 @@ struct StreamDesc {  // one per stage, written by the producer before the copy i
   int sel_rel;       // selected token relative to the chunk's first logit
 };
 static_assert(sizeof(StreamDesc) <= kTDescBytes, "descriptor slot");
+
+constexpr int kTSelKB = 16;  // block maxima per consumer thread per round in the fused select
+constexpr int kTSmem = kTSmemRing + static_cast<int>(sizeof(SelectSmem<kTConsumers>));
 
 template <typename T>
 __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kernel(const ReduceArgs a) {
@@ -290,6 +654,7 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kTChunkBytes + S * kTDescBytes);
   uint64_t* empty = full + S;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
+  SelectSmem<kTConsumers>& sm = *reinterpret_cast<SelectSmem<kTConsumers>*>(smem + kTSmemRing);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -301,7 +666,7 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
     mbar_init_fence();
   }
   __syncthreads();
-  pdl_launch_dependents();  // the select kernel may be scheduled; it waits for this grid's results
+  pdl_launch_dependents();  // a following kernel may be scheduled; it waits for this grid's results
 
   if (warp == kTConsumerWarps) {
     // ------------------------------ producer ------------------------------
@@ -313,7 +678,7 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
     const int64_t total = static_cast<int64_t>(a.rows) * a.cpr;
     const int64_t first_dynamic = static_cast<int64_t>(S) * gridDim.x;
     const uint64_t policy = l2_evict_first_policy();  // logits are read once; the block maxima stay in L2
-    // The kernel may start while its predecessor (the ticket reset) still runs:
+    // The kernel may start while its predecessor (the counter reset) still runs:
     // wait for it before the first ticket, load or workspace write (the
     // consumers write only data that arrived after this point).
     pdl_wait();
@@ -323,7 +688,7 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
     for (;; ++issued) {
       const int s = static_cast<int>(issued % S);
       if (issued >= static_cast<uint32_t>(S) &&
-          !wait_or_abort(&empty[s], ((issued / S) & 1u) ^ 1u, abort_flag, a.dev_status))
+          !wait_or_abort(&empty[s], ((issued / S) & 1u) ^ 1u, abort_flag, a.dev_status, a.wait_ns))
         break;
       const int64_t c = next;
       StreamDesc& d = desc[s];
@@ -355,80 +720,118 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
       bulk_load_hint(stages + static_cast<size_t>(s) * kTChunkBytes, src, static_cast<uint32_t>(ne * ES), &full[s],
                      policy);
     }
-    // Copies still in flight (only after an abort) land before the CTA exits.
+    // Copies still in flight (only after an abort) land before the CTA exits;
+    // these waits keep the full limit whatever a.wait_ns is.
     const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
     for (uint32_t i = first; i < issued; ++i) mbar_wait(&full[i % S], (i / S) & 1u);
     return;
   }
 
   // ------------------------------ consumers ------------------------------
-  const int c = tid;  // consumer thread 0..255: bytes [128c, 128c + 128) of a chunk
+  // The four consumer warps take every chunk together and decide together (a
+  // barrier with an OR vote) whether to stop, so that none of them waits at a
+  // named barrier the others have left.  Each chunk is counted against its row
+  // (row_done) one iteration later, by thread 0 at the start of the next
+  // iteration: by then the chunk's results are long written, so the fence is
+  // short, and the count's result is read only after the next chunk is
+  // processed, so its round trip hides behind that work.  The CTA whose count
+  // completes a row selects that row (select_row) while the other CTAs keep
+  // streaming; the end marker's iteration counts the CTA's last chunk.
+  const int c = tid;  // consumer thread 0..127: bytes [128c, 128c + 128) of a chunk
   const int rot = c & 7;  // vector order rotated by lane: conflict-free 16-byte shared loads
   const int bi = c / TPB;
   const float L = kLog2e;
+  int prev_row = -1;       // the row of the chunk processed last iteration, not yet counted
+  unsigned prev_old = 0u;  // thread 0: the count before adding that chunk
   for (uint32_t i = 0;; ++i) {
     const int s = static_cast<int>(i % S);
-    bool ok = wait_or_abort(&full[s], (i / S) & 1u, abort_flag, a.dev_status);
-    if (!__all_sync(0xffffffffu, ok)) break;
-    const StreamDesc d = desc[s];
-    if (d.row < 0) break;
-    const unsigned char* stg = stages + static_cast<size_t>(s) * kTChunkBytes;
-    uint4 w[8];
+    const bool ok = __all_sync(0xffffffffu, wait_or_abort(&full[s], (i / S) & 1u, abort_flag, a.dev_status, a.wait_ns));
+    StreamDesc d;
+    d.row = -1;
+    if (ok) d = desc[s];
+    const bool stop = !ok || d.row < 0;
+    // Count the previous chunk.  Every consumer's writes of it preceded the last
+    // barrier; thread 0's fence and increment publish them to the CTA that completes
+    // the row (the pattern of a grid-wide barrier: bar.sync, fence, atomic).
+    if (tid == 0 && prev_row >= 0) {
+      __threadfence();
+      prev_old = atomicAdd(a.parts.row_done + prev_row, 1u);
+    }
+    if (!stop) {
+      const unsigned char* stg = stages + static_cast<size_t>(s) * kTChunkBytes;
+      uint4 w[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) w[j] = *reinterpret_cast<const uint4*>(stg + c * 128 + ((j + rot) & 7) * 16);
-    const bool sel_hit = static_cast<unsigned>(d.sel_rel - c * EPT) < static_cast<unsigned>(EPT) && d.sel_rel < d.ne;
-    float selv = 0.0f;
-    if (sel_hit) selv = VT::at(stg, d.sel_rel);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);  // the stage is in registers: release it
-    if (sel_hit) a.parts.sel_logit[d.row] = selv;
+      for (int j = 0; j < 8; ++j) w[j] = *reinterpret_cast<const uint4*>(stg + c * 128 + ((j + rot) & 7) * 16);
+      const bool sel_hit =
+          static_cast<unsigned>(d.sel_rel - c * EPT) < static_cast<unsigned>(EPT) && d.sel_rel < d.ne;
+      float selv = 0.0f;
+      if (sel_hit) selv = VT::at(stg, d.sel_rel);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // the stage is in registers: release it
+      if (sel_hit) a.parts.sel_logit[d.row] = selv;
 
-    const int ne_t = d.ne - c * EPT;  // real logits among this thread's
-    if (ne_t < EPT) {
+      const int ne_t = d.ne - c * EPT;  // real logits among this thread's
+      if (ne_t < EPT) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (((j + rot) & 7) * EPV >= ne_t) w[j] = make_uint4(VT::kNegInfWord, VT::kNegInfWord, VT::kNegInfWord, VT::kNegInfWord);
-    }
-    const float vm = VT::max8(w);  // this thread's maximum
-    float bmx = vm;
-    if (TPB == 2) bmx = fmaxf(bmx, __shfl_xor_sync(0xffffffffu, bmx, 1));
-    if ((c % TPB) == 0 && bi < d.nbk) a.parts.bmax[static_cast<int64_t>(d.row) * a.nblk + d.lb + bi] = bmx;
-    float ts = 0.0f;  // sum of exp(x - vm) over this thread's logits
-    if (vm > -INFINITY) {
-      // exp(x - m) = 2^(x*log2e - m*log2e): one packed FFMA2 and one packed
-      // FADD2 per pair of logits around the two ex2
-      const float2 L2 = make_float2(L, L), nmL2 = make_float2(-vm * L, -vm * L);
-      float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
-                       make_float2(0.0f, 0.0f)};
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float2 p[EPV / 2];
-        VT::pairs(w[j], p);
-#pragma unroll
-        for (int q = 0; q < EPV / 2; ++q) {
-          const float2 y = __ffma2_rn(p[q], L2, nmL2);
-          acc[q & 3] = __fadd2_rn(acc[q & 3], make_float2(ex2_approx(y.x), ex2_approx(y.y)));
-        }
+        for (int j = 0; j < 8; ++j)
+          if (((j + rot) & 7) * EPV >= ne_t)
+            w[j] = make_uint4(VT::kNegInfWord, VT::kNegInfWord, VT::kNegInfWord, VT::kNegInfWord);
       }
-      const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
-      const float2 a = __fadd2_rn(a01, a23);
-      ts = a.x + a.y;
+      const float vm = VT::max8(w);  // this thread's maximum
+      float bmx = vm;
+      if (TPB == 2) bmx = fmaxf(bmx, __shfl_xor_sync(0xffffffffu, bmx, 1));
+      if ((c % TPB) == 0 && bi < d.nbk) a.parts.bmax[static_cast<int64_t>(d.row) * a.nblk + d.lb + bi] = bmx;
+      float ts = 0.0f;  // sum of exp(x - vm) over this thread's logits
+      if (vm > -INFINITY) {
+        // exp(x - m) = 2^(x*log2e - m*log2e): one packed FFMA2 and one packed
+        // FADD2 per pair of logits around the two ex2
+        const float2 L2 = make_float2(L, L), nmL2 = make_float2(-vm * L, -vm * L);
+        float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                         make_float2(0.0f, 0.0f)};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float2 p[EPV / 2];
+          VT::pairs(w[j], p);
+#pragma unroll
+          for (int q = 0; q < EPV / 2; ++q) {
+            const float2 y = __ffma2_rn(p[q], L2, nmL2);
+            acc[q & 3] = __fadd2_rn(acc[q & 3], make_float2(ex2_approx(y.x), ex2_approx(y.y)));
+          }
+        }
+        const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+        const float2 a = __fadd2_rn(a01, a23);
+        ts = a.x + a.y;
+      }
+      // the warp's (m, s) over this chunk
+      const float M = warp_max(vm);
+      const float sc = warp_sum(vm == -INFINITY ? 0.0f : ts * ex2_approx((vm - M) * L));
+      if (lane == 0) a.parts.part_ms[d.slot + warp] = make_float2(M, M == -INFINITY ? 0.0f : sc);
     }
-    // the warp's (m, s) over this chunk
-    const float M = warp_max(vm);
-    const float sc = warp_sum(vm == -INFINITY ? 0.0f : ts * ex2_approx((vm - M) * L));
-    if (lane == 0) a.parts.part_ms[d.slot + warp] = make_float2(M, M == -INFINITY ? 0.0f : sc);
+    const bool any_stop = named_bar_or(kSelBar, kTConsumers, stop);
+    if (tid == 0) {
+      const bool last = prev_row >= 0 && prev_old == static_cast<unsigned>(a.cpr) - 1u;
+      if (last) __threadfence();  // the other CTAs' writes to the row are visible from here on
+      sm.flag = last ? prev_row : -1;
+    }
+    named_bar_sync(kSelBar, kTConsumers);
+    if (sm.flag >= 0)
+      select_row<T, kTConsumers, kTSelKB>(a, sm.flag, tid, sm, a.lse, a.sel_logprob, a.topk_ids, a.topk_logprobs);
+    if (any_stop) break;
+    prev_row = d.row;
   }
 }
 
-// Zeroes the chunk ticket before the TMA-path stream kernel.  A kernel (not a
-// memset) so that the chain previous kernel -> reset -> stream can use
-// programmatic dependent launch: it waits for its predecessor, whose work may
-// still read the workspace, and lets the stream kernel be scheduled meanwhile.
-__global__ void ticket_reset_kernel(unsigned int* ticket) {
+// Zeroes the chunk ticket and the per-row chunk counters before the TMA-path
+// stream kernel.  A kernel (not a memset) so that the chain previous kernel ->
+// reset -> stream can use programmatic dependent launch: it waits for its
+// predecessor, whose work may still read the workspace, and lets the stream
+// kernel be scheduled meanwhile.
+__global__ void __launch_bounds__(256) counters_reset_kernel(unsigned int* ticket, unsigned int* row_done, int rows) {
   pdl_launch_dependents();
   pdl_wait();
-  if (threadIdx.x == 0) *ticket = 0u;
+  const int i0 = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i0 == 0) *ticket = 0u;
+  for (int i = i0; i < rows; i += gridDim.x * blockDim.x) row_done[i] = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -547,333 +950,15 @@ __global__ void __launch_bounds__(kRThreads, kRCtasPerSm) logits_stream_regs_ker
   }
 }
 
-// ---------------------------------------------------------------------------
-// per-row selection
-// ---------------------------------------------------------------------------
-constexpr int kSThreads = 256;
-constexpr int kSWarps = kSThreads / 32;
-constexpr int kSCandCap = 512;   // candidate keys held in shared memory
-
-constexpr int kSWarpKept = 64;   // kept blocks listed per warp
-constexpr int kSGather = 4;      // candidate vectors per lane in flight
-constexpr int kSBatch = 16;      // block maxima per thread loaded per round (rows of <= 4096 blocks: one)
-
-// Lower bound on the k-th largest logit of a row from its block maxima.
-// `tmax` is each thread's maximum over its share of the blocks; in every warp
-// the q-th largest of those (q = ceil(k / warps)) is a value that q blocks of
-// the warp reach, so the minimum t over the warps is reached by q * warps >= k
-// distinct blocks, each holding a logit >= t: the k-th largest logit is >= t,
-// every top-k logit is >= t and lies in a block whose maximum is >= t.
-__device__ __forceinline__ float topk_lower_bound(float tmax, int k, float* wq) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int q = (k + kSWarps - 1) / kSWarps;
-  // the q-th largest of the warp's values: q rounds of (warp max, one holder drops out)
-  uint32_t key = f32_ord(tmax);  // > 0 for every value that is not NaN; 0 marks a dropped lane
-  uint32_t m = 0;
-  for (int r = 0; r < q; ++r) {
-    m = __reduce_max_sync(0xffffffffu, key);
-    const unsigned holders = __ballot_sync(0xffffffffu, key == m);
-    if (lane == __ffs(holders) - 1) key = 0;
-  }
-  if (lane == 0) wq[warp] = ord_f32(m);
-  __syncthreads();
-  float t = wq[0];
-#pragma unroll
-  for (int w = 1; w < kSWarps; ++w) t = fminf(t, wq[w]);
-  return t;
-}
-
+// The register path's select: one CTA per row, after the stream kernel.
 template <typename T>
 __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceArgs a, float* lse_out,
                                                                   float* sel_logprob, int32_t* topk_ids,
                                                                   float* topk_logprobs) {
-  using VT = Vec16<T>;
-  constexpr int EPV = VT::N;
-  constexpr int VPB = kBlock / EPV;
-  __shared__ uint64_t cand[kSCandCap];
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t misc[4];  // [0] candidates, [1..2] select broadcast, [3] kept-list overflow
-  __shared__ float wq[kSWarps];
-  __shared__ int wkept[kSWarps][kSWarpKept];
-  __shared__ float s_lse;
+  __shared__ SelectSmem<kSThreads> sm;
   pdl_wait();  // the block maxima and (m, s) come from the stream kernel just before
   pdl_launch_dependents();  // a following kernel may be scheduled; it waits for this grid before using its results
-
-  const int row = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t b0 = static_cast<int64_t>(row) * a.nblk;
-  // Every independent load first, so that their latencies overlap: the row's
-  // block maxima (kept in registers when one round covers the row), its K,
-  // the selected token and its logit, and (warp 0) the (m, s) slots.
-  const int nb = a.nblk;
-  const float* bm = a.parts.bmax + b0;
-  const bool one_round = nb <= kSBatch * kSThreads;
-  float bv[kSBatch];
-  if (one_round) {
-#pragma unroll
-    for (int i = 0; i < kSBatch; ++i) {
-      const int b = tid + i * kSThreads;
-      bv[i] = b < nb ? bm[b] : -INFINITY;
-    }
-  }
-  const int k_row = a.row_k ? a.row_k[row] : a.k_max;
-  int sel_t = -1;
-  float sel_x = 0.0f;
-  if (tid == 0 && a.sel) {
-    sel_t = a.sel[row];
-    sel_x = a.parts.sel_logit[row];  // meaningful only when sel_t is in range
-  }
-  // (m, s) slots: warp 0 loads them now and folds them into the lse later,
-  // off the path to the first barrier (rows of <= 128 slots: one round)
-  const int nslots = a.cpr > 0 ? a.cpr * kTConsumerWarps
-                               : static_cast<int>((b0 + a.nblk - 1) / a.per - b0 / a.per + 1);
-  const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.P;
-  float2 msv[4];
-  if (warp == 0) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j = u * 32 + lane;
-      msv[u] = j < nslots ? ms[j] : make_float2(-INFINITY, 0.0f);
-    }
-  }
-  // lse = M + log(sum_j s_j exp(m_j - M)); warp 0 writes it (and the selected
-  // token's logprob) and leaves it in s_lse
-  auto row_lse = [&]() {
-    // two passes over the slots (max, then the rescaled sum): short, parallel dependency chains
-    float tm = fmaxf(fmaxf(msv[0].x, msv[1].x), fmaxf(msv[2].x, msv[3].x));
-    for (int j = 4 * 32 + lane; j < nslots; j += 32) tm = fmaxf(tm, ms[j].x);
-    const float M = warp_max(tm);
-    float ts = 0.0f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) ts += msv[u].x == -INFINITY ? 0.0f : msv[u].y * expf(msv[u].x - M);
-      for (int j = 4 * 32 + lane; j < nslots; j += 32) {
-        const float2 p = ms[j];
-        ts += p.x == -INFINITY ? 0.0f : p.y * expf(p.x - M);
-      }
-    }
-    const float S = warp_sum(ts);
-    const float lse = (M == -INFINITY) ? -INFINITY : M + logf(S);
-    if (lane == 0) {
-      s_lse = lse;
-      lse_out[row] = lse;
-      if (a.sel) {
-        float v = __int_as_float(0x7fc00000);  // NaN: no selected token / out of range
-        if (sel_t >= 0 && sel_t < a.V)
-          v = sel_x - lse;
-        else if (sel_t != -1)
-          set_status(a.dev_status, LMH_DS_SEL_OUT_OF_RANGE);
-        sel_logprob[row] = v;
-      }
-    }
-  };
-  if (tid == 0) {
-    misc[0] = 0;
-    misc[3] = 0;
-  }
-  const int k = min(max(k_row, 0), a.k_max);
-  if (k == 0) {
-    if (warp == 0) row_lse();
-    if (a.k_max == 0) return;
-    int32_t* out_ids = topk_ids + static_cast<int64_t>(row) * a.k_max;
-    float* out_lp = topk_logprobs + static_cast<int64_t>(row) * a.k_max;
-    for (int r = tid; r < a.k_max; r += kSThreads) {
-      out_ids[r] = -1;
-      out_lp[r] = -INFINITY;
-    }
-    return;
-  }
-
-  // ---- t <= the k-th largest logit ----
-  float tmax = -INFINITY;  // never NaN: fmaxf drops NaN block maxima
-  if (one_round) {
-#pragma unroll
-    for (int i = 0; i < kSBatch; ++i) tmax = fmaxf(tmax, bv[i]);
-  } else {
-    for (int base = 0; base < nb; base += kSBatch * kSThreads) {
-      float v[kSBatch];
-#pragma unroll
-      for (int i = 0; i < kSBatch; ++i) {
-        const int b = base + tid + i * kSThreads;
-        v[i] = b < nb ? bm[b] : -INFINITY;
-      }
-#pragma unroll
-      for (int i = 0; i < kSBatch; ++i) tmax = fmaxf(tmax, v[i]);
-    }
-  }
-  const float t = topk_lower_bound(tmax, k, wq);  // (its barrier also publishes misc[0] and misc[3])
-  int32_t* out_ids = topk_ids + static_cast<int64_t>(row) * a.k_max;
-  float* out_lp = topk_logprobs + static_cast<int64_t>(row) * a.k_max;
-
-  // ---- kept blocks (maximum >= t), listed per warp; the warp gathers their entries >= t ----
-  const T* rowp = reinterpret_cast<const T*>(a.logits) + static_cast<int64_t>(row) * a.row_stride;
-  int* wk = wkept[warp];
-  int nk = 0;  // the warp's kept blocks (uniform across the warp)
-  auto add_kept = [&](int b, bool keep) {
-    const unsigned m = __ballot_sync(0xffffffffu, keep);
-    if (keep) {
-      const int pos = nk + __popc(m & ((1u << lane) - 1u));
-      if (pos < kSWarpKept) wk[pos] = b;
-    }
-    nk += __popc(m);
-  };
-  if (one_round) {
-    // this thread's kept blocks as a bit mask; positions by a warp prefix sum of the counts
-    uint32_t kmask = 0;
-#pragma unroll
-    for (int i = 0; i < kSBatch; ++i) kmask |= ((tid + i * kSThreads < nb && bv[i] >= t) ? 1u : 0u) << i;
-    const int mine = __popc(kmask);
-    int incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    nk = __shfl_sync(0xffffffffu, incl, 31);
-    int pos = incl - mine;
-    while (kmask) {
-      const int i = __ffs(kmask) - 1;
-      kmask &= kmask - 1;
-      if (pos < kSWarpKept) wk[pos] = tid + i * kSThreads;
-      ++pos;
-    }
-  } else {
-    for (int base = 0; base < nb; base += kSBatch * kSThreads) {
-      float v[kSBatch];
-#pragma unroll
-      for (int i = 0; i < kSBatch; ++i) {
-        const int b = base + tid + i * kSThreads;
-        v[i] = b < nb ? bm[b] : -INFINITY;
-      }
-#pragma unroll
-      for (int i = 0; i < kSBatch; ++i) {
-        const int b = base + tid + i * kSThreads;
-        add_kept(b, b < nb && v[i] >= t);
-      }
-    }
-  }
-  __syncwarp();
-  auto add_cand = [&](float x, int e) {
-    if (x >= t) {
-      const uint32_t pos = atomicAdd(&misc[0], 1u);
-      if (pos < kSCandCap) cand[pos] = make_key(x, e);
-    }
-  };
-  if (nk > kSWarpKept) {
-    if (lane == 0) misc[3] = 1;  // more kept blocks than the list holds: exact path below
-  } else if (a.vec_ok) {
-    // 16-byte vectors of the kept blocks, kSGather per lane in flight; none straddles the row end.
-    // The warp's candidates are placed with one shared atomic: per-lane bit masks and a prefix sum.
-    const int n_vec = nk * VPB;
-    for (int base = 0; base < n_vec; base += kSGather * 32) {
-      uint4 w[kSGather];
-      int e0[kSGather];
-#pragma unroll
-      for (int u = 0; u < kSGather; ++u) {
-        const int j = base + u * 32 + lane;
-        e0[u] = -1;
-        if (j < n_vec) {
-          const int e = wk[j / VPB] * kBlock + (j % VPB) * EPV;
-          if (e < a.V) {
-            e0[u] = e;
-            w[u] = *reinterpret_cast<const uint4*>(rowp + e);
-          }
-        }
-      }
-      uint32_t cmask = 0;  // bit u * EPV + e: element e of vector u reaches t
-#pragma unroll
-      for (int u = 0; u < kSGather; ++u) {
-        float x[EPV];
-        VT::unpack(w[u], x);
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) cmask |= ((e0[u] >= 0 && x[e] >= t) ? 1u : 0u) << (u * EPV + e);
-      }
-      const int mine = __popc(cmask);
-      int incl = mine;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int total = __shfl_sync(0xffffffffu, incl, 31);
-      uint32_t wbase = 0;
-      if (lane == 31 && total > 0) wbase = atomicAdd(&misc[0], static_cast<uint32_t>(total));
-      wbase = __shfl_sync(0xffffffffu, wbase, 31);
-      uint32_t pos = wbase + static_cast<uint32_t>(incl - mine);
-#pragma unroll
-      for (int u = 0; u < kSGather; ++u) {
-        uint32_t mu = (cmask >> (u * EPV)) & ((1u << EPV) - 1u);
-        if (!mu) continue;
-        float x[EPV];
-        VT::unpack(w[u], x);
-        while (mu) {
-          const int e = __ffs(mu) - 1;
-          mu &= mu - 1;
-          float v = x[0];  // x[e] without dynamic register indexing
-#pragma unroll
-          for (int ee = 1; ee < EPV; ++ee) v = (e == ee) ? x[ee] : v;
-          if (pos < kSCandCap) cand[pos] = make_key(v, e0[u] + e);
-          ++pos;
-        }
-      }
-    }
-  } else {
-    const int n_el = nk * kBlock;
-    for (int j = lane; j < n_el; j += 32) {
-      const int e = wk[j / kBlock] * kBlock + (j % kBlock);
-      if (e < a.V) add_cand(VT::at(rowp, e), e);
-    }
-  }
-  if (warp == 0) row_lse();
-  __syncthreads();
-  int cnt = static_cast<int>(misc[0]);
-  const float lse = s_lse;
-  if (cnt > kSCandCap || misc[3] != 0) {
-    // too many entries reach t (ties, rows of -inf): the exact k-th key over
-    // them, then the k keys at or above it
-    auto in_set = [&](int i, uint64_t* key) -> bool {
-      if (i >= a.V || !(bm[i / kBlock] >= t)) return false;
-      const float x = VT::at(rowp, i);
-      if (!(x >= t)) return false;
-      *key = make_key(x, i);
-      return true;
-    };
-    int above;
-    const int n_items = nb * kBlock;
-    const uint64_t T64 = cta_radix_select(in_set, n_items, k, 64, hist, misc + 1, &above);
-    __syncthreads();
-    if (tid == 0) misc[0] = 0;
-    __syncthreads();
-    for (int i = tid; i < n_items; i += kSThreads) {
-      uint64_t key = 0;
-      if (in_set(i, &key) && key >= T64) {
-        const uint32_t pos = atomicAdd(&misc[0], 1u);  // exactly k of them
-        if (pos < kSCandCap) cand[pos] = key;
-      }
-    }
-    __syncthreads();
-    cnt = min(k, static_cast<int>(misc[0]));
-  }
-  // ---- exact order by rank (keys are unique): G threads per candidate ----
-  int G = 1;  // a power of two <= 32 with G * cnt <= kSThreads, at least 1
-  while (G < 32 && 2 * G * cnt <= kSThreads) G *= 2;
-  const int groups = kSThreads / G;
-  for (int base = 0; base < cnt; base += groups) {
-    const int i = base + tid / G, sub = tid % G;
-    const uint64_t key = i < cnt ? cand[i] : 0ull;
-    int rank = 0;
-    if (i < cnt)
-      for (int j = sub; j < cnt; j += G) rank += cand[j] > key;
-    for (int o = G / 2; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-    if (i < cnt && sub == 0 && rank < k) {
-      out_ids[rank] = key_id(key);
-      out_lp[rank] = key_value(key) - lse;
-    }
-  }
-  for (int r = min(cnt, k) + tid; r < a.k_max; r += kSThreads) {  // ranks without a candidate, and ranks >= k
-    out_ids[r] = -1;
-    out_lp[r] = -INFINITY;
-  }
+  select_row<T, kSThreads, 16>(a, blockIdx.x, threadIdx.x, sm, lse_out, sel_logprob, topk_ids, topk_logprobs);
 }
 
 // ---------------------------------------------------------------------------
@@ -983,7 +1068,7 @@ cudaError_t logits_reduce_setup() {
 size_t stream_partials_bytes(int rows, const VocabSplit& vs) {
   auto al = [](size_t n) { return (n + 255) & ~static_cast<size_t>(255); };
   return al(static_cast<size_t>(rows) * vs.slots * 8) + al(static_cast<size_t>(rows) * 4) +
-         al(static_cast<size_t>(rows) * vs.nblk * 4) + al(4);
+         al(static_cast<size_t>(rows) * vs.nblk * 4) + al(4) + al(static_cast<size_t>(rows) * 4);
 }
 
 Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs) {
@@ -997,6 +1082,8 @@ Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs) {
   out.bmax = reinterpret_cast<float*>(p);
   p += al(static_cast<size_t>(rows) * vs.nblk * 4);
   out.ticket = reinterpret_cast<unsigned int*>(p);
+  p += al(4);
+  out.row_done = reinterpret_cast<unsigned int*>(p);
   out.part_keys = nullptr;
   out.part_samp = nullptr;
   return out;
@@ -1011,18 +1098,26 @@ static cudaError_t launch_both(ReduceArgs a, const VocabSplit& split, float* lse
     a.cpr = (a.nblk + CH - 1) / CH;
     const int64_t chunks = static_cast<int64_t>(a.rows) * a.cpr;
     const int grid = static_cast<int>(chunks < split.ctas ? chunks : split.ctas);
+    // the stream kernel selects every row itself (the CTA that completes the row's last chunk)
+    a.lse = lse;
+    a.sel_logprob = sel_logprob;
+    a.topk_ids = topk_ids;
+    a.topk_logprobs = topk_logprobs;
+    const int reset_grid = a.rows / 256 + 1 < 64 ? a.rows / 256 + 1 : 64;
     trace_begin(kTraceReset, stream);
-    e = launch_kernel(ticket_reset_kernel, dim3(1), dim3(32), 0, stream, true, a.parts.ticket);
+    e = launch_kernel(counters_reset_kernel, dim3(reset_grid), dim3(256), 0, stream, true, a.parts.ticket,
+                      a.parts.row_done, a.rows);
     trace_end(kTraceReset, stream);
     if (e != cudaSuccess) return e;
     trace_begin(kTraceReduce, stream);
     e = launch_kernel(logits_stream_tma_kernel<T>, dim3(grid), dim3(kTThreads), static_cast<size_t>(kTSmem), stream,
                       true, a);
-  } else {
-    a.cpr = 0;
-    trace_begin(kTraceReduce, stream);
-    e = launch_kernel(logits_stream_regs_kernel<T>, dim3(split.grid), dim3(kRThreads), 0, stream, false, a);
+    trace_end(kTraceReduce, stream);
+    return e;
   }
+  a.cpr = 0;
+  trace_begin(kTraceReduce, stream);
+  e = launch_kernel(logits_stream_regs_kernel<T>, dim3(split.grid), dim3(kRThreads), 0, stream, false, a);
   trace_end(kTraceReduce, stream);
   if (e != cudaSuccess) return e;
   trace_begin(kTraceLogitsSelect, stream);
@@ -1058,6 +1153,9 @@ cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t ro
   a.k_max = k_max;
   a.parts = parts;
   a.dev_status = dev_status;
+  a.wait_ns = wait_limit_ns();
+  a.lse = a.sel_logprob = a.topk_logprobs = nullptr;
+  a.topk_ids = nullptr;
   cudaError_t e;
   switch (dtype) {
     case LMH_BF16:

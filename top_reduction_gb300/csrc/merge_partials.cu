@@ -27,7 +27,27 @@ struct MergeArgs {
   float* topk_logprobs;
   uint32_t* dev_status;
   SampleArgs samp;
+  RecordOut rec;  // rec.base != null: write each row's vocabulary-parallel record instead of results
 };
+
+// The row's record (vocabulary-parallel share) and its keys.
+__device__ __forceinline__ VocabRecord* row_record(const MergeArgs& a, int row) {
+  return reinterpret_cast<VocabRecord*>(a.rec.base + static_cast<int64_t>(row) * record_bytes(a.k_max));
+}
+__device__ __forceinline__ unsigned long long* record_keys(VocabRecord* r) {
+  return reinterpret_cast<unsigned long long*>(r + 1);
+}
+
+// Record mode: the share's (M, S), and the selected logit when the token lies in the share.
+__device__ __forceinline__ void write_record_head(const MergeArgs& a, int row, float M, float S) {
+  VocabRecord* r = row_record(a, row);
+  const int t = a.sel ? a.sel[row] : -1;
+  const bool has = t >= a.rec.v_begin && t < a.rec.v_begin + a.rec.v_count;
+  r->m = M;
+  r->s = M == -INFINITY ? 0.0f : S;
+  r->sel_logit = has ? a.parts.sel_logit[row] : 0.0f;
+  r->flags = has ? kRecordHasSel : 0u;
+}
 
 // Sampling partials (score, id bits, z, -): a beats b when it has a token and a
 // higher score, ties to the smaller id (the order in which one stream meets them).
@@ -151,7 +171,11 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_partials_kernel(const 
   }
   const float S = block_sum(sloc, red);
   const float lse = (M == -INFINITY) ? -INFINITY : M + logf(S);
-  if (tid == 0) {
+  const bool rec_mode = a.rec.base != nullptr;
+  if (tid == 0 && rec_mode) {
+    write_record_head(a, row, M, S);
+    misc[0] = 0;
+  } else if (tid == 0) {
     a.lse[row] = lse;
     if (a.sel) {
       float v = __int_as_float(0x7fc00000);  // NaN: no selected token / out of range
@@ -165,13 +189,20 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_partials_kernel(const 
   }
   if (a.samp.enabled) cta_sample(a, row, nslots, lse);  // the sampled token: the best slot partial
   if (a.k_max == 0) return;
-  int32_t* out_ids = a.topk_ids + static_cast<int64_t>(row) * a.k_max;
-  float* out_lp = a.topk_logprobs + static_cast<int64_t>(row) * a.k_max;
-  if (k == 0) {
-    for (int r = tid; r < a.k_max; r += kMergeThreads) {
-      out_ids[r] = -1;
-      out_lp[r] = -INFINITY;
+  int32_t* out_ids = rec_mode ? nullptr : a.topk_ids + static_cast<int64_t>(row) * a.k_max;
+  float* out_lp = rec_mode ? nullptr : a.topk_logprobs + static_cast<int64_t>(row) * a.k_max;
+  unsigned long long* out_keys = rec_mode ? record_keys(row_record(a, row)) : nullptr;
+  // rank r: the key (record mode) or its id and logprob (key 0: no entry)
+  auto put = [&](int r, uint64_t key) {
+    if (rec_mode) {
+      out_keys[r] = key;
+    } else {
+      out_ids[r] = key ? key_id(key) : -1;
+      out_lp[r] = key ? key_value(key) - lse : -INFINITY;
     }
+  };
+  if (k == 0) {
+    for (int r = tid; r < a.k_max; r += kMergeThreads) put(r, 0ull);
     return;
   }
 
@@ -281,36 +312,59 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_partials_kernel(const 
     if (i < cnt)
       for (int j = sub; j < cnt; j += G) rank += cand[j] > key;
     for (int o = G / 2; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-    if (i < cnt && sub == 0 && rank < k) {
-      out_ids[rank] = key_id(key);
-      out_lp[rank] = key_value(key) - lse;
-    }
+    if (i < cnt && sub == 0 && rank < k) put(rank, key);
   }
-  for (int r = min(cnt, k) + tid; r < a.k_max; r += kMergeThreads) {  // ranks without a candidate, and ranks >= k
-    out_ids[r] = -1;
-    out_lp[r] = -INFINITY;
-  }
+  for (int r = min(cnt, k) + tid; r < a.k_max; r += kMergeThreads) put(r, 0ull);  // no candidate, and ranks >= k
 }
 
 // ---------------------------------------------------------------------------
 // One warp per row, for plans whose slots hold at most kWarpItems keys per row
-// (many rows, few slots: the CTA-wide barriers of the kernel above would
-// dominate).  Same steps; every candidate fits the warp's buffer, so there
-// is no overflow path.
+// and lists of at most kWarpMaxK entries (few slots, or short lists: the
+// CTA-wide barriers of the kernel above would dominate).  The row's keys are
+// held in registers, 16 per lane; the output ranks come out of a tournament:
+// every round the warp's largest remaining key (two redux.sync max steps, on
+// the high then the low word; keys are unique, so exactly one lane holds it)
+// is the next rank, and its holder drops it and recomputes its own best.  k
+// rounds, no shared memory and no ranking pass.
 // ---------------------------------------------------------------------------
 constexpr int kWarpItems = 512;
-constexpr int kWarpRowsPerCta = 8;
+constexpr int kWarpPerLane = kWarpItems / 32;
+constexpr int kWarpMaxK = 32;
+constexpr int kWarpRowsPerCtaMax = 8;
 
-__global__ void __launch_bounds__(kWarpRowsPerCta * 32) merge_partials_warp_kernel(const MergeArgs a) {
-  __shared__ uint64_t sbuf[kWarpRowsPerCta][kWarpItems];
+__device__ __forceinline__ uint64_t max_of(const uint64_t (&kv)[kWarpPerLane]) {
+  uint64_t m = kv[0];
+#pragma unroll
+  for (int t = 1; t < kWarpPerLane; ++t) m = kv[t] > m ? kv[t] : m;
+  return m;
+}
+
+__global__ void __launch_bounds__(kWarpRowsPerCtaMax * 32) merge_partials_warp_kernel(const MergeArgs a) {
   pdl_wait();  // the partials come from the kernel launched just before
   pdl_launch_dependents();  // a following kernel may be scheduled; it waits for this grid before using its results
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int row = blockIdx.x * kWarpRowsPerCta + w;
+  const int row = blockIdx.x * (blockDim.x >> 5) + w;
   if (row >= a.rows) return;
-  uint64_t* buf = sbuf[w];
   const int nslots = a.splits;
   const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.splits;
+
+  // ---- every independent load first: K, the row's keys, the slots' (m, s) ----
+  int k = a.k_max;
+  if (a.row_k) k = min(max(a.row_k[row], 0), a.k_max);
+  const unsigned long long* keys = a.parts.part_keys + static_cast<int64_t>(row) * a.splits * a.k_max;
+  // item i = (slot i / k, rank i % k) of the slots' sorted lists; only the first k of a
+  // list can reach the row's top k
+  const int n_items = nslots * k;
+  uint64_t kv[kWarpPerLane];
+#pragma unroll
+  for (int t = 0; t < kWarpPerLane; ++t) {
+    const int i = lane + 32 * t;
+    kv[t] = 0;
+    if (i < n_items) {
+      const int j = i / k;
+      kv[t] = keys[static_cast<int64_t>(j) * a.k_max + (i - j * k)];
+    }
+  }
 
   // ---- lse ----
   float tm = -INFINITY, ts = 0.0f;
@@ -325,7 +379,10 @@ __global__ void __launch_bounds__(kWarpRowsPerCta * 32) merge_partials_warp_kern
   const float M = warp_max(tm);
   const float S = warp_sum((tm == -INFINITY) ? 0.0f : ts * expf(tm - M));
   const float lse = (M == -INFINITY) ? -INFINITY : M + logf(S);
-  if (lane == 0) {
+  const bool rec_mode = a.rec.base != nullptr;
+  if (lane == 0 && rec_mode) {
+    write_record_head(a, row, M, S);
+  } else if (lane == 0) {
     a.lse[row] = lse;
     if (a.sel) {
       const int t = a.sel[row];
@@ -348,82 +405,76 @@ __global__ void __launch_bounds__(kWarpRowsPerCta * 32) merge_partials_warp_kern
     if (lane == 0) samp_write(a, row, b, lse);
   }
   if (a.k_max == 0) return;
-  int k = a.k_max;
-  if (a.row_k) k = min(max(a.row_k[row], 0), a.k_max);
-  int32_t* out_ids = a.topk_ids + static_cast<int64_t>(row) * a.k_max;
-  float* out_lp = a.topk_logprobs + static_cast<int64_t>(row) * a.k_max;
-  if (k == 0) {
-    for (int r = lane; r < a.k_max; r += 32) {
+  int32_t* out_ids = rec_mode ? nullptr : a.topk_ids + static_cast<int64_t>(row) * a.k_max;
+  float* out_lp = rec_mode ? nullptr : a.topk_logprobs + static_cast<int64_t>(row) * a.k_max;
+  unsigned long long* out_keys = rec_mode ? record_keys(row_record(a, row)) : nullptr;
+
+  // ---- tournament: rank r is the largest key left after ranks 0..r-1 ----
+  uint64_t best = max_of(kv);
+  int32_t my_id = -1;  // lane r % 32 keeps rank r's result for a coalesced store
+  float my_lp = -INFINITY;
+  uint64_t my_key = 0;
+  for (int r = 0; r < k; ++r) {
+    const uint32_t hi = __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(best >> 32));
+    const uint32_t lo =
+        __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(best >> 32) == hi ? static_cast<uint32_t>(best) : 0u);
+    const uint64_t key = (static_cast<uint64_t>(hi) << 32) | lo;
+    if (key != 0ull && best == key) {  // the one holder drops it
+#pragma unroll
+      for (int t = 0; t < kWarpPerLane; ++t) kv[t] = kv[t] == key ? 0ull : kv[t];
+      best = max_of(kv);
+    }
+    if (lane == (r & 31)) {  // key 0: fewer than k candidates
+      my_key = key;
+      my_id = key ? key_id(key) : -1;
+      my_lp = key ? key_value(key) - lse : -INFINITY;
+    }
+    if ((r & 31) == 31 || r == k - 1) {
+      const int r0 = r & ~31;
+      if (lane <= (r & 31)) {
+        if (rec_mode) {
+          out_keys[r0 + lane] = my_key;
+        } else {
+          out_ids[r0 + lane] = my_id;
+          out_lp[r0 + lane] = my_lp;
+        }
+      }
+    }
+  }
+  for (int r = k + lane; r < a.k_max; r += 32) {  // ranks >= k
+    if (rec_mode) {
+      out_keys[r] = 0ull;
+    } else {
       out_ids[r] = -1;
       out_lp[r] = -INFINITY;
     }
-    return;
   }
-  const unsigned long long* keys = a.parts.part_keys + static_cast<int64_t>(row) * a.splits * a.k_max;
+}
 
-  // ---- lb: the k-th largest of the slots' q leading keys (q = ceil(k / nslots)) ----
-  const int q = (k + nslots - 1) / nslots;
-  const int nu = q * nslots;  // <= nslots * k <= kWarpItems
-  for (int i = lane; i < nu; i += 32) {
-    const int j = i / q;
-    buf[i] = keys[static_cast<int64_t>(j) * a.k_max + (i - j * q)];
+// ---------------------------------------------------------------------------
+// vocabulary-parallel records -> the merge's partials (one slot per part)
+// ---------------------------------------------------------------------------
+// Thread t of row r copies part t's (m, s) and keys; the part whose share holds
+// the selected token provides its logit.
+__global__ void __launch_bounds__(128) unpack_records_kernel(const unsigned char* __restrict__ records,
+                                                             int num_parts, int rows, int k_max, Partials parts) {
+  const int row = blockIdx.x;
+  const size_t rb = record_bytes(k_max);
+  for (int p = threadIdx.x; p < num_parts; p += blockDim.x) {
+    const VocabRecord* r =
+        reinterpret_cast<const VocabRecord*>(records + (static_cast<int64_t>(p) * rows + row) * rb);
+    const int64_t slot = static_cast<int64_t>(row) * num_parts + p;
+    parts.part_ms[slot] = make_float2(r->m, r->s);
+    const unsigned long long* keys = reinterpret_cast<const unsigned long long*>(r + 1);
+    for (int j = 0; j < k_max; ++j) parts.part_keys[slot * k_max + j] = keys[j];
+    if (r->flags & kRecordHasSel) parts.sel_logit[row] = r->sel_logit;
   }
-  __syncwarp();
-  uint64_t lb = 0;
-  for (int base = 0; base < nu; base += 32) {
-    const int i = base + lane;
-    uint64_t key = 0;
-    bool hit = false;
-    if (i < nu) {
-      key = buf[i];
-      int rank = 0;  // by key desc, then position asc
-      for (int j = 0; j < nu; ++j) {
-        const uint64_t o = buf[j];
-        rank += (o > key) | ((o == key) & (j < i));
-      }
-      hit = rank == k - 1;
-    }
-    const unsigned m = __ballot_sync(0xffffffffu, hit);
-    if (m) lb = __shfl_sync(0xffffffffu, key, __ffs(m) - 1);
-  }
-  __syncwarp();
+}
 
-  // ---- gather the keys >= lb (loads first, then a ballot compaction) ----
-  const int n_items = nslots * k;
-  constexpr int kPer = kWarpItems / 32;
-  uint64_t kv[kPer];
-#pragma unroll
-  for (int t = 0; t < kPer; ++t) {
-    const int i = lane + 32 * t;
-    kv[t] = 0;
-    if (i < n_items) {
-      const int j = i / k;
-      kv[t] = keys[static_cast<int64_t>(j) * a.k_max + (i - j * k)];
-    }
-  }
-  int cnt = 0;
-#pragma unroll
-  for (int t = 0; t < kPer; ++t) {
-    const bool pass = kv[t] != 0ull && kv[t] >= lb;
-    const unsigned m = __ballot_sync(0xffffffffu, pass);
-    if (pass) buf[cnt + __popc(m & ((1u << lane) - 1u))] = kv[t];
-    cnt += __popc(m);
-  }
-  __syncwarp();
-  // ---- exact order by rank (keys are unique) ----
-  for (int i = lane; i < cnt; i += 32) {
-    const uint64_t key = buf[i];
-    int rank = 0;
-    for (int j = 0; j < cnt; ++j) rank += buf[j] > key;
-    if (rank < k) {
-      out_ids[rank] = key_id(key);
-      out_lp[rank] = key_value(key) - lse;
-    }
-  }
-  for (int r = min(cnt, k) + lane; r < a.k_max; r += 32) {  // ranks without a candidate, and ranks >= k
-    out_ids[r] = -1;
-    out_lp[r] = -INFINITY;
-  }
+cudaError_t launch_unpack_records(const void* records, int num_parts, int rows, int k_max, Partials parts,
+                                  cudaStream_t stream) {
+  return launch_kernel(unpack_records_kernel, dim3(rows), dim3(128), 0, stream, false,
+                       static_cast<const unsigned char*>(records), num_parts, rows, k_max, parts);
 }
 
 cudaError_t merge_setup() { return cudaSuccess; }
@@ -431,7 +482,7 @@ cudaError_t merge_setup() { return cudaSuccess; }
 cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts, const int32_t* sel,
                          const int32_t* row_k, float* lse, float* sel_logprob, int32_t* topk_ids,
                          float* topk_logprobs, uint32_t* dev_status, cudaStream_t stream, bool pdl,
-                         const SampleArgs* samp) {
+                         const SampleArgs* samp, int num_sms, const RecordOut* rec) {
   MergeArgs a;
   a.rows = rows;
   a.splits = splits;
@@ -446,9 +497,15 @@ cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts,
   a.topk_logprobs = topk_logprobs;
   a.dev_status = dev_status;
   a.samp = samp ? *samp : SampleArgs{};
-  if (static_cast<int64_t>(splits) * k_max <= kWarpItems)
-    return launch_kernel(merge_partials_warp_kernel, dim3((rows + kWarpRowsPerCta - 1) / kWarpRowsPerCta),
-                         dim3(kWarpRowsPerCta * 32), 0, stream, pdl, a);
+  a.rec = rec ? *rec : RecordOut{nullptr, 0, 0};
+  if (static_cast<int64_t>(splits) * k_max <= kWarpItems && k_max <= kWarpMaxK) {
+    // rows spread over the SMs first: one warp per CTA while there are SMs to spare
+    const int sms = num_sms > 0 ? num_sms : 1;
+    int rpc = 1;
+    while (rpc < kWarpRowsPerCtaMax && static_cast<int64_t>(rows) > static_cast<int64_t>(2 * rpc) * sms) rpc *= 2;
+    return launch_kernel(merge_partials_warp_kernel, dim3((rows + rpc - 1) / rpc), dim3(rpc * 32), 0, stream, pdl,
+                         a);
+  }
   return launch_kernel(merge_partials_kernel, dim3(rows), dim3(kMergeThreads), 0, stream, pdl, a);
 }
 

@@ -9,20 +9,25 @@
 //     framework's allocator;
 //   * latency-critical loops where cudaMalloc / cudaFree would synchronise
 //     the device.
-// This variant runs the same two kernels as lmh_logprobs_from_logits
-// (logits stream + per-row select) but keeps their intermediate results in a
-// fixed array in the library's own device memory, so the call allocates
-// nothing.
+// This variant runs the same kernels as lmh_logprobs_from_logits (the
+// counter reset and the logits stream with its per-row select, or the
+// plain-load stream and a select kernel) but keeps their intermediate results
+// in a fixed array in the library's own device memory, so the call allocates
+// nothing.  Its launches are recorded by the kernel trace like those of the
+// workspace entry point (launch_logits_reduce brackets every launch).
 //
 // Limits and sharing:
 //   * the array holds kStaticScratchBytes (8 MiB) on every GPU that loads
 //     the library, until the process exits;
 //   * requests whose partials do not fit are rejected with
-//     LMH_ERR_WORKSPACE_TOO_SMALL before anything is launched;
+//     LMH_ERR_WORKSPACE_TOO_SMALL before anything is launched (about
+//     rows * (4 * ceil(V / 64) + 8 * slots + 8) bytes: up to 479 rows of
+//     248320 logits, 782 rows of 151936);
 //   * every call uses the same array and it keeps the previous call's
-//     contents; nothing in it needs to start at zero (each call writes every
-//     slot it reads), but calls that overlap on the GPU (two streams, or two
-//     threads) race on it and must be serialised by the caller;
+//     contents; nothing in it needs to start at zero (each call zeroes its
+//     counters in its first kernel and writes every other slot it reads),
+//     but calls that overlap on the GPU (two streams, or two threads) race on
+//     it and must be serialised by the caller;
 //   * the first call on each device does a one-time set-up with that device
 //     current (kernel attributes and the array's device address through
 //     cudaGetSymbolAddress); make that first call before any stream capture.

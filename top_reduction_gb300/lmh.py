@@ -39,7 +39,8 @@ EXPORTS = ("lmh_select_rows", "lmh_count_selected_rows", "lmh_workspace_bytes",
            "lmh_project_logprobs", "lmh_project_logprobs_scaled", "lmh_project_logprobs_sample",
            "lmh_probe_selective",
            "lmh_logprobs_from_logits", "lmh_status_string",
-           "lmh_version", "lmh_trace_enable", "lmh_trace_read", "lmh_trace_reset")
+           "lmh_version", "lmh_trace_enable", "lmh_trace_read", "lmh_trace_reset", "lmh_debug_set_wait_limit",
+           "lmh_record_bytes", "lmh_project_partials", "lmh_merge_workspace_bytes", "lmh_merge_records")
 
 _lib = None
 
@@ -90,6 +91,17 @@ def load():
     lib.lmh_trace_read.argtypes = [ctypes.c_char_p, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]
     lib.lmh_trace_read.restype = ctypes.c_int
     lib.lmh_trace_reset.restype = None
+    lib.lmh_debug_set_wait_limit.argtypes = [ctypes.c_uint64]
+    lib.lmh_debug_set_wait_limit.restype = ctypes.c_int
+    lib.lmh_record_bytes.argtypes = [i32]
+    lib.lmh_record_bytes.restype = u64
+    lib.lmh_project_partials.argtypes = [P, i64, i32, P, i32, i32, P, ctypes.c_int, i32, i32, i32, P, P, i32,
+                                         P, P, u64, P, P]
+    lib.lmh_project_partials.restype = ctypes.c_int
+    lib.lmh_merge_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.lmh_merge_workspace_bytes.restype = u64
+    lib.lmh_merge_records.argtypes = [P, i32, i32, i32, P, P, i32, P, P, P, P, P, u64, P, P]
+    lib.lmh_merge_records.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -300,7 +312,7 @@ def logprobs_from_logits(logits, sel=None, row_k=None, k_max=0, workspace=None, 
 # ---------------------------------------------------------------------------
 
 TRACE_KERNELS = ("select_rows", "gather_rows", "head_logprobs", "logits_reduce", "merge_partials",
-                 "logits_select", "ticket_reset", "full_logprobs")
+                 "logits_select", "counters_reset", "full_logprobs")
 
 
 def trace_enable(on=True):
@@ -317,3 +329,111 @@ def trace_read(kernel):
     ms = ctypes.c_double(0.0)
     _check(load().lmh_trace_read(kernel.encode(), ctypes.byref(n), ctypes.byref(ms)), "lmh_trace_read")
     return int(n.value), float(ms.value)
+
+
+def debug_set_wait_limit(limit_ns):
+    """Test hook: the kernels' bounded waits give up after limit_ns (0: the 2 s default)."""
+    _check(load().lmh_debug_set_wait_limit(int(limit_ns)), "lmh_debug_set_wait_limit")
+
+
+# ---------------------------------------------------------------------------
+# vocabulary-parallel head (several GPUs, each holding a share of the vocabulary)
+# ---------------------------------------------------------------------------
+
+def vocab_share(V, rank, world):
+    """(v_begin, v_count): rank's share of token ids [0, V), whole 64-id blocks spread as
+    evenly as possible (the last share takes the ragged tail).  Pure host arithmetic."""
+    assert 0 <= rank < world and V >= 1
+    nblk = (V + 63) // 64
+    lo = (nblk * rank) // world
+    hi = (nblk * (rank + 1)) // world
+    begin, end = 64 * lo, min(V, 64 * hi)
+    return begin, max(0, end - begin)
+
+
+def record_bytes(k_max):
+    """Bytes of one row's record (include/lmh.h: lmh_record_bytes)."""
+    n = int(load().lmh_record_bytes(int(k_max)))
+    if n == 0:
+        raise LMHError(ERR_INVALID_ARG, "lmh_record_bytes")
+    return n
+
+
+def project_partials(hidden, W_share, v_begin, V, row_idx=None, rows=None, sel=None, row_k=None, k_max=0,
+                     records=None, workspace=None, dev_status=None, stream=None):
+    """One share of a vocabulary-parallel head (lmh_project_partials).
+
+    W_share: bf16 [v_count, H], rows v_begin.. of lm_head.weight; sel holds global ids.
+    Returns the uint8 [rows, record_bytes(k_max)] record buffer.
+    """
+    assert hidden.is_cuda and hidden.dtype == torch.bfloat16 and hidden.dim() == 2 and hidden.stride(1) == 1
+    assert W_share.is_cuda and W_share.dtype == torch.bfloat16 and W_share.is_contiguous()
+    T, H = hidden.shape
+    v_count = W_share.shape[0]
+    assert W_share.shape[1] == H
+    dev = hidden.device
+    if row_idx is not None:
+        rows = row_idx.numel() if rows is None else rows
+        assert row_idx.dtype == torch.int32 and row_idx.is_cuda
+    elif rows is None:
+        rows = T
+    sel_t = _dev_i32(sel, dev, rows, "sel")
+    rk_t = _dev_i32(row_k, dev, rows, "row_k")
+    rb = record_bytes(k_max)
+    if records is None:
+        records = torch.empty((rows, rb), dtype=torch.uint8, device=dev)
+    assert records.is_cuda and records.is_contiguous() and records.numel() >= rows * rb
+    ws = _workspace(workspace, workspace_bytes(rows, H, v_count, k_max, PATH_PROJECT), dev)
+    _check(load().lmh_project_partials(
+        _p(hidden), hidden.stride(0) if T > 1 else H, T, _p(row_idx), int(rows), H, _p(W_share), W_VH,
+        int(v_begin), int(v_count), int(V), _p(sel_t), _p(rk_t), int(k_max), _p(records), _p(ws),
+        ws.numel() * ws.element_size(), _p(dev_status), _stream(stream)), "lmh_project_partials")
+    return records
+
+
+def merge_records(records, num_parts, rows, V, sel=None, row_k=None, k_max=0, workspace=None, dev_status=None,
+                  out=None, stream=None):
+    """Final results from the gathered records [num_parts, rows, record_bytes] (lmh_merge_records)."""
+    assert records.is_cuda and records.is_contiguous()
+    dev = records.device
+    sel_t = _dev_i32(sel, dev, rows, "sel")
+    rk_t = _dev_i32(row_k, dev, rows, "row_k")
+    o = out if out is not None else _outputs(rows, k_max, sel_t is not None, dev, V)
+    need = int(load().lmh_merge_workspace_bytes(int(rows), int(num_parts), int(k_max)))
+    if need == 0:
+        raise LMHError(ERR_INVALID_ARG, "lmh_merge_workspace_bytes")
+    ws = _workspace(workspace, need, dev)
+    _check(load().lmh_merge_records(
+        _p(records), int(num_parts), int(rows), int(V), _p(sel_t), _p(rk_t), int(k_max), _p(o["lse"]),
+        _p(o["sel_logprob"]), _p(o["topk_ids"]), _p(o["topk_logprobs"]), _p(ws), ws.numel() * ws.element_size(),
+        _p(dev_status), _stream(stream)), "lmh_merge_records")
+    return o
+
+
+def gather_records(records, group=None):
+    """All-gather of every rank's record buffer, in rank order: [world, *records.shape].
+
+    The one exchange step of the vocabulary-parallel head (a collective of the
+    caller's torch.distributed group: NCCL into device memory on GPUs, gloo on the
+    host).  Pure plumbing: the records are opaque bytes here.
+    """
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    out = torch.empty((world,) + tuple(records.shape), dtype=records.dtype, device=records.device)
+    if dist.get_backend(group) == "nccl":
+        dist.all_gather_into_tensor(out, records.contiguous(), group=group)
+    else:
+        dist.all_gather(list(out.unbind(0)), records.contiguous(), group=group)
+    return out
+
+
+def vocab_parallel_logprobs(hidden, W_share, v_begin, V, row_idx=None, rows=None, sel=None, row_k=None, k_max=0,
+                            group=None, dev_status=None, stream=None):
+    """The rows' O(k+1) results with the head split over the ranks of `group` by vocabulary:
+    this rank's share (project_partials), one all-gather of the records, the merge."""
+    rec = project_partials(hidden, W_share, v_begin, V, row_idx=row_idx, rows=rows, sel=sel, row_k=row_k,
+                           k_max=k_max, dev_status=dev_status, stream=stream)
+    allrec = gather_records(rec, group)
+    n = rec.shape[0]
+    return merge_records(allrec, allrec.shape[0], n, V, sel=sel, row_k=row_k, k_max=k_max, dev_status=dev_status,
+                         stream=stream)
