@@ -450,10 +450,8 @@ int32_t lmh_version(void);
  * lmh_trace_read waits for the recorded events, then reports the launches
  * and total milliseconds of the named kernel ("select_rows", "gather_rows",
  * "head_logprobs", "merge_partials", "logits_reduce" (the streaming pass of
- * lmh_logprobs_from_logits; with 16-byte aligned rows it also selects every
- * row), "logits_select" (the per-row selection after the plain-load pass),
- * "counters_reset" (the reset of the chunk and row counters before the
- * streaming pass),
+ * lmh_logprobs_from_logits), "logits_select" (its per-row selection),
+ * "ticket_reset" (the chunk-counter reset before the streaming pass),
  * "full_logprobs" (the pass that writes the k_max = LMH_K_FULL output)) since
  * the last reset.
  * lmh_trace_reset clears the totals.

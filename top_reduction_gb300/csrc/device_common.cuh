@@ -170,6 +170,18 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return p;
 }
 
+// L2 policy for data read again soon: its lines are evicted last.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// fp32 store with an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void st_keep(float* dst, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(dst), "f"(v), "l"(policy) : "memory");
+}
+
 // bulk_load with an L2 cache policy (from createpolicy).
 __device__ __forceinline__ void bulk_load_hint(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar,
                                                uint64_t policy) {

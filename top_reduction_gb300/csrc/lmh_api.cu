@@ -67,7 +67,6 @@ Partials carve_partials(void* base, int rows, int splits, int k_max) {
   out.part_samp = reinterpret_cast<float4*>(p);
   out.bmax = nullptr;
   out.ticket = nullptr;
-  out.row_done = nullptr;
   return out;
 }
 
@@ -76,7 +75,7 @@ Partials carve_partials(void* base, int rows, int splits, int k_max) {
 // ---------------------------------------------------------------------------
 static const char* const kTraceNames[kTraceCount] = {"select_rows",   "gather_rows",    "head_logprobs",
                                                      "logits_reduce", "merge_partials", "logits_select",
-                                                     "counters_reset", "full_logprobs"};
+                                                     "ticket_reset",  "full_logprobs"};
 
 struct TraceRecord {
   int kernel;

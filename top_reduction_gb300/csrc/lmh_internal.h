@@ -39,7 +39,6 @@ struct Partials {
   unsigned int* ticket;  // standalone reduction: chunk counter of the dynamic schedule (else unused)
   float4* part_samp;     // head path: per-(row, split) sampling partial (best score, id bits, z, -)
   float* bmax;  // standalone reduction: block maxima [rows * nblk] (else unused)
-  unsigned int* row_done;  // standalone reduction: chunks of each row completed (else unused)
 };
 
 // Device-side sampling on the head path (lmh_project_logprobs_sample): Gumbel-max
@@ -104,13 +103,13 @@ cudaError_t launch_select_rows(const int32_t* cu, int num_seqs, int num_decode, 
                                cudaStream_t stream);
 
 // Workspace of the standalone reduction: part_ms [rows * slots], sel_logit
-// [rows], bmax [rows * nblk], the chunk counter, the per-row chunk counters.
+// [rows], bmax [rows * nblk], the chunk counter.
 size_t stream_partials_bytes(int rows, const VocabSplit& vs);
 Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs);
 
-// Counter reset and the stream kernel, which selects each row in the CTA that
-// completes it (16-byte aligned rows), or the register-path stream kernel and a
-// per-row select kernel; the results go straight to the outputs.
+// Ticket reset and the bulk-copy stream kernel (16-byte aligned rows), or the
+// register-path stream kernel; then the per-row select kernel, which writes the
+// outputs.
 cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t row_stride, int rows, int V,
                                  VocabSplit split, const int32_t* sel, const int32_t* row_k, int k_max,
                                  Partials parts, float* lse, float* sel_logprob, int32_t* topk_ids,

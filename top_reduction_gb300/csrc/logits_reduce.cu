@@ -13,29 +13,26 @@
 //     up the selected token's logit.
 //       - logits_stream_tma_kernel (rows and the row length 16-byte
 //         aligned; four CTAs per SM): the logits are cut into 16 KB chunks
-//         of one row, handed out dynamically (a ticket counter), so CTAs that
-//         get more bandwidth take more chunks.  One producer lane streams its
-//         chunks into a ring of shared-memory stages with bulk copies
-//         (cp.async.bulk, completion on mbarriers); four consumer warps read
-//         them, each thread owning 128 contiguous bytes (one bf16/f16 block,
-//         half an f32 block), so a block's maximum needs no exchange between
-//         lanes; one (m, s) pair per warp and chunk.  After each chunk the
-//         CTA counts it against its row; the CTA that counts a row's last
-//         chunk selects that row at once (select_row, below), while the other
-//         CTAs keep streaming, so only the last rows' selections follow the
-//         stream.  A small kernel before it zeroes the counters.
+//         of one row, handed out dynamically (a ticket counter, zeroed by a
+//         one-thread kernel before it), so CTAs that get more bandwidth take
+//         more chunks.  One producer lane streams its chunks into a ring of
+//         shared-memory stages with bulk copies (cp.async.bulk, completion on
+//         mbarriers); four consumer warps read them, each thread owning 128
+//         contiguous bytes (one bf16/f16 block, half an f32 block), so a
+//         block's maximum needs no exchange between lanes; one (m, s) pair
+//         per warp and chunk.
 //       - logits_stream_regs_kernel (any element-aligned layout; two CTAs
 //         per SM): the flattened (row, 64-block) space is cut into equal
 //         contiguous ranges, one per CTA; every thread loads 16-byte vectors
 //         (or elements at unaligned rows) straight into registers, two
 //         chunks in flight; the lanes of a block combine their maxima by
-//         shuffles; one (m, s) pair per row piece.  logits_select_kernel then
-//         selects every row, one CTA per row.
-//   * select_row -- lse from the row's (m, s) pairs (one warp); a lower bound
+//         shuffles; one (m, s) pair per row piece.
+//   * logits_select_kernel, one CTA per row, after the stream kernel
+//     (select_row): lse from the row's (m, s) pairs (one warp); a lower bound
 //     t on the row's k-th largest logit from the block maxima; candidates =
 //     entries >= t of the blocks whose maximum is >= t, re-read from memory
-//     (L2 for a row just streamed) by the warp that owns the block; their
-//     exact top-k by key (value desc, id asc), ordered by rank.
+//     with their 16-byte loads spread evenly over the CTA (one round trip);
+//     their exact top-k by key (value desc, id asc), ordered by rank.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -203,12 +200,6 @@ struct ReduceArgs {
   Partials parts;
   uint32_t* dev_status;
   uint64_t wait_ns;  // limit of a bounded wait on another role of the CTA
-  // TMA path: the CTA that completes a row's last chunk selects the row and
-  // writes these outputs itself
-  float* lse;
-  float* sel_logprob;
-  int32_t* topk_ids;
-  float* topk_logprobs;
 };
 
 // One chunk of a CTA's work: up to CH blocks of one row inside one range.
@@ -279,27 +270,27 @@ __device__ __forceinline__ int64_t piece_slot(const ReduceArgs& a, int row, int 
 // select_row() finishes one row from the stream kernel's results: lse from the
 // row's (m, s) slots, the selected token's logprob, and the exact top-k.  It is
 // run by a group of NT threads (whole warps, ranks tid = 0..NT-1) synchronised
-// on named barrier kSelBar: the four consumer warps of the stream CTA that
-// completed the row's last chunk (TMA path), or a CTA of its own per row
-// (logits_select_kernel, register path).  The block maxima, (m, s) slots and
-// selected logit were written by other CTAs of the same grid, so they are read
-// through L2 (ld.global.cg), never from a possibly stale L1 line.
+// on named barrier kSelBar: one CTA per row of logits_select_kernel, launched
+// after the stream kernel.  (Selecting a row inside the stream kernel, in the
+// CTA that completes it, was measured slower: each dependent load of a select
+// waits behind the stream's own traffic, and the CTA streams nothing meanwhile.)
+// The block maxima, (m, s) slots and selected logit come from the stream
+// kernel; they are read through L2 (ld.global.cg).
 constexpr int kSelBar = 1;      // named barrier of the selecting group
 constexpr int kSThreads = 256;  // logits_select_kernel
 constexpr int kSCandCap = 512;  // candidate keys held in shared memory
-constexpr int kSWarpKept = 64;  // kept blocks listed per warp
-constexpr int kSGather = 4;     // candidate vectors per lane in flight
+constexpr int kSKeptCap = 512;  // kept blocks listed per row
+constexpr int kSGather = 8;     // candidate vectors per thread in flight
 
 template <int NT>
 struct SelectSmem {
   static constexpr int kWarps = NT / 32;
   uint64_t cand[kSCandCap];
   uint32_t hist[256];
-  uint32_t misc[4];  // [0] candidates, [1..2] select broadcast, [3] kept-list overflow
+  uint32_t misc[4];  // [0] candidates, [1..2] select broadcast, [3] kept blocks
   float wq[kWarps];
-  int wkept[kWarps][kSWarpKept];
+  int kept[kSKeptCap];  // the row's kept blocks, in no particular order
   float lse;
-  int flag;  // stream kernel: the row this CTA's last count completed, or -1
 };
 
 // Lower bound on the k-th largest logit of a row from its block maxima.
@@ -452,28 +443,31 @@ __device__ void select_row(const ReduceArgs& a, int row, int tid, SelectSmem<NT>
   int32_t* out_ids = topk_ids + static_cast<int64_t>(row) * a.k_max;
   float* out_lp = topk_logprobs + static_cast<int64_t>(row) * a.k_max;
 
-  // ---- kept blocks (maximum >= t), listed per warp; the warp gathers their entries >= t ----
+  // ---- kept blocks (maximum >= t), one list for the row ----
   const T* rowp = reinterpret_cast<const T*>(a.logits) + static_cast<int64_t>(row) * a.row_stride;
-  int* wk = sm.wkept[warp];
-  int nk = 0;  // the warp's kept blocks (uniform across the warp)
-  if (one_round) {
-    // this thread's kept blocks as a bit mask; positions by a warp prefix sum of the counts
-    uint32_t kmask = 0;
-#pragma unroll
-    for (int i = 0; i < KB; ++i) kmask |= ((tid + i * NT < nb && bv[i] >= t) ? 1u : 0u) << i;
-    const int mine = __popc(kmask);
+  // a warp places its `mine` blocks (per lane) with one shared atomic; returns the lane's first slot
+  auto place = [&](int mine) -> int {
     int incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
-    nk = __shfl_sync(0xffffffffu, incl, 31);
-    int pos = incl - mine;
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    uint32_t wbase = 0;
+    if (lane == 31 && total > 0) wbase = atomicAdd(&sm.misc[3], static_cast<uint32_t>(total));
+    wbase = __shfl_sync(0xffffffffu, wbase, 31);
+    return static_cast<int>(wbase) + incl - mine;
+  };
+  if (one_round) {
+    uint32_t kmask = 0;  // this thread's kept blocks as a bit mask
+#pragma unroll
+    for (int i = 0; i < KB; ++i) kmask |= ((tid + i * NT < nb && bv[i] >= t) ? 1u : 0u) << i;
+    int pos = place(__popc(kmask));
     while (kmask) {
       const int i = __ffs(kmask) - 1;
       kmask &= kmask - 1;
-      if (pos < kSWarpKept) wk[pos] = tid + i * NT;
+      if (pos < kSKeptCap) sm.kept[pos] = tid + i * NT;
       ++pos;
     }
   } else {
@@ -484,50 +478,58 @@ __device__ void select_row(const ReduceArgs& a, int row, int tid, SelectSmem<NT>
         const int b = base + tid + i * NT;
         v[i] = b < nb ? __ldcg(bm + b) : -INFINITY;
       }
+      uint32_t kmask = 0;
 #pragma unroll
-      for (int i = 0; i < KB; ++i) {
-        const int b = base + tid + i * NT;
-        const bool keep = b < nb && v[i] >= t;
-        const unsigned m = __ballot_sync(0xffffffffu, keep);
-        if (keep) {
-          const int pos = nk + __popc(m & ((1u << lane) - 1u));
-          if (pos < kSWarpKept) wk[pos] = b;
-        }
-        nk += __popc(m);
+      for (int i = 0; i < KB; ++i) kmask |= ((base + tid + i * NT < nb && v[i] >= t) ? 1u : 0u) << i;
+      int pos = place(__popc(kmask));
+      while (kmask) {
+        const int i = __ffs(kmask) - 1;
+        kmask &= kmask - 1;
+        if (pos < kSKeptCap) sm.kept[pos] = base + tid + i * NT;
+        ++pos;
       }
     }
   }
-  __syncwarp();
-  if (nk > kSWarpKept) {
-    if (lane == 0) sm.misc[3] = 1;  // more kept blocks than the list holds: exact path below
+  named_bar_sync(kSelBar, NT);
+  const int nkept = static_cast<int>(sm.misc[3]);  // uniform
+  auto add_cand = [&](float x, int e) {
+    if (x >= t) {
+      const uint32_t pos = atomicAdd(&sm.misc[0], 1u);
+      if (pos < kSCandCap) sm.cand[pos] = make_key(x, e);
+    }
+  };
+  if (nkept > kSKeptCap) {
+    // more kept blocks than the list holds: the exact path below
   } else if (a.vec_ok) {
-    // 16-byte vectors of the kept blocks, kSGather per lane in flight; none straddles the row end.
-    // The warp's candidates are placed with one shared atomic: per-lane bit masks and a prefix sum.
-    const int n_vec = nk * VPB;
-    for (int base = 0; base < n_vec; base += kSGather * 32) {
+    // the kept blocks' 16-byte vectors spread evenly over the group, kSGather per thread in
+    // flight (one memory round trip for up to NT * kSGather vectors); none straddles the row end.
+    // A warp's candidates are placed with one shared atomic: per-lane bit masks and a prefix sum.
+    static_assert(kSGather * EPV <= 64, "candidate bit mask");
+    const int n_vec = nkept * VPB;
+    for (int base = 0; base < n_vec; base += kSGather * NT) {
       uint4 w[kSGather];
       int e0[kSGather];
 #pragma unroll
       for (int u = 0; u < kSGather; ++u) {
-        const int j = base + u * 32 + lane;
+        const int j = base + u * NT + tid;
         e0[u] = -1;
         if (j < n_vec) {
-          const int e = wk[j / VPB] * kBlock + (j % VPB) * EPV;
+          const int e = sm.kept[j / VPB] * kBlock + (j % VPB) * EPV;
           if (e < a.V) {
             e0[u] = e;
             w[u] = *reinterpret_cast<const uint4*>(rowp + e);
           }
         }
       }
-      uint32_t cmask = 0;  // bit u * EPV + e: element e of vector u reaches t
+      uint64_t cmask = 0;  // bit u * EPV + e: element e of vector u reaches t
 #pragma unroll
       for (int u = 0; u < kSGather; ++u) {
         float x[EPV];
         VT::unpack(w[u], x);
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) cmask |= ((e0[u] >= 0 && x[e] >= t) ? 1u : 0u) << (u * EPV + e);
+        for (int e = 0; e < EPV; ++e) cmask |= ((e0[u] >= 0 && x[e] >= t) ? 1ull : 0ull) << (u * EPV + e);
       }
-      const int mine = __popc(cmask);
+      const int mine = __popcll(cmask);
       int incl = mine;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -541,7 +543,7 @@ __device__ void select_row(const ReduceArgs& a, int row, int tid, SelectSmem<NT>
       uint32_t pos = wbase + static_cast<uint32_t>(incl - mine);
 #pragma unroll
       for (int u = 0; u < kSGather; ++u) {
-        uint32_t mu = (cmask >> (u * EPV)) & ((1u << EPV) - 1u);
+        uint32_t mu = static_cast<uint32_t>(cmask >> (u * EPV)) & ((1u << EPV) - 1u);
         if (!mu) continue;
         float x[EPV];
         VT::unpack(w[u], x);
@@ -557,23 +559,17 @@ __device__ void select_row(const ReduceArgs& a, int row, int tid, SelectSmem<NT>
       }
     }
   } else {
-    const int n_el = nk * kBlock;
-    for (int j = lane; j < n_el; j += 32) {
-      const int e = wk[j / kBlock] * kBlock + (j % kBlock);
-      if (e < a.V) {
-        const float x = VT::at(rowp, e);
-        if (x >= t) {
-          const uint32_t pos = atomicAdd(&sm.misc[0], 1u);
-          if (pos < kSCandCap) sm.cand[pos] = make_key(x, e);
-        }
-      }
+    const int n_el = nkept * kBlock;
+    for (int j = tid; j < n_el; j += NT) {
+      const int e = sm.kept[j / kBlock] * kBlock + (j % kBlock);
+      if (e < a.V) add_cand(VT::at(rowp, e), e);
     }
   }
   if (warp == 0) row_lse();
   named_bar_sync(kSelBar, NT);
   int cnt = static_cast<int>(sm.misc[0]);
   const float lse = sm.lse;
-  if (cnt > kSCandCap || sm.misc[3] != 0) {
+  if (cnt > kSCandCap || nkept > kSKeptCap) {
     // too many entries reach t (ties, rows of -inf): the exact k-th key over
     // them, then the k keys at or above it
     auto in_set = [&](int i, uint64_t* key) -> bool {
@@ -600,11 +596,44 @@ __device__ void select_row(const ReduceArgs& a, int row, int tid, SelectSmem<NT>
     sync();
     cnt = min(k, static_cast<int>(sm.misc[0]));
   }
-  // ---- exact order by rank (keys are unique): G threads per candidate ----
-  int G = 1;  // a power of two <= 32 with G * cnt <= NT, at least 1
-  while (G < 32 && 2 * G * cnt <= NT) G *= 2;
-  const int groups = NT / G;
-  for (int base = 0; base < cnt; base += groups) {
+  // ---- exact order (keys are unique) ----
+  if (cnt <= 64) {
+    // one warp: a bitonic sort of the <= 64 keys, two per lane (key i = lane + 32 h), descending
+    if (warp == 0) {
+      uint64_t v0 = lane < cnt ? sm.cand[lane] : 0ull, v1 = lane + 32 < cnt ? sm.cand[lane + 32] : 0ull;
+#pragma unroll
+      for (int size = 2; size <= 64; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          if (stride == 32) {  // partners in one lane (size 64: the whole sequence descends)
+            const uint64_t hi = v0 > v1 ? v0 : v1, lo = v0 > v1 ? v1 : v0;
+            v0 = hi;
+            v1 = lo;
+          } else {
+            const bool lower = (lane & stride) == 0;
+            const uint64_t y0 = __shfl_xor_sync(0xffffffffu, v0, stride);
+            const uint64_t y1 = __shfl_xor_sync(0xffffffffu, v1, stride);
+            const bool d0 = (lane & size) == 0, d1 = ((lane + 32) & size) == 0;  // descending runs
+            v0 = (d0 == lower) ? (v0 > y0 ? v0 : y0) : (v0 < y0 ? v0 : y0);
+            v1 = (d1 == lower) ? (v1 > y1 ? v1 : y1) : (v1 < y1 ? v1 : y1);
+          }
+        }
+      }
+      if (lane < cnt && lane < k) {
+        out_ids[lane] = key_id(v0);
+        out_lp[lane] = key_value(v0) - lse;
+      }
+      if (lane + 32 < cnt && lane + 32 < k) {
+        out_ids[lane + 32] = key_id(v1);
+        out_lp[lane + 32] = key_value(v1) - lse;
+      }
+    }
+  } else {
+    // G threads per candidate, each counting the larger keys among a share of the candidates
+    int G = 1;  // a power of two <= 32 with G * cnt <= NT, at least 1
+    while (G < 32 && 2 * G * cnt <= NT) G *= 2;
+    const int groups = NT / G;
+    for (int base = 0; base < cnt; base += groups) {
     const int i = base + tid / G, sub = tid % G;
     const uint64_t key = i < cnt ? sm.cand[i] : 0ull;
     int rank = 0;
@@ -614,6 +643,7 @@ __device__ void select_row(const ReduceArgs& a, int row, int tid, SelectSmem<NT>
     if (i < cnt && sub == 0 && rank < k) {
       out_ids[rank] = key_id(key);
       out_lp[rank] = key_value(key) - lse;
+    }
     }
   }
   for (int r = min(cnt, k) + tid; r < a.k_max; r += NT) {  // ranks without a candidate, and ranks >= k
@@ -635,8 +665,7 @@ struct StreamDesc {  // one per stage, written by the producer before the copy i
 };
 static_assert(sizeof(StreamDesc) <= kTDescBytes, "descriptor slot");
 
-constexpr int kTSelKB = 16;  // block maxima per consumer thread per round in the fused select
-constexpr int kTSmem = kTSmemRing + static_cast<int>(sizeof(SelectSmem<kTConsumers>));
+constexpr int kTSmem = kTSmemRing;
 
 template <typename T>
 __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kernel(const ReduceArgs a) {
@@ -654,7 +683,6 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * kTChunkBytes + S * kTDescBytes);
   uint64_t* empty = full + S;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
-  SelectSmem<kTConsumers>& sm = *reinterpret_cast<SelectSmem<kTConsumers>*>(smem + kTSmemRing);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -666,7 +694,7 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
     mbar_init_fence();
   }
   __syncthreads();
-  pdl_launch_dependents();  // a following kernel may be scheduled; it waits for this grid's results
+  pdl_launch_dependents();  // the select kernel may be scheduled; it waits for this grid's results
 
   if (warp == kTConsumerWarps) {
     // ------------------------------ producer ------------------------------
@@ -678,7 +706,7 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
     const int64_t total = static_cast<int64_t>(a.rows) * a.cpr;
     const int64_t first_dynamic = static_cast<int64_t>(S) * gridDim.x;
     const uint64_t policy = l2_evict_first_policy();  // logits are read once; the block maxima stay in L2
-    // The kernel may start while its predecessor (the counter reset) still runs:
+    // The kernel may start while its predecessor (the ticket reset) still runs:
     // wait for it before the first ticket, load or workspace write (the
     // consumers write only data that arrived after this point).
     pdl_wait();
@@ -728,110 +756,78 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
   }
 
   // ------------------------------ consumers ------------------------------
-  // The four consumer warps take every chunk together and decide together (a
-  // barrier with an OR vote) whether to stop, so that none of them waits at a
-  // named barrier the others have left.  Each chunk is counted against its row
-  // (row_done) one iteration later, by thread 0 at the start of the next
-  // iteration: by then the chunk's results are long written, so the fence is
-  // short, and the count's result is read only after the next chunk is
-  // processed, so its round trip hides behind that work.  The CTA whose count
-  // completes a row selects that row (select_row) while the other CTAs keep
-  // streaming; the end marker's iteration counts the CTA's last chunk.
   const int c = tid;  // consumer thread 0..127: bytes [128c, 128c + 128) of a chunk
   const int rot = c & 7;  // vector order rotated by lane: conflict-free 16-byte shared loads
+  // The block maxima are read back by the select kernel right after this one: they stay in
+  // L2 (evict-last) while the logits, read once, go first (evict-first).
+  const uint64_t keep_policy = l2_evict_last_policy();
   const int bi = c / TPB;
   const float L = kLog2e;
-  int prev_row = -1;       // the row of the chunk processed last iteration, not yet counted
-  unsigned prev_old = 0u;  // thread 0: the count before adding that chunk
   for (uint32_t i = 0;; ++i) {
     const int s = static_cast<int>(i % S);
-    const bool ok = __all_sync(0xffffffffu, wait_or_abort(&full[s], (i / S) & 1u, abort_flag, a.dev_status, a.wait_ns));
-    StreamDesc d;
-    d.row = -1;
-    if (ok) d = desc[s];
-    const bool stop = !ok || d.row < 0;
-    // Count the previous chunk.  Every consumer's writes of it preceded the last
-    // barrier; thread 0's fence and increment publish them to the CTA that completes
-    // the row (the pattern of a grid-wide barrier: bar.sync, fence, atomic).
-    if (tid == 0 && prev_row >= 0) {
-      __threadfence();
-      prev_old = atomicAdd(a.parts.row_done + prev_row, 1u);
-    }
-    if (!stop) {
-      const unsigned char* stg = stages + static_cast<size_t>(s) * kTChunkBytes;
-      uint4 w[8];
+    const bool ok = wait_or_abort(&full[s], (i / S) & 1u, abort_flag, a.dev_status, a.wait_ns);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    const StreamDesc d = desc[s];
+    if (d.row < 0) break;
+    const unsigned char* stg = stages + static_cast<size_t>(s) * kTChunkBytes;
+    uint4 w[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) w[j] = *reinterpret_cast<const uint4*>(stg + c * 128 + ((j + rot) & 7) * 16);
-      const bool sel_hit =
-          static_cast<unsigned>(d.sel_rel - c * EPT) < static_cast<unsigned>(EPT) && d.sel_rel < d.ne;
-      float selv = 0.0f;
-      if (sel_hit) selv = VT::at(stg, d.sel_rel);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);  // the stage is in registers: release it
-      if (sel_hit) a.parts.sel_logit[d.row] = selv;
+    for (int j = 0; j < 8; ++j) w[j] = *reinterpret_cast<const uint4*>(stg + c * 128 + ((j + rot) & 7) * 16);
+    const bool sel_hit = static_cast<unsigned>(d.sel_rel - c * EPT) < static_cast<unsigned>(EPT) && d.sel_rel < d.ne;
+    float selv = 0.0f;
+    if (sel_hit) selv = VT::at(stg, d.sel_rel);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);  // the stage is in registers: release it
+    if (sel_hit) a.parts.sel_logit[d.row] = selv;
 
-      const int ne_t = d.ne - c * EPT;  // real logits among this thread's
-      if (ne_t < EPT) {
+    const int ne_t = d.ne - c * EPT;  // real logits among this thread's
+    if (ne_t < EPT) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (((j + rot) & 7) * EPV >= ne_t)
-            w[j] = make_uint4(VT::kNegInfWord, VT::kNegInfWord, VT::kNegInfWord, VT::kNegInfWord);
-      }
-      const float vm = VT::max8(w);  // this thread's maximum
-      float bmx = vm;
-      if (TPB == 2) bmx = fmaxf(bmx, __shfl_xor_sync(0xffffffffu, bmx, 1));
-      if ((c % TPB) == 0 && bi < d.nbk) a.parts.bmax[static_cast<int64_t>(d.row) * a.nblk + d.lb + bi] = bmx;
-      float ts = 0.0f;  // sum of exp(x - vm) over this thread's logits
-      if (vm > -INFINITY) {
-        // exp(x - m) = 2^(x*log2e - m*log2e): one packed FFMA2 and one packed
-        // FADD2 per pair of logits around the two ex2
-        const float2 L2 = make_float2(L, L), nmL2 = make_float2(-vm * L, -vm * L);
-        float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
-                         make_float2(0.0f, 0.0f)};
+      for (int j = 0; j < 8; ++j)
+        if (((j + rot) & 7) * EPV >= ne_t)
+          w[j] = make_uint4(VT::kNegInfWord, VT::kNegInfWord, VT::kNegInfWord, VT::kNegInfWord);
+    }
+    const float vm = VT::max8(w);  // this thread's maximum
+    float bmx = vm;
+    if (TPB == 2) bmx = fmaxf(bmx, __shfl_xor_sync(0xffffffffu, bmx, 1));
+    if ((c % TPB) == 0 && bi < d.nbk)
+      st_keep(a.parts.bmax + static_cast<int64_t>(d.row) * a.nblk + d.lb + bi, bmx, keep_policy);
+    float ts = 0.0f;  // sum of exp(x - vm) over this thread's logits
+    if (vm > -INFINITY) {
+      // exp(x - m) = 2^(x*log2e - m*log2e): one packed FFMA2 and one packed
+      // FADD2 per pair of logits around the two ex2
+      const float2 L2 = make_float2(L, L), nmL2 = make_float2(-vm * L, -vm * L);
+      float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                       make_float2(0.0f, 0.0f)};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float2 p[EPV / 2];
-          VT::pairs(w[j], p);
+      for (int j = 0; j < 8; ++j) {
+        float2 p[EPV / 2];
+        VT::pairs(w[j], p);
 #pragma unroll
-          for (int q = 0; q < EPV / 2; ++q) {
-            const float2 y = __ffma2_rn(p[q], L2, nmL2);
-            acc[q & 3] = __fadd2_rn(acc[q & 3], make_float2(ex2_approx(y.x), ex2_approx(y.y)));
-          }
+        for (int q = 0; q < EPV / 2; ++q) {
+          const float2 y = __ffma2_rn(p[q], L2, nmL2);
+          acc[q & 3] = __fadd2_rn(acc[q & 3], make_float2(ex2_approx(y.x), ex2_approx(y.y)));
         }
-        const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
-        const float2 a = __fadd2_rn(a01, a23);
-        ts = a.x + a.y;
       }
-      // the warp's (m, s) over this chunk
-      const float M = warp_max(vm);
-      const float sc = warp_sum(vm == -INFINITY ? 0.0f : ts * ex2_approx((vm - M) * L));
-      if (lane == 0) a.parts.part_ms[d.slot + warp] = make_float2(M, M == -INFINITY ? 0.0f : sc);
+      const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+      const float2 a = __fadd2_rn(a01, a23);
+      ts = a.x + a.y;
     }
-    const bool any_stop = named_bar_or(kSelBar, kTConsumers, stop);
-    if (tid == 0) {
-      const bool last = prev_row >= 0 && prev_old == static_cast<unsigned>(a.cpr) - 1u;
-      if (last) __threadfence();  // the other CTAs' writes to the row are visible from here on
-      sm.flag = last ? prev_row : -1;
-    }
-    named_bar_sync(kSelBar, kTConsumers);
-    if (sm.flag >= 0)
-      select_row<T, kTConsumers, kTSelKB>(a, sm.flag, tid, sm, a.lse, a.sel_logprob, a.topk_ids, a.topk_logprobs);
-    if (any_stop) break;
-    prev_row = d.row;
+    // the warp's (m, s) over this chunk
+    const float M = warp_max(vm);
+    const float sc = warp_sum(vm == -INFINITY ? 0.0f : ts * ex2_approx((vm - M) * L));
+    if (lane == 0) a.parts.part_ms[d.slot + warp] = make_float2(M, M == -INFINITY ? 0.0f : sc);
   }
 }
 
-// Zeroes the chunk ticket and the per-row chunk counters before the TMA-path
-// stream kernel.  A kernel (not a memset) so that the chain previous kernel ->
-// reset -> stream can use programmatic dependent launch: it waits for its
-// predecessor, whose work may still read the workspace, and lets the stream
-// kernel be scheduled meanwhile.
-__global__ void __launch_bounds__(256) counters_reset_kernel(unsigned int* ticket, unsigned int* row_done, int rows) {
+// Zeroes the chunk ticket before the TMA-path stream kernel.  A kernel (not a
+// memset) so that the chain previous kernel -> reset -> stream can use
+// programmatic dependent launch: it waits for its predecessor, whose work may
+// still read the workspace, and lets the stream kernel be scheduled meanwhile.
+__global__ void ticket_reset_kernel(unsigned int* ticket) {
   pdl_launch_dependents();
   pdl_wait();
-  const int i0 = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i0 == 0) *ticket = 0u;
-  for (int i = i0; i < rows; i += gridDim.x * blockDim.x) row_done[i] = 0u;
+  if (threadIdx.x == 0) *ticket = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -950,7 +946,7 @@ __global__ void __launch_bounds__(kRThreads, kRCtasPerSm) logits_stream_regs_ker
   }
 }
 
-// The register path's select: one CTA per row, after the stream kernel.
+// The per-row select: one CTA per row, after the stream kernel.
 template <typename T>
 __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceArgs a, float* lse_out,
                                                                   float* sel_logprob, int32_t* topk_ids,
@@ -1068,7 +1064,7 @@ cudaError_t logits_reduce_setup() {
 size_t stream_partials_bytes(int rows, const VocabSplit& vs) {
   auto al = [](size_t n) { return (n + 255) & ~static_cast<size_t>(255); };
   return al(static_cast<size_t>(rows) * vs.slots * 8) + al(static_cast<size_t>(rows) * 4) +
-         al(static_cast<size_t>(rows) * vs.nblk * 4) + al(4) + al(static_cast<size_t>(rows) * 4);
+         al(static_cast<size_t>(rows) * vs.nblk * 4) + al(4);
 }
 
 Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs) {
@@ -1082,8 +1078,6 @@ Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs) {
   out.bmax = reinterpret_cast<float*>(p);
   p += al(static_cast<size_t>(rows) * vs.nblk * 4);
   out.ticket = reinterpret_cast<unsigned int*>(p);
-  p += al(4);
-  out.row_done = reinterpret_cast<unsigned int*>(p);
   out.part_keys = nullptr;
   out.part_samp = nullptr;
   return out;
@@ -1098,26 +1092,18 @@ static cudaError_t launch_both(ReduceArgs a, const VocabSplit& split, float* lse
     a.cpr = (a.nblk + CH - 1) / CH;
     const int64_t chunks = static_cast<int64_t>(a.rows) * a.cpr;
     const int grid = static_cast<int>(chunks < split.ctas ? chunks : split.ctas);
-    // the stream kernel selects every row itself (the CTA that completes the row's last chunk)
-    a.lse = lse;
-    a.sel_logprob = sel_logprob;
-    a.topk_ids = topk_ids;
-    a.topk_logprobs = topk_logprobs;
-    const int reset_grid = a.rows / 256 + 1 < 64 ? a.rows / 256 + 1 : 64;
     trace_begin(kTraceReset, stream);
-    e = launch_kernel(counters_reset_kernel, dim3(reset_grid), dim3(256), 0, stream, true, a.parts.ticket,
-                      a.parts.row_done, a.rows);
+    e = launch_kernel(ticket_reset_kernel, dim3(1), dim3(32), 0, stream, true, a.parts.ticket);
     trace_end(kTraceReset, stream);
     if (e != cudaSuccess) return e;
     trace_begin(kTraceReduce, stream);
     e = launch_kernel(logits_stream_tma_kernel<T>, dim3(grid), dim3(kTThreads), static_cast<size_t>(kTSmem), stream,
                       true, a);
-    trace_end(kTraceReduce, stream);
-    return e;
+  } else {
+    a.cpr = 0;
+    trace_begin(kTraceReduce, stream);
+    e = launch_kernel(logits_stream_regs_kernel<T>, dim3(split.grid), dim3(kRThreads), 0, stream, false, a);
   }
-  a.cpr = 0;
-  trace_begin(kTraceReduce, stream);
-  e = launch_kernel(logits_stream_regs_kernel<T>, dim3(split.grid), dim3(kRThreads), 0, stream, false, a);
   trace_end(kTraceReduce, stream);
   if (e != cudaSuccess) return e;
   trace_begin(kTraceLogitsSelect, stream);
@@ -1154,8 +1140,6 @@ cudaError_t launch_logits_reduce(const void* logits, lmh_dtype dtype, int64_t ro
   a.parts = parts;
   a.dev_status = dev_status;
   a.wait_ns = wait_limit_ns();
-  a.lse = a.sel_logprob = a.topk_logprobs = nullptr;
-  a.topk_ids = nullptr;
   cudaError_t e;
   switch (dtype) {
     case LMH_BF16:

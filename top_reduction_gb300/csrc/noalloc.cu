@@ -10,8 +10,8 @@
 //   * latency-critical loops where cudaMalloc / cudaFree would synchronise
 //     the device.
 // This variant runs the same kernels as lmh_logprobs_from_logits (the
-// counter reset and the logits stream with its per-row select, or the
-// plain-load stream and a select kernel) but keeps their intermediate results
+// ticket reset, the logits stream and the per-row select) but keeps their
+// intermediate results
 // in a fixed array in the library's own device memory, so the call allocates
 // nothing.  Its launches are recorded by the kernel trace like those of the
 // workspace entry point (launch_logits_reduce brackets every launch).
@@ -25,7 +25,7 @@
 //     248320 logits, 782 rows of 151936);
 //   * every call uses the same array and it keeps the previous call's
 //     contents; nothing in it needs to start at zero (each call zeroes its
-//     counters in its first kernel and writes every other slot it reads),
+//     chunk counter in its first kernel and writes every other slot it reads),
 //     but calls that overlap on the GPU (two streams, or two threads) race on
 //     it and must be serialised by the caller;
 //   * the first call on each device does a one-time set-up with that device
