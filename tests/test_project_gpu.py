@@ -171,6 +171,28 @@ def test_selected_rows_equal_full_projection_sliced(lmh, tiny):
     assert not torch.equal(sel_logits, full_logits[shifted.long()])
 
 
+@pytest.mark.parametrize("rows,T,H,V", [(5, 64, 128, 4096), (37, 300, 512, 3000), (200, 260, 256, 2000),
+                                         (129, 140, 64, 1000)])
+def test_gather_paths_agree(lmh, rows, T, H, V):
+    """The selected rows' logits are the full projection's rows, bit for bit, whether the row
+    gather copies 16-byte vectors (aligned rows) or elements (a row stride that is not a
+    multiple of 8 elements, which the head then reads from the gathered copy)."""
+    g = torch.Generator().manual_seed(rows + T)
+    hidden = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    W = (torch.randn(V, H, generator=g) / H ** 0.5).to(torch.bfloat16).cuda()
+    ri = torch.randperm(T, generator=g)[:rows].to(torch.int32).cuda()
+    _, st0, full = gpu_project(lmh, hidden.cuda(), W, k=0, materialize=True)
+    _, st1, by_vector = gpu_project(lmh, hidden.cuda(), W, row_idx=ri, k=0, materialize=True)
+    padded = torch.zeros(T, H + 3, dtype=torch.bfloat16)
+    padded[:, :H] = hidden
+    odd = padded.cuda()[:, :H]  # row stride H + 3
+    _, st2, by_element = gpu_project(lmh, odd, W, row_idx=ri, k=0, materialize=True)
+    assert st0 == st1 == st2 == 0
+    want = full[ri.long()]
+    assert torch.equal(by_vector, want)
+    assert torch.equal(by_element, want)
+
+
 def test_row_idx_out_of_range_sets_status(lmh, tiny):
     from top_reduction_gb300 import lmh as L
     b = tiny

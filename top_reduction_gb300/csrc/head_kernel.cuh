@@ -48,6 +48,10 @@ constexpr int kHeadThreads = 192;
 constexpr int kTmemCols = 512;
 constexpr uint32_t kStageBytesA = kBM * kBK * 2;  // 16 KB
 constexpr uint32_t kStageBytesB = kBN * kBK * 2;  // 32 KB
+// W slices the producer prefetches into L2 past its ring while it waits for the kernel
+// before it (the grid-dependency wait): HBM keeps streaming W during that wait instead of
+// idling once the ring is full.  Prefetching in the steady state measured slower.
+constexpr int kWaitPrefetch = 16;
 
 // KCAP: per-row candidate capacity.  KCAP <= 32 keeps each row's top-k list
 // in registers and uses the shared region to stage candidate blocks (4 warps x
@@ -107,6 +111,13 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       "[%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
+}
+
+// Bulk tensor prefetch of one box into L2 (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
@@ -483,6 +494,29 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
           np = j + 1;
           ++n_issued;
         }
+      }
+      // During the grid-dependency wait: the next kWaitPrefetch W slices into L2, by the CTAs
+      // of the first row tile only (the other row tiles read the same slices).
+      {
+        const int su = u, smt = m_tile, sn = n, sne = n_end, skb = kb;
+        const bool sv = valid;
+        for (int j = 0; j < kWaitPrefetch && valid; ++j) {
+          if (m_tile == 0) {
+            if constexpr (kHV) {
+#pragma unroll
+              for (int q = 0; q < kBN / 64; ++q) tma_prefetch_l2_2d(&tmap_b, n * kBN + 64 * q, kb * kBK);
+            } else {
+              tma_prefetch_l2_2d(&tmap_b, kb * kBK, n * kBN);
+            }
+          }
+          advance();
+        }
+        u = su;
+        m_tile = smt;
+        n = sn;
+        n_end = sne;
+        kb = skb;
+        valid = sv;
       }
       // the stage's A slice: one box, or with the column split one box per row copy
       auto load_a = [&](int s, int kb_, int m_tile_) {

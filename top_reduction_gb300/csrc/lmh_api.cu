@@ -279,13 +279,15 @@ static lmh_status project_impl(const void* hidden, int64_t hidden_row_stride, in
     A = ws;
     a_stride = H;
   }
-  // One vocabulary split: the head kernel finishes every row itself.
+  // One vocabulary split: the head kernel finishes every row itself.  The head is always
+  // launched with programmatic dependent launch: it streams its first W slices while the
+  // kernel before it (the row gather, or the previous call's merge) ends.
   const RowOutputs outs{lse, sel_logprob, topk_ids, topk_logprobs};
   const bool one_split = plan.splits == 1;
   if (e == cudaSuccess) {
     Traced tr(kTraceHead, stream);
     e = launch_head(A, a_stride, rows, H, W, V, plan, sel_ids, row_k, k_max, parts, z_out, dev_status, stream,
-                    /*pdl=*/gather, one_split ? &outs : nullptr, logit_scale, samp, w_layout == LMH_W_HV);
+                    /*pdl=*/true, one_split ? &outs : nullptr, logit_scale, samp, w_layout == LMH_W_HV);
   }
   if (e == cudaSuccess && !one_split) {
     Traced tr(kTraceMerge, stream);
@@ -445,7 +447,7 @@ lmh_status lmh_project_partials(const void* hidden, int64_t hidden_row_stride, i
   if (e == cudaSuccess) {
     Traced tr(kTraceHead, stream);
     e = launch_head(A, a_stride, rows, H, W_share, v_count, plan, sel_ids, row_k, k_max, parts, nullptr, dev_status,
-                    stream, /*pdl=*/gather, nullptr, 1.0f, nullptr, false, v_begin);
+                    stream, /*pdl=*/true, nullptr, 1.0f, nullptr, false, v_begin);
   }
   if (e == cudaSuccess) {
     const RecordOut rec{static_cast<unsigned char*>(records), v_begin, v_count};
