@@ -349,16 +349,17 @@ def e2e_leg(lmh, b, device, steps):
     Every step copies its inputs host->device (hidden rows, cu_seqlens,
     selected ids; the head weight stays resident like model weights), runs
     the path, copies the compact result device->host and reads it on the
-    host.  As a serving loop would, each step (the copy in, the API calls and
-    the copy out) is captured once in a CUDA graph and replayed every step;
-    if capture fails the calls run eagerly.  Two buffer sets alternate and
-    step i+1 is issued before the host waits for step i's result.
+    host.  As a serving loop would, each step's calls and its copy out are
+    captured once in a CUDA graph and replayed every step (if capture fails
+    the calls run eagerly), two buffer sets alternate, and step i+1 is issued
+    before the host waits for step i's result.
 
-    The value is the loop with both buffer sets on one stream, as an
-    autoregressive loop over one batch runs: each step's GPU work follows the
-    previous step's.  The "pipelined" record repeats it with one stream per
-    buffer set (two independent batches in flight); there two heads run at
-    once and share W's reads in L2, so it is context, not the metric.
+    The value is the loop as a serving engine runs it: the copies in go on a
+    copy stream, so step i+1's inputs cross while step i computes, and every
+    step's GPU work runs on one compute stream, after the previous step's.
+    Two more loops are reported as context: "serial" (copy in and compute on
+    one stream, nothing overlaps) and "pipelined" (one stream per buffer set:
+    two independent batches in flight, whose heads share W's reads in L2).
     """
     import torch
     chunk = b["name"] == "logits_chunk"
@@ -379,6 +380,7 @@ def e2e_leg(lmh, b, device, steps):
         ws_bytes = lmh.workspace_bytes(rows, 0, b["V"], k, lmh.PATH_FROM_LOGITS)
     else:
         ws_bytes = lmh.workspace_bytes(rows, int(b["H"]), int(b["V"]), k, lmh.PATH_PROJECT)
+    copy_stream, compute_stream = torch.cuda.Stream(), torch.cuda.Stream()
 
     def buffers():
         d_in_buf, d_in = packed(h_in, device)
@@ -387,15 +389,18 @@ def e2e_leg(lmh, b, device, steps):
         h_out_buf, h_out = packed(shapes, "cpu", pinned=True)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
         return {"d_in_buf": d_in_buf, "d_in": d_in, "d_out_buf": d_out_buf, "out": out, "h_out_buf": h_out_buf,
-                "h_out": h_out, "ws": ws, "ev": torch.cuda.Event(), "stream": torch.cuda.Stream()}
+                "h_out": h_out, "ws": ws, "ev": torch.cuda.Event(), "in_ev": torch.cuda.Event(),
+                "stream": torch.cuda.Stream()}
 
     bufs = [buffers(), buffers()]
     h2d = sum(v.numel() * v.element_size() for v in h_in.values())
     d2h = sum(v.numel() * v.element_size() for v in bufs[0]["h_out"].values())
 
-    def step_ops(bf):
-        d_in = bf["d_in"]
+    def copy_in(bf):
         bf["d_in_buf"].copy_(h_in_buf, non_blocking=True)  # one copy in
+
+    def compute_ops(bf):
+        d_in = bf["d_in"]
         if chunk:
             o = lmh.logprobs_from_logits(d_in["logits"], sel=d_in["sel"], k_max=k, workspace=bf["ws"],
                                          out=bf["out"])
@@ -409,13 +414,28 @@ def e2e_leg(lmh, b, device, steps):
         assert all(o[key].data_ptr() == bf["out"][key].data_ptr() for key in bf["out"])
         bf["h_out_buf"].copy_(bf["d_out_buf"], non_blocking=True)  # one copy out
 
-    def issue(bf):
-        with torch.cuda.stream(bf["stream"]):
-            if "graph" in bf:
-                bf["graph"].replay()
-            else:
-                step_ops(bf)
-            bf["ev"].record()
+    def run_compute(bf):
+        if "graph" in bf:
+            bf["graph"].replay()
+        else:
+            compute_ops(bf)
+
+    def issue(bf, mode):
+        if mode == "overlap":  # copy in on the copy stream, compute on the compute stream
+            copy_stream.wait_event(bf["ev"])  # the buffer set's previous step has finished with it
+            with torch.cuda.stream(copy_stream):
+                copy_in(bf)
+                bf["in_ev"].record()
+            compute_stream.wait_event(bf["in_ev"])
+            with torch.cuda.stream(compute_stream):
+                run_compute(bf)
+                bf["ev"].record()
+        else:
+            st = compute_stream if mode == "serial" else bf["stream"]
+            with torch.cuda.stream(st):
+                copy_in(bf)
+                run_compute(bf)
+                bf["ev"].record()
 
     def read(bf):  # the host waits for, and touches, the step's result
         bf["ev"].synchronize()
@@ -423,44 +443,48 @@ def e2e_leg(lmh, b, device, steps):
 
     torch.cuda.synchronize()  # the weights and inputs above were placed on the default stream
     for s in range(5):
-        issue(bufs[s % 2])
+        issue(bufs[s % 2], "serial")
         read(bufs[s % 2])
-    mode = "CUDA graph per buffer set, one stream per buffer set"
+    graph_note = "each step's calls and copy out replayed from a CUDA graph"
     try:
         for bf in bufs:
+            copy_in(bf)
+            torch.cuda.synchronize()
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                step_ops(bf)
+                compute_ops(bf)
             bf["graph"] = g
         for s in range(4):
-            issue(bufs[s % 2])
+            issue(bufs[s % 2], "serial")
             read(bufs[s % 2])
     except Exception as e:  # capture is an optimisation of the loop, not a requirement
         for bf in bufs:
             bf.pop("graph", None)
-        mode = "eager, one stream per buffer set (graph capture failed: %s)" % str(e).splitlines()[0][:80]
+        graph_note = "eager calls (graph capture failed: %s)" % str(e).splitlines()[0][:80]
         torch.cuda.synchronize()
-    def timed(n):
+
+    def timed(n, mode):
+        torch.cuda.synchronize()
         t0 = time.perf_counter()
         for s in range(n):
-            issue(bufs[s % 2])
+            issue(bufs[s % 2], mode)
             if s > 0:
                 read(bufs[(s - 1) % 2])
         read(bufs[(n - 1) % 2])
         return time.perf_counter() - t0
 
-    dt_pipe = timed(steps)
-    # the metric: both buffer sets on one stream, each step's GPU work after the previous step's
-    two_streams = bufs[1]["stream"]
-    bufs[1]["stream"] = bufs[0]["stream"]
-    dt = timed(steps)
-    bufs[1]["stream"] = two_streams
+    dt = timed(steps, "overlap")
+    dt_serial = timed(steps, "serial")
+    dt_pipe = timed(steps, "pipelined")
     return {"value": rows * steps / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": 1e3 * dt / steps,
-            "mode": "one stream, steps back to back; " + mode.replace(", one stream per buffer set", ""),
+            "mode": "copies in on a copy stream overlap the previous step's compute; every step's GPU work on "
+                    "one compute stream; " + graph_note,
+            "serial": {"value": rows * steps / dt_serial, "ms_per_step": 1e3 * dt_serial / steps,
+                       "note": "copy in, compute and copy out on one stream: nothing overlaps"},
             "pipelined": {"value": rows * steps / dt_pipe, "ms_per_step": 1e3 * dt_pipe / steps,
-                          "note": "two buffer sets on two streams: two independent batches in flight, whose "
-                                  "heads share W's reads in L2 (context only)"}}
+                          "note": "one stream per buffer set: two independent batches in flight, whose heads "
+                                  "share W's reads in L2 (context only)"}}
 
 
 def load_peaks():

@@ -339,34 +339,12 @@ __device__ __forceinline__ uint64_t max_of(const uint64_t (&kv)[kWarpPerLane]) {
   return m;
 }
 
-__global__ void __launch_bounds__(kWarpRowsPerCtaMax * 32) merge_partials_warp_kernel(const MergeArgs a) {
-  pdl_wait();  // the partials come from the kernel launched just before
-  pdl_launch_dependents();  // a following kernel may be scheduled; it waits for this grid before using its results
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int row = blockIdx.x * (blockDim.x >> 5) + w;
-  if (row >= a.rows) return;
+// One warp's row: lse = M + log(sum_j s_j exp(m_j - M)) over the row's slots, the
+// selected token's logprob, the sampled token (the best slot partial), or in record
+// mode the row's record head.  Every lane gets lse.
+__device__ __forceinline__ float warp_row_head(const MergeArgs& a, int row, int lane) {
   const int nslots = a.splits;
   const float2* ms = a.parts.part_ms + static_cast<int64_t>(row) * a.splits;
-
-  // ---- every independent load first: K, the row's keys, the slots' (m, s) ----
-  int k = a.k_max;
-  if (a.row_k) k = min(max(a.row_k[row], 0), a.k_max);
-  const unsigned long long* keys = a.parts.part_keys + static_cast<int64_t>(row) * a.splits * a.k_max;
-  // item i = (slot i / k, rank i % k) of the slots' sorted lists; only the first k of a
-  // list can reach the row's top k
-  const int n_items = nslots * k;
-  uint64_t kv[kWarpPerLane];
-#pragma unroll
-  for (int t = 0; t < kWarpPerLane; ++t) {
-    const int i = lane + 32 * t;
-    kv[t] = 0;
-    if (i < n_items) {
-      const int j = i / k;
-      kv[t] = keys[static_cast<int64_t>(j) * a.k_max + (i - j * k)];
-    }
-  }
-
-  // ---- lse ----
   float tm = -INFINITY, ts = 0.0f;
   for (int j = lane; j < nslots; j += 32) {
     const float2 p = ms[j];
@@ -379,8 +357,7 @@ __global__ void __launch_bounds__(kWarpRowsPerCtaMax * 32) merge_partials_warp_k
   const float M = warp_max(tm);
   const float S = warp_sum((tm == -INFINITY) ? 0.0f : ts * expf(tm - M));
   const float lse = (M == -INFINITY) ? -INFINITY : M + logf(S);
-  const bool rec_mode = a.rec.base != nullptr;
-  if (lane == 0 && rec_mode) {
+  if (lane == 0 && a.rec.base != nullptr) {
     write_record_head(a, row, M, S);
   } else if (lane == 0) {
     a.lse[row] = lse;
@@ -404,26 +381,28 @@ __global__ void __launch_bounds__(kWarpRowsPerCtaMax * 32) merge_partials_warp_k
     b = samp_warp_best(b);
     if (lane == 0) samp_write(a, row, b, lse);
   }
-  if (a.k_max == 0) return;
-  int32_t* out_ids = rec_mode ? nullptr : a.topk_ids + static_cast<int64_t>(row) * a.k_max;
-  float* out_lp = rec_mode ? nullptr : a.topk_logprobs + static_cast<int64_t>(row) * a.k_max;
-  unsigned long long* out_keys = rec_mode ? record_keys(row_record(a, row)) : nullptr;
+  return lse;
+}
 
-  // ---- tournament: rank r is the largest key left after ranks 0..r-1 ----
-  uint64_t best = max_of(kv);
-  int32_t my_id = -1;  // lane r % 32 keeps rank r's result for a coalesced store
+// Writes a warp's ranks: rank r's key comes out of round r (the same key in every
+// lane); lane r % 32 keeps it and the lanes store 32 ranks at a time, coalesced.
+// Ranks >= k get (-1, -inf), or key 0 in record mode.
+struct WarpRankWriter {
+  int32_t* ids;
+  float* lps;
+  unsigned long long* keys;  // record mode
+  float lse;
+  int32_t my_id = -1;
   float my_lp = -INFINITY;
   uint64_t my_key = 0;
-  for (int r = 0; r < k; ++r) {
-    const uint32_t hi = __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(best >> 32));
-    const uint32_t lo =
-        __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(best >> 32) == hi ? static_cast<uint32_t>(best) : 0u);
-    const uint64_t key = (static_cast<uint64_t>(hi) << 32) | lo;
-    if (key != 0ull && best == key) {  // the one holder drops it
-#pragma unroll
-      for (int t = 0; t < kWarpPerLane; ++t) kv[t] = kv[t] == key ? 0ull : kv[t];
-      best = max_of(kv);
-    }
+
+  __device__ __forceinline__ WarpRankWriter(const MergeArgs& a, int row, float lse_) : lse(lse_) {
+    const bool rec = a.rec.base != nullptr;
+    ids = rec ? nullptr : a.topk_ids + static_cast<int64_t>(row) * a.k_max;
+    lps = rec ? nullptr : a.topk_logprobs + static_cast<int64_t>(row) * a.k_max;
+    keys = rec ? record_keys(row_record(a, row)) : nullptr;
+  }
+  __device__ __forceinline__ void put(int r, int k, int lane, uint64_t key) {
     if (lane == (r & 31)) {  // key 0: fewer than k candidates
       my_key = key;
       my_id = key ? key_id(key) : -1;
@@ -432,23 +411,76 @@ __global__ void __launch_bounds__(kWarpRowsPerCtaMax * 32) merge_partials_warp_k
     if ((r & 31) == 31 || r == k - 1) {
       const int r0 = r & ~31;
       if (lane <= (r & 31)) {
-        if (rec_mode) {
-          out_keys[r0 + lane] = my_key;
+        if (keys) {
+          keys[r0 + lane] = my_key;
         } else {
-          out_ids[r0 + lane] = my_id;
-          out_lp[r0 + lane] = my_lp;
+          ids[r0 + lane] = my_id;
+          lps[r0 + lane] = my_lp;
         }
       }
     }
   }
-  for (int r = k + lane; r < a.k_max; r += 32) {  // ranks >= k
-    if (rec_mode) {
-      out_keys[r] = 0ull;
-    } else {
-      out_ids[r] = -1;
-      out_lp[r] = -INFINITY;
+  __device__ __forceinline__ void pad(int k, int k_max, int lane) {
+    for (int r = k + lane; r < k_max; r += 32) {
+      if (keys) {
+        keys[r] = 0ull;
+      } else {
+        ids[r] = -1;
+        lps[r] = -INFINITY;
+      }
     }
   }
+};
+
+// The warp's largest key among every lane's `cand` (keys are unique: one lane holds it).
+__device__ __forceinline__ uint64_t warp_max_key(uint64_t cand) {
+  const uint32_t hi = __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(cand >> 32));
+  const uint32_t lo =
+      __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(cand >> 32) == hi ? static_cast<uint32_t>(cand) : 0u);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+__global__ void __launch_bounds__(kWarpRowsPerCtaMax * 32) merge_partials_warp_kernel(const MergeArgs a) {
+  pdl_wait();  // the partials come from the kernel launched just before
+  pdl_launch_dependents();  // a following kernel may be scheduled; it waits for this grid before using its results
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int row = blockIdx.x * (blockDim.x >> 5) + w;
+  if (row >= a.rows) return;
+  const int nslots = a.splits;
+
+  // ---- every independent load first: K and the row's keys ----
+  int k = a.k_max;
+  if (a.row_k) k = min(max(a.row_k[row], 0), a.k_max);
+  const unsigned long long* keys = a.parts.part_keys + static_cast<int64_t>(row) * a.splits * a.k_max;
+  // item i = (slot i / k, rank i % k) of the slots' sorted lists; only the first k of a
+  // list can reach the row's top k
+  const int n_items = nslots * k;
+  uint64_t kv[kWarpPerLane];
+#pragma unroll
+  for (int t = 0; t < kWarpPerLane; ++t) {
+    const int i = lane + 32 * t;
+    kv[t] = 0;
+    if (i < n_items) {
+      const int j = i / k;
+      kv[t] = keys[static_cast<int64_t>(j) * a.k_max + (i - j * k)];
+    }
+  }
+  const float lse = warp_row_head(a, row, lane);
+  if (a.k_max == 0) return;
+
+  // ---- tournament: rank r is the largest key left after ranks 0..r-1 ----
+  WarpRankWriter out(a, row, lse);
+  uint64_t best = max_of(kv);
+  for (int r = 0; r < k; ++r) {
+    const uint64_t key = warp_max_key(best);
+    if (key != 0ull && best == key) {  // the one holder drops it
+#pragma unroll
+      for (int t = 0; t < kWarpPerLane; ++t) kv[t] = kv[t] == key ? 0ull : kv[t];
+      best = max_of(kv);
+    }
+    out.put(r, k, lane, key);
+  }
+  out.pad(k, a.k_max, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -498,14 +530,15 @@ cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts,
   a.dev_status = dev_status;
   a.samp = samp ? *samp : SampleArgs{};
   a.rec = rec ? *rec : RecordOut{nullptr, 0, 0};
+  const int sms = num_sms > 0 ? num_sms : 1;
   if (static_cast<int64_t>(splits) * k_max <= kWarpItems && k_max <= kWarpMaxK) {
     // rows spread over the SMs first: one warp per CTA while there are SMs to spare
-    const int sms = num_sms > 0 ? num_sms : 1;
     int rpc = 1;
     while (rpc < kWarpRowsPerCtaMax && static_cast<int64_t>(rows) > static_cast<int64_t>(2 * rpc) * sms) rpc *= 2;
     return launch_kernel(merge_partials_warp_kernel, dim3((rows + rpc - 1) / rpc), dim3(rpc * 32), 0, stream, pdl,
                          a);
   }
+
   return launch_kernel(merge_partials_kernel, dim3(rows), dim3(kMergeThreads), 0, stream, pdl, a);
 }
 
