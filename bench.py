@@ -657,13 +657,13 @@ def cpu_baseline(b, budget_s=12.0, single_s=4.0, gpu_ids=None):
 
 def roofline(b, per_kernel, ms_per_step, peaks, peak_src):
     """The dominant kernel's roofline record: algorithmic amount over its traced launch time
-    (for the logits chunk the whole call, ticket reset, stream and select kernels, over the
-    step's event time)."""
+    (for the logits chunk the whole call, stream and select kernels, over the step's event
+    time)."""
     bound, amount, unit = algorithmic(b)
     kernel = dominant_kernel(b)
     if b["name"] == "logits_chunk" and b["k"] >= 0:
         us = 1e3 * ms_per_step
-        kernel_label = "logits_reduce whole call (ticket_reset + logits_stream_tma + logits_select)"
+        kernel_label = "logits_reduce whole call (logits_stream_tma + logits_select)"
     else:
         us = per_kernel.get(kernel, {}).get("avg_us")
         kernel_label = kernel

@@ -451,7 +451,6 @@ int32_t lmh_version(void);
  * and total milliseconds of the named kernel ("select_rows", "gather_rows",
  * "head_logprobs", "merge_partials", "logits_reduce" (the streaming pass of
  * lmh_logprobs_from_logits), "logits_select" (its per-row selection),
- * "ticket_reset" (the chunk-counter reset before the streaming pass),
  * "full_logprobs" (the pass that writes the k_max = LMH_K_FULL output)) since
  * the last reset.
  * lmh_trace_reset clears the totals.

@@ -207,3 +207,21 @@ def test_full_vocabulary_ragged(lmh, dtype, V):
     check_from_logits({"lse": o["lse"], "sel_logprob": o["sel_logprob"]},
                       {"lse": orc["lse"], "sel_logprob": orc["sel_logprob"]}, 0, what="full ragged")
     assert np.max(np.abs(o["topk_logprobs"].cpu().numpy() - _oracle_full(x, orc["lse"]))) <= 1e-5
+
+
+def test_reused_workspace_schedules(lmh):
+    """One workspace over several calls: its first call finds no valid chunk-counter base and
+    hands out the chunks in a fixed order; the later calls draw them from the counter. Every
+    call matches the oracle, on different inputs and row counts, and a workspace whose counter
+    words hold leftovers of another use is still read correctly."""
+    from top_reduction_gb300 import lmh as L
+    V = 50000
+    need = max(L.workspace_bytes(r, 0, V, 20, L.PATH_FROM_LOGITS) for r in (64, 48))
+    ws = torch.full((need,), 0x5A, dtype=torch.uint8, device="cuda")  # leftovers, not zeros
+    for i, rows in enumerate((64, 48, 64, 64)):
+        c = workloads.logits_chunk("normal", seed=40 + i, rows=rows, V=V)
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        o = lmh.logprobs_from_logits(c["logits"].cuda(), sel=c["sel"], k_max=20, workspace=ws, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        check_from_logits(o, oracle_ref(c["logits"], c["sel"], 20), 20, what="call %d" % i)

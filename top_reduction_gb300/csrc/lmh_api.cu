@@ -73,9 +73,9 @@ Partials carve_partials(void* base, int rows, int splits, int k_max) {
 // ---------------------------------------------------------------------------
 // kernel trace
 // ---------------------------------------------------------------------------
-static const char* const kTraceNames[kTraceCount] = {"select_rows",   "gather_rows",    "head_logprobs",
-                                                     "logits_reduce", "merge_partials", "logits_select",
-                                                     "ticket_reset",  "full_logprobs"};
+static const char* const kTraceNames[kTraceCount] = {"select_rows",    "gather_rows",   "head_logprobs",
+                                                     "logits_reduce",  "merge_partials", "logits_select",
+                                                     "full_logprobs"};
 
 struct TraceRecord {
   int kernel;

@@ -28,6 +28,18 @@ struct VocabSplit {
   int slots;     // (m, s) slots per row in the workspace (enough for either stream kernel)
 };
 
+// The chunk counter of the standalone reduction's dynamic schedule.  It is never
+// reset: after every call the select kernel records its value as the next call's
+// base, with the bitwise complement as a check.  A stream kernel that finds the
+// pair consistent draws chunks base + 0, 1, ...; one that does not (a workspace
+// never used by this path, or reused for something else) hands out its chunks in
+// a fixed order instead (the same results, a little slower).
+struct TicketState {
+  unsigned long long ticket;
+  unsigned long long base;
+  unsigned long long check;  // ~base when base is valid
+};
+
 // Per-(row, split) partial results, laid out in the caller's workspace:
 //   part_ms   float2 [rows * splits]            (chunk max m, sum exp(x - m))
 //   part_keys uint64 [rows * splits * k_max]    sorted top-k keys of the chunk
@@ -36,7 +48,7 @@ struct Partials {
   float2* part_ms;
   unsigned long long* part_keys;
   float* sel_logit;
-  unsigned int* ticket;  // standalone reduction: chunk counter of the dynamic schedule (else unused)
+  struct TicketState* ticket;  // standalone reduction: the dynamic chunk schedule's counter (else unused)
   float4* part_samp;     // head path: per-(row, split) sampling partial (best score, id bits, z, -)
   float* bmax;  // standalone reduction: block maxima [rows * nblk] (else unused)
 };
@@ -189,7 +201,6 @@ enum TraceKernel {
   kTraceReduce,
   kTraceMerge,
   kTraceLogitsSelect,
-  kTraceReset,
   kTraceFull,
   kTraceCount
 };

@@ -13,9 +13,9 @@
 //     up the selected token's logit.
 //       - logits_stream_tma_kernel (rows and the row length 16-byte
 //         aligned; four CTAs per SM): the logits are cut into 16 KB chunks
-//         of one row, handed out dynamically (a ticket counter, zeroed by a
-//         one-thread kernel before it), so CTAs that get more bandwidth take
-//         more chunks.  One producer lane streams its chunks into a ring of
+//         of one row, handed out dynamically (a ticket counter whose base the
+//         previous call's select kernel recorded), so CTAs that get more
+//         bandwidth take more chunks.  One producer lane streams its chunks into a ring of
 //         shared-memory stages with bulk copies (cp.async.bulk, completion on
 //         mbarriers); four consumer warps read them, each thread owning 128
 //         contiguous bytes (one bf16/f16 block, half an f32 block), so a
@@ -701,15 +701,21 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
     // Chunks (CH blocks of one row; chunk c is row c / cpr, part c % cpr) are
     // handed out dynamically, so CTAs that stream faster take more of them:
     // the first S of a CTA are fixed (blockIdx.x + j * gridDim.x), the rest
-    // come from the ticket counter, drawn one chunk ahead.
+    // come from the ticket counter (draws base + 0, 1, ...), drawn one chunk
+    // ahead.  Without a valid base (TicketState) every chunk is fixed.
     if (lane != 0) return;
     const int64_t total = static_cast<int64_t>(a.rows) * a.cpr;
     const int64_t first_dynamic = static_cast<int64_t>(S) * gridDim.x;
     const uint64_t policy = l2_evict_first_policy();  // logits are read once; the block maxima stay in L2
-    // The kernel may start while its predecessor (the ticket reset) still runs:
-    // wait for it before the first ticket, load or workspace write (the
+    // The kernel may start while its predecessor (the previous call's select kernel,
+    // which still reads the workspace and records the ticket's base) runs: wait for
+    // it before reading the base, the first ticket, load or workspace write (the
     // consumers write only data that arrived after this point).
     pdl_wait();
+    // Read through L2 (another kernel wrote them; an L1 line of an earlier call could be stale).
+    TicketState* tk = a.parts.ticket;
+    const unsigned long long base = __ldcg(&tk->base);
+    const bool dynamic = __ldcg(&tk->check) == ~base;  // the same in every CTA: nothing writes these now
     uint32_t issued = 0;
     int64_t next = blockIdx.x;
     int sel_row = -1, sel_id = -1;
@@ -726,8 +732,9 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
         ++issued;
         break;
       }
-      next = issued + 1 < static_cast<uint32_t>(S) ? blockIdx.x + static_cast<int64_t>(issued + 1) * gridDim.x
-                                                   : first_dynamic + atomicAdd(a.parts.ticket, 1u);
+      next = (issued + 1 < static_cast<uint32_t>(S) || !dynamic)
+                 ? blockIdx.x + static_cast<int64_t>(issued + 1) * gridDim.x
+                 : first_dynamic + static_cast<int64_t>(atomicAdd(&tk->ticket, 1ull) - base);
       const int row = static_cast<int>(c / a.cpr);
       const int ci = static_cast<int>(c - static_cast<int64_t>(row) * a.cpr);
       const int lb = ci * CH;
@@ -818,16 +825,6 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
     const float sc = warp_sum(vm == -INFINITY ? 0.0f : ts * ex2_approx((vm - M) * L));
     if (lane == 0) a.parts.part_ms[d.slot + warp] = make_float2(M, M == -INFINITY ? 0.0f : sc);
   }
-}
-
-// Zeroes the chunk ticket before the TMA-path stream kernel.  A kernel (not a
-// memset) so that the chain previous kernel -> reset -> stream can use
-// programmatic dependent launch: it waits for its predecessor, whose work may
-// still read the workspace, and lets the stream kernel be scheduled meanwhile.
-__global__ void ticket_reset_kernel(unsigned int* ticket) {
-  pdl_launch_dependents();
-  pdl_wait();
-  if (threadIdx.x == 0) *ticket = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -954,6 +951,12 @@ __global__ void __launch_bounds__(kSThreads) logits_select_kernel(const ReduceAr
   __shared__ SelectSmem<kSThreads> sm;
   pdl_wait();  // the block maxima and (m, s) come from the stream kernel just before
   pdl_launch_dependents();  // a following kernel may be scheduled; it waits for this grid before using its results
+  if (blockIdx.x == 0 && threadIdx.x == 0) {  // the stream kernel is done with the ticket: the next call's base
+    TicketState* tk = a.parts.ticket;
+    const unsigned long long t = __ldcg(&tk->ticket);  // through L2: the stream kernel's atomics wrote it
+    tk->base = t;
+    tk->check = ~t;
+  }
   select_row<T, kSThreads, 16>(a, blockIdx.x, threadIdx.x, sm, lse_out, sel_logprob, topk_ids, topk_logprobs);
 }
 
@@ -1064,7 +1067,7 @@ cudaError_t logits_reduce_setup() {
 size_t stream_partials_bytes(int rows, const VocabSplit& vs) {
   auto al = [](size_t n) { return (n + 255) & ~static_cast<size_t>(255); };
   return al(static_cast<size_t>(rows) * vs.slots * 8) + al(static_cast<size_t>(rows) * 4) +
-         al(static_cast<size_t>(rows) * vs.nblk * 4) + al(4);
+         al(static_cast<size_t>(rows) * vs.nblk * 4) + al(sizeof(TicketState));
 }
 
 Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs) {
@@ -1077,7 +1080,7 @@ Partials carve_stream_partials(void* base, int rows, const VocabSplit& vs) {
   p += al(static_cast<size_t>(rows) * 4);
   out.bmax = reinterpret_cast<float*>(p);
   p += al(static_cast<size_t>(rows) * vs.nblk * 4);
-  out.ticket = reinterpret_cast<unsigned int*>(p);
+  out.ticket = reinterpret_cast<TicketState*>(p);
   out.part_keys = nullptr;
   out.part_samp = nullptr;
   return out;
@@ -1092,10 +1095,6 @@ static cudaError_t launch_both(ReduceArgs a, const VocabSplit& split, float* lse
     a.cpr = (a.nblk + CH - 1) / CH;
     const int64_t chunks = static_cast<int64_t>(a.rows) * a.cpr;
     const int grid = static_cast<int>(chunks < split.ctas ? chunks : split.ctas);
-    trace_begin(kTraceReset, stream);
-    e = launch_kernel(ticket_reset_kernel, dim3(1), dim3(32), 0, stream, true, a.parts.ticket);
-    trace_end(kTraceReset, stream);
-    if (e != cudaSuccess) return e;
     trace_begin(kTraceReduce, stream);
     e = launch_kernel(logits_stream_tma_kernel<T>, dim3(grid), dim3(kTThreads), static_cast<size_t>(kTSmem), stream,
                       true, a);

@@ -10,8 +10,7 @@
 //   * latency-critical loops where cudaMalloc / cudaFree would synchronise
 //     the device.
 // This variant runs the same kernels as lmh_logprobs_from_logits (the
-// ticket reset, the logits stream and the per-row select) but keeps their
-// intermediate results
+// logits stream and the per-row select) but keeps their intermediate results
 // in a fixed array in the library's own device memory, so the call allocates
 // nothing.  Its launches are recorded by the kernel trace like those of the
 // workspace entry point (launch_logits_reduce brackets every launch).
@@ -24,8 +23,8 @@
 //     rows * (4 * ceil(V / 64) + 8 * slots + 8) bytes: up to 479 rows of
 //     248320 logits, 782 rows of 151936);
 //   * every call uses the same array and it keeps the previous call's
-//     contents; nothing in it needs to start at zero (each call zeroes its
-//     chunk counter in its first kernel and writes every other slot it reads),
+//     contents; nothing in it needs to start at zero (the chunk counter's base
+//     is checked before use, and every other slot is written before it is read),
 //     but calls that overlap on the GPU (two streams, or two threads) race on
 //     it and must be serialised by the caller;
 //   * the first call on each device does a one-time set-up with that device

@@ -312,7 +312,7 @@ def logprobs_from_logits(logits, sel=None, row_k=None, k_max=0, workspace=None, 
 # ---------------------------------------------------------------------------
 
 TRACE_KERNELS = ("select_rows", "gather_rows", "head_logprobs", "logits_reduce", "merge_partials",
-                 "logits_select", "ticket_reset", "full_logprobs")
+                 "logits_select", "full_logprobs")
 
 
 def trace_enable(on=True):
