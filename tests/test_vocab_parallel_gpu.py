@@ -94,3 +94,33 @@ def test_record_layout(lmh):
             assert abs(head[i, 2] - z[i, int(sel[i]) - b]) <= TOL_FUSED
         ids = (~keys[i].astype(np.uint64) & np.uint64(0xFFFFFFFF)).astype(np.int64)
         assert np.array_equal(ids, np.argsort(-z[i], kind="stable")[:k] + b)
+
+
+def test_nccl_exchange_one_rank(lmh):
+    """The exchange through NCCL on this GPU: a one-rank group, so the all-gather is the
+    identity, but the records go through the real path (project_partials -> NCCL
+    all_gather_into_tensor into device memory -> merge_records) and must equal the
+    unsharded call."""
+    import os
+    import socket
+    import torch.distributed as dist
+    if dist.is_initialized():
+        pytest.skip("a process group is already initialised")
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    os.environ.setdefault("NCCL_NVLS_ENABLE", "0")
+    dist.init_process_group("nccl", init_method="tcp://127.0.0.1:%d" % port, rank=0, world_size=1,
+                            device_id=torch.device("cuda", torch.cuda.current_device()))
+    try:
+        hidden, W, ri, sel = _case(24, 40, 256, 6000, seed=9)
+        hd, Wd, rid = hidden.cuda(), W.cuda(), ri.cuda()
+        b, n = lmh.vocab_share(6000, 0, 1)
+        o = lmh.vocab_parallel_logprobs(hd, Wd[b:b + n], b, 6000, row_idx=rid, sel=sel, k_max=8)
+        ref = lmh.project_logprobs(hd, Wd, row_idx=rid, sel=sel, k_max=8)
+        torch.cuda.synchronize()
+        assert torch.equal(o["topk_ids"], ref["topk_ids"])
+        for key in ("lse", "sel_logprob", "topk_logprobs"):
+            assert_close(o[key].cpu().numpy(), ref[key].cpu().numpy(), 1e-5, "nccl exchange " + key)
+    finally:
+        dist.destroy_process_group()
