@@ -6,8 +6,9 @@
 // - lse, evaluated only at the survivors and at the scored token; exact ties
 // by ascending id.
 //
-// One CTA per row (merge_partials_kernel), or one warp per row when a row's
-// slots hold few keys (merge_partials_warp_kernel).
+// One CTA per row (merge_partials_kernel), or one warp per row when a row has at
+// most 32 slots (merge_partials_slots_kernel) or its slots hold few keys
+// (merge_partials_warp_kernel).
 #include "device_common.cuh"
 #include "lmh_internal.h"
 
@@ -331,6 +332,7 @@ constexpr int kWarpItems = 512;
 constexpr int kWarpPerLane = kWarpItems / 32;
 constexpr int kWarpMaxK = 32;
 constexpr int kWarpRowsPerCtaMax = 8;
+constexpr size_t kSlotsSmemMax = 48 * 1024;  // dynamic shared memory of one slots-kernel CTA
 
 __device__ __forceinline__ uint64_t max_of(const uint64_t (&kv)[kWarpPerLane]) {
   uint64_t m = kv[0];
@@ -392,8 +394,6 @@ struct WarpRankWriter {
   float* lps;
   unsigned long long* keys;  // record mode
   float lse;
-  int32_t my_id = -1;
-  float my_lp = -INFINITY;
   uint64_t my_key = 0;
 
   __device__ __forceinline__ WarpRankWriter(const MergeArgs& a, int row, float lse_) : lse(lse_) {
@@ -403,19 +403,15 @@ struct WarpRankWriter {
     keys = rec ? record_keys(row_record(a, row)) : nullptr;
   }
   __device__ __forceinline__ void put(int r, int k, int lane, uint64_t key) {
-    if (lane == (r & 31)) {  // key 0: fewer than k candidates
-      my_key = key;
-      my_id = key ? key_id(key) : -1;
-      my_lp = key ? key_value(key) - lse : -INFINITY;
-    }
+    if (lane == (r & 31)) my_key = key;  // key 0: fewer than k candidates
     if ((r & 31) == 31 || r == k - 1) {
       const int r0 = r & ~31;
       if (lane <= (r & 31)) {
         if (keys) {
           keys[r0 + lane] = my_key;
         } else {
-          ids[r0 + lane] = my_id;
-          lps[r0 + lane] = my_lp;
+          ids[r0 + lane] = my_key ? key_id(my_key) : -1;
+          lps[r0 + lane] = my_key ? key_value(my_key) - lse : -INFINITY;
         }
       }
     }
@@ -484,6 +480,50 @@ __global__ void __launch_bounds__(kWarpRowsPerCtaMax * 32) merge_partials_warp_k
 }
 
 // ---------------------------------------------------------------------------
+// One warp per row, one slot per lane, for plans with at most 32 slots: the warp
+// copies the row's lists into shared memory (coalesced), and lane l walks slot l's
+// sorted list with a head pointer, holding its current and next entries in
+// registers.  Round r: the warp's largest head (warp_max_key) is rank r; the lane
+// that holds it moves on by one entry and fetches the one after.  A round is a few
+// instructions for the warp, where the tournament above rescans a lane's 16 items.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kWarpRowsPerCtaMax * 32) merge_partials_slots_kernel(const MergeArgs a) {
+  extern __shared__ unsigned long long s_lists[];  // per warp: splits * k_max keys
+  pdl_wait();  // the partials come from the kernel launched just before
+  pdl_launch_dependents();  // a following kernel may be scheduled; it waits for this grid before using its results
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int row = blockIdx.x * (blockDim.x >> 5) + w;
+  if (row >= a.rows) return;
+  int k = a.k_max;
+  if (a.row_k) k = min(max(a.row_k[row], 0), a.k_max);
+  const int n = a.splits * a.k_max;
+  unsigned long long* lists = s_lists + static_cast<int64_t>(w) * n;
+  const unsigned long long* src = a.parts.part_keys + static_cast<int64_t>(row) * n;
+  for (int i = lane; i < n; i += 32) lists[i] = src[i];  // entries past a list's first k are never read
+  const float lse = warp_row_head(a, row, lane);
+  if (a.k_max == 0) return;
+  __syncwarp();
+
+  // only the first k entries of a list can reach the row's top k
+  const unsigned long long* mine = lists + lane * a.k_max;
+  const bool has = lane < a.splits;
+  int p = 0;  // entries of this lane's list already ranked
+  uint64_t head = (has && k > 0) ? mine[0] : 0ull;
+  uint64_t next = (has && k > 1) ? mine[1] : 0ull;
+  WarpRankWriter out(a, row, lse);
+  for (int r = 0; r < k; ++r) {
+    const uint64_t key = warp_max_key(head);
+    if (key != 0ull && head == key) {  // the one holder moves on
+      head = next;
+      ++p;
+      next = (p + 1 < k) ? mine[p + 1] : 0ull;
+    }
+    out.put(r, k, lane, key);
+  }
+  out.pad(k, a.k_max, lane);
+}
+
+// ---------------------------------------------------------------------------
 // vocabulary-parallel records -> the merge's partials (one slot per part)
 // ---------------------------------------------------------------------------
 // Thread t of row r copies part t's (m, s) and keys; the part whose share holds
@@ -531,6 +571,15 @@ cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts,
   a.samp = samp ? *samp : SampleArgs{};
   a.rec = rec ? *rec : RecordOut{nullptr, 0, 0};
   const int sms = num_sms > 0 ? num_sms : 1;
+  if (splits <= 32 && k_max <= kWarpMaxK) {
+    const size_t per_warp = static_cast<size_t>(splits) * k_max * sizeof(unsigned long long);
+    int rpc = 1;
+    while (rpc < kWarpRowsPerCtaMax && static_cast<int64_t>(rows) > static_cast<int64_t>(2 * rpc) * sms &&
+           2 * rpc * per_warp <= kSlotsSmemMax)
+      rpc *= 2;
+    return launch_kernel(merge_partials_slots_kernel, dim3((rows + rpc - 1) / rpc), dim3(rpc * 32), rpc * per_warp,
+                         stream, pdl, a);
+  }
   if (static_cast<int64_t>(splits) * k_max <= kWarpItems && k_max <= kWarpMaxK) {
     // rows spread over the SMs first: one warp per CTA while there are SMs to spare
     int rpc = 1;
