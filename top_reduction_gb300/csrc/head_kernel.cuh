@@ -70,12 +70,14 @@ struct HeadCfg {
   static constexpr size_t kListBytes = kDeep ? static_cast<size_t>(64) * 32 * 4
                                        : kRegList ? static_cast<size_t>(4) * 64 * 32 * 4
                                                   : static_cast<size_t>(kBM) * KCAP * 8;
-  static constexpr size_t kSmem = 1024 /*alignment slack*/ + kStages * (kStageA + kStageBytesB) +
-                                  kListBytes + (2 * kStages + 7) * 8 + 16;
   // Small batches may split each tile's columns over the epilogue warps (see
   // HeadArgs::rep); a warp then hands its row state to the leader through its
   // own staging region: 7 words plus (value, id) per list entry, per lane.
   static constexpr bool kRepOk = kRegList && 7 + 2 * KCAP <= 64;
+  // column split: every copy's current list threshold, one (unit, value) word per lane
+  static constexpr size_t kTauBytes = kRepOk ? 4 * 32 * 8 : 0;
+  static constexpr size_t kSmem = 1024 /*alignment slack*/ + kStages * (kStageA + kStageBytesB) +
+                                  kListBytes + (2 * kStages + 7) * 8 + 16 + kTauBytes;
 };
 
 struct HeadArgs {
@@ -280,6 +282,14 @@ static __device__ __noinline__ void heap_sort_desc(uint64_t* h, int r, int n) {
 // ---------------------------------------------------------------------------
 // per-row top-k list in registers (KCAP <= 32)
 // ---------------------------------------------------------------------------
+// The largest float below x (x itself for -inf and NaN).
+__device__ __forceinline__ float float_below(float x) {
+  if (!(x > -INFINITY)) return x;
+  if (x == 0.0f) return -1.40129846e-45f;  // the negative denormal nearest zero
+  const uint32_t b = __float_as_uint(x);
+  return __uint_as_float(x > 0.0f ? b - 1u : b + 1u);
+}
+
 // V[0..KC) holds the row's best values sorted descending, I[] their ids
 // (-inf / -1 in empty slots).  Entries reach a thread with ascending ids (the
 // tiles of a unit, the blocks of a tile and the columns of a block are
@@ -391,8 +401,10 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
   static_assert(!kDeep || (Cfg::kRegList && kSamp == 0), "the deep layout: register lists, no sampling");
   constexpr int S = Cfg::kStages;
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned (the 128-B swizzle atoms), as an offset from smem_raw so that the
+  // compiler still sees shared-memory pointers (plain LDS/STS, not generic accesses)
+  unsigned char* smem =
+      smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u);
   unsigned char* sA = smem;
   unsigned char* sB = sA + S * Cfg::kStageA;
   uint64_t* lists = reinterpret_cast<uint64_t*>(sB + S * kStageBytesB);
@@ -405,6 +417,9 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
   uint64_t* mma_drain = xchg_empty + 1;   // the MMA thread's work in flight has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // column split: [lane quarter][lane] (unit << 32 | threshold bits) of each row copy
+  volatile uint64_t* tau_sh =
+      reinterpret_cast<volatile uint64_t*>(reinterpret_cast<unsigned char*>(full) + (2 * S + 7) * 8 + 16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int k_blocks = (a.H + kBK - 1) / kBK;
@@ -424,6 +439,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
     *abort_flag = 0;
     mbar_init_fence();
   }
+  if (Cfg::kRepOk && threadIdx.x < 128) tau_sh[threadIdx.x] = ~0ull;  // no unit yet
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols)
@@ -697,21 +713,23 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                   if (j < nvalid) dst[j] = v[j];
               }
             }
-            float bm = v[0];
+            // block max and exp-sum as 8 and 4 independent chains (one warp runs this alone)
+            float tm[8];
 #pragma unroll
-            for (int j = 1; j < kBlock; ++j) bm = fmaxf(bm, v[j]);
+            for (int i = 0; i < 8; ++i) tm[i] = v[i];
+#pragma unroll
+            for (int j = 8; j < kBlock; ++j) tm[j & 7] = fmaxf(tm[j & 7], v[j]);
+            const float bm = fmaxf(fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])),
+                                   fmaxf(fmaxf(tm[4], tm[5]), fmaxf(tm[6], tm[7])));
             if (bm > m) {
               ssum *= ex2_approx((m - bm) * L);
               m = bm;
             }
             const float mL = m * L;
-            float acc0 = 0.f, acc1 = 0.f;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < kBlock; j += 2) {
-              acc0 += ex2_approx(fmaf(v[j], L, -mL));
-              acc1 += ex2_approx(fmaf(v[j + 1], L, -mL));
-            }
-            ssum += acc0 + acc1;
+            for (int j = 0; j < kBlock; ++j) acc[j & 3] += ex2_approx(fmaf(v[j], L, -mL));
+            ssum += (acc[0] + acc[1]) + (acc[2] + acc[3]);
             const int gcol0 = col0 + a.id_off;  // token id of the block's first logit
             const unsigned rel = static_cast<unsigned>(sel_id - gcol0);
             if (rel < static_cast<unsigned>(kBlock)) {
@@ -805,21 +823,33 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
               }
             }
             if constexpr (Cfg::kRegList) {
+              // Candidates: above this copy's own threshold, and not below any other copy's
+              // (another copy's KCAP-th value bounds the row's KCAP-th value from below;
+              // ">=" there keeps a tie that the smaller id may still win).
+              float thr = rt.tau;
+              if (Cfg::kRepOk && n_rep > 1) {
+                float ts = -INFINITY;
+                for (int p = 0; p < n_rep; ++p) {
+                  if (p == copy) continue;
+                  const uint64_t w = tau_sh[((q % a.rep_nq) + p * a.rep_nq) * 32 + lane];
+                  if (static_cast<uint32_t>(w >> 32) == static_cast<uint32_t>(u))
+                    ts = fmaxf(ts, __uint_as_float(static_cast<uint32_t>(w)));
+                }
+                thr = fmaxf(thr, float_below(ts));
+              }
               // Stage the block for the lanes that have candidates; each lane then walks only its
               // own candidate mask, so the warp pays the largest per-lane count, not their union.
-              const bool want = k_row > 0 && bm > rt.tau;
+              const bool want = k_row > 0 && bm > thr;
               if (__any_sync(valid_mask, want)) {
                 float* stg = reinterpret_cast<float*>(lists) + q * (kBlock * 32);
-                uint32_t mlo = 0, mhi = 0;
+                uint32_t mq[4] = {0u, 0u, 0u, 0u};  // candidate bits of the block's four 16-logit quarters
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
+                for (int j = 0; j < kBlock; ++j) {
                   stg[j * 32 + lane] = v[j];
-                  stg[(j + 32) * 32 + lane] = v[j + 32];
-                  mlo |= (v[j] > rt.tau ? 1u : 0u) << j;
-                  mhi |= (v[j + 32] > rt.tau ? 1u : 0u) << j;
+                  mq[j >> 4] |= (v[j] > thr ? 1u : 0u) << (j & 15);
                 }
                 __syncwarp(valid_mask);
-                uint64_t cm = want ? ((static_cast<uint64_t>(mhi) << 32) | mlo) : 0ull;
+                uint64_t cm = want ? ((static_cast<uint64_t>(mq[2] | (mq[3] << 16)) << 32) | (mq[0] | (mq[1] << 16))) : 0ull;
                 while (cm) {
                   const int j = __ffsll(static_cast<long long>(cm)) - 1;
                   cm &= cm - 1;
@@ -827,6 +857,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
                   if (x > rt.tau) rt.insert(x, gcol0 + j);
                 }
                 __syncwarp(valid_mask);
+                if (Cfg::kRepOk && n_rep > 1 && want)
+                  tau_sh[q * 32 + lane] = (static_cast<uint64_t>(static_cast<uint32_t>(u)) << 32) | __float_as_uint(rt.tau);
               }
             } else {
               if (k_row > 0 && bm > st.tau) {
@@ -901,20 +933,32 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
             const bool four = n_rep > 2;
             int h0 = 0, h1 = 0, h2 = 0, h3 = 0;
             uint64_t k0 = xk[w0], k1 = xk[w1], k2 = four ? xk[w2] : 0ull, k3 = four ? xk[w3] : 0ull;
-            for (int j = 0; j < k_row; ++j) {
+            // merged into registers first, written out after; each pop is branch-free (one
+            // load from the popped list), so lanes that pop different lists do not diverge
+            uint64_t res[KC];
+#pragma unroll
+            for (int j = 0; j < KC; ++j) {
               const uint64_t best = max(max(k0, k1), max(k2, k3));
-              f(j, best);
-              if (best == 0ull) continue;
-              if (best == k0) {
-                k0 = (++h0 < KC) ? xk[w0 + h0 * 32] : 0ull;
-              } else if (best == k1) {
-                k1 = (++h1 < KC) ? xk[w1 + h1 * 32] : 0ull;
-              } else if (best == k2) {
-                k2 = (++h2 < KC) ? xk[w2 + h2 * 32] : 0ull;
-              } else {
-                k3 = (++h3 < KC) ? xk[w3 + h3 * 32] : 0ull;
+              res[j] = best;
+              if (j + 1 < KC) {
+                const bool p0 = best == k0, p1 = !p0 && best == k1, p2 = !p0 && !p1 && best == k2;
+                const int hp = (p0 ? h0 : p1 ? h1 : p2 ? h2 : h3) + 1;
+                const int wp = p0 ? w0 : p1 ? w1 : p2 ? w2 : w3;
+                const uint64_t nk = (hp < KC && best != 0ull) ? xk[wp + hp * 32] : 0ull;
+                const bool p3 = !p0 && !p1 && !p2;
+                k0 = p0 ? nk : k0;
+                h0 = p0 ? hp : h0;
+                k1 = p1 ? nk : k1;
+                h1 = p1 ? hp : h1;
+                k2 = p2 ? nk : k2;
+                h2 = p2 ? hp : h2;
+                k3 = p3 ? nk : k3;
+                h3 = p3 ? hp : h3;
               }
             }
+#pragma unroll
+            for (int j = 0; j < KC; ++j)
+              if (j < k_row) f(j, res[j]);
           } else {
 #pragma unroll
             for (int j = 0; j < KC; ++j)
