@@ -725,11 +725,18 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
               ssum *= ex2_approx((m - bm) * L);
               m = bm;
             }
-            const float mL = m * L;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            // exp(x - m) = 2^(x log2e - m log2e): one packed FFMA2 and one packed FADD2 per
+            // pair of logits around the two ex2
+            const float2 L2 = make_float2(L, L), nmL2 = make_float2(-m * L, -m * L);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int j = 0; j < kBlock; ++j) acc[j & 3] += ex2_approx(fmaf(v[j], L, -mL));
-            ssum += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            for (int j = 0; j < kBlock; j += 2) {
+              const float2 y = __ffma2_rn(make_float2(v[j], v[j + 1]), L2, nmL2);
+              acc[(j >> 1) & 3] = __fadd2_rn(acc[(j >> 1) & 3], make_float2(ex2_approx(y.x), ex2_approx(y.y)));
+            }
+            const float2 a2 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+            ssum += a2.x + a2.y;
             const int gcol0 = col0 + a.id_off;  // token id of the block's first logit
             const unsigned rel = static_cast<unsigned>(sel_id - gcol0);
             if (rel < static_cast<unsigned>(kBlock)) {
@@ -841,19 +848,33 @@ __global__ void __launch_bounds__(kHeadThreads, 1)
               // own candidate mask, so the warp pays the largest per-lane count, not their union.
               const bool want = k_row > 0 && bm > thr;
               if (__any_sync(valid_mask, want)) {
+                // staging: logit j of a lane at [j / 4][lane][j % 4] (16-byte stores, conflict-free)
                 float* stg = reinterpret_cast<float*>(lists) + q * (kBlock * 32);
-                uint32_t mq[4] = {0u, 0u, 0u, 0u};  // candidate bits of the block's four 16-logit quarters
 #pragma unroll
-                for (int j = 0; j < kBlock; ++j) {
-                  stg[j * 32 + lane] = v[j];
-                  mq[j >> 4] |= (v[j] > thr ? 1u : 0u) << (j & 15);
+                for (int j = 0; j < kBlock; j += 4)
+                  *reinterpret_cast<float4*>(stg + (j >> 2) * 128 + lane * 4) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                // candidate bits: the sign of thr - x is set exactly when x > thr (NaN and
+                // -inf - -inf give a clear sign); funnel shifts collect one bit per logit,
+                // the last logit first, so logit j lands on bit j
+                const float2 t2 = make_float2(thr, thr), m1 = make_float2(-1.0f, -1.0f);
+                uint32_t mlo = 0u, mhi = 0u;
+#pragma unroll
+                for (int j = kBlock - 2; j >= 0; j -= 2) {
+                  const float2 d = __ffma2_rn(make_float2(v[j], v[j + 1]), m1, t2);
+                  if (j >= 32) {
+                    mhi = __funnelshift_l(__float_as_uint(d.y), mhi, 1);
+                    mhi = __funnelshift_l(__float_as_uint(d.x), mhi, 1);
+                  } else {
+                    mlo = __funnelshift_l(__float_as_uint(d.y), mlo, 1);
+                    mlo = __funnelshift_l(__float_as_uint(d.x), mlo, 1);
+                  }
                 }
                 __syncwarp(valid_mask);
-                uint64_t cm = want ? ((static_cast<uint64_t>(mq[2] | (mq[3] << 16)) << 32) | (mq[0] | (mq[1] << 16))) : 0ull;
+                uint64_t cm = want ? ((static_cast<uint64_t>(mhi) << 32) | mlo) : 0ull;
                 while (cm) {
                   const int j = __ffsll(static_cast<long long>(cm)) - 1;
                   cm &= cm - 1;
-                  const float x = stg[j * 32 + lane];
+                  const float x = stg[(j >> 2) * 128 + lane * 4 + (j & 3)];
                   if (x > rt.tau) rt.insert(x, gcol0 + j);
                 }
                 __syncwarp(valid_mask);
