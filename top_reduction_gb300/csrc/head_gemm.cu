@@ -60,7 +60,6 @@ cudaError_t launch_gather_rows(const void* hidden, int64_t hidden_stride, int nu
 constexpr int kRepMaxH = 2048;  // hidden sizes from which lists of 16-20 need no column split
 
 HeadPlan head_plan(int rows, int H, int V, int k_max, int num_sms) {
-  (void)H;
   HeadPlan p;
   p.m_tiles = (rows + kBM - 1) / kBM;
   p.n_tiles = (V + kBN - 1) / kBN;
@@ -72,15 +71,19 @@ HeadPlan head_plan(int rows, int H, int V, int k_max, int num_sms) {
            : k_max <= 32 ? 32
                          : 128;
   const int G = num_sms > 0 ? num_sms : 1;
-  // choose the vocabulary split that minimises the busiest CTA's tile count
-  // (plus a small cost per unit for its flush and pipeline refill)
+  // Choose the vocabulary split that minimises the busiest CTA's tile count plus a cost
+  // per unit.  A unit starts with empty candidate lists, so its first tile's reduction
+  // takes about 23 us for 128 rows at K 20 (every logit of the first block enters the
+  // list), against 4.5 us for later tiles.  With H below 2048 the MMA of two tiles
+  // (5.4 us each at H 1024) cannot cover it and the unit start costs about two tiles;
+  // with longer tiles only the flush and refill remain (a quarter of a tile).
   double best = 1e300;
   int best_s = 1;
   for (int s = 1; s <= p.n_tiles; ++s) {
     const int tps = (p.n_tiles + s - 1) / s;
     const int units = p.m_tiles * ((p.n_tiles + tps - 1) / tps);
     const int waves = (units + G - 1) / G;
-    const double cost = static_cast<double>(waves) * (tps + 0.25);
+    const double cost = static_cast<double>(waves) * (tps + (H < 2048 ? 2.0 : 0.25));
     if (cost < best - 1e-9) {
       best = cost;
       best_s = s;
