@@ -130,7 +130,10 @@ def test_mixed_step_sampled(lmh):
 
 @pytest.mark.parametrize("rows,H,V,k", [(200, 136, 4100, 20), (129, 64, 1000, 128), (3, 520, 70000, 0),
                                         (1, 8, 300, 7), (300, 1024, 20000, 33), (64, 256, 9000, 12),
-                                        (130, 512, 12000, 30), (17, 64, 2000, 3), (16, 64, 40000, 128)])
+                                        (130, 512, 12000, 30), (17, 64, 2000, 3), (16, 64, 40000, 128),
+                                        # vocabulary ranges per row on 152 SMs: 128 (the warp-per-row
+                                        # merge at 4 lists per lane), 129 (one CTA per row), 98 at K 32
+                                        (40, 256, 32768, 20), (24, 128, 33000, 20), (50, 192, 25000, 32)])
 def test_ragged_shapes(lmh, rows, H, V, k):
     g = torch.Generator().manual_seed(rows * 7 + H)
     T = rows + 5

@@ -7,7 +7,7 @@
 // by ascending id.
 //
 // One CTA per row (merge_partials_kernel), or one warp per row when a row has at
-// most 32 slots (merge_partials_slots_kernel) or its slots hold few keys
+// most 128 slots (merge_partials_slots_kernel) or its slots hold few keys
 // (merge_partials_warp_kernel).
 #include "device_common.cuh"
 #include "lmh_internal.h"
@@ -118,7 +118,6 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_partials_kernel(const 
   __shared__ uint32_t hist[256];
   __shared__ uint32_t misc[4];  // [0] candidates, [1..2] select broadcast
   __shared__ float red[32];
-  __shared__ uint64_t red64[32];
   __shared__ uint32_t lbw[kMergeThreads / 32];  // per-warp bounds (read once, after one barrier)
   pdl_wait();  // the partials come from the kernel launched just before
   pdl_launch_dependents();  // a following kernel may be scheduled; it waits for this grid before using its results
@@ -480,13 +479,15 @@ __global__ void __launch_bounds__(kWarpRowsPerCtaMax * 32) merge_partials_warp_k
 }
 
 // ---------------------------------------------------------------------------
-// One warp per row, one slot per lane, for plans with at most 32 slots: the warp
-// copies the row's lists into shared memory (coalesced), and lane l walks slot l's
-// sorted list with a head pointer, holding its current and next entries in
-// registers.  Round r: the warp's largest head (warp_max_key) is rank r; the lane
-// that holds it moves on by one entry and fetches the one after.  A round is a few
-// instructions for the warp, where the tournament above rescans a lane's 16 items.
+// One warp per row for plans with at most 32 * SPL slots: the warp copies the row's
+// lists into shared memory (coalesced), and lane l walks the sorted lists of slots
+// l, l + 32, ... (SPL of them) with head pointers, holding each list's current and
+// next entries in registers.  Round r: the warp's largest head (warp_max_key over each
+// lane's best head) is rank r; the lane that holds it moves that list on by one entry
+// and fetches the one after.  A round is a few instructions for the warp, where the
+// tournament above rescans a lane's 16 items.
 // ---------------------------------------------------------------------------
+template <int SPL>
 __global__ void __launch_bounds__(kWarpRowsPerCtaMax * 32) merge_partials_slots_kernel(const MergeArgs a) {
   extern __shared__ unsigned long long s_lists[];  // per warp: splits * k_max keys
   pdl_wait();  // the partials come from the kernel launched just before
@@ -505,18 +506,31 @@ __global__ void __launch_bounds__(kWarpRowsPerCtaMax * 32) merge_partials_slots_
   __syncwarp();
 
   // only the first k entries of a list can reach the row's top k
-  const unsigned long long* mine = lists + lane * a.k_max;
-  const bool has = lane < a.splits;
-  int p = 0;  // entries of this lane's list already ranked
-  uint64_t head = (has && k > 0) ? mine[0] : 0ull;
-  uint64_t next = (has && k > 1) ? mine[1] : 0ull;
+  int p[SPL];  // entries of each of this lane's lists already ranked
+  uint64_t head[SPL], next[SPL];
+#pragma unroll
+  for (int i = 0; i < SPL; ++i) {
+    const bool has = lane + 32 * i < a.splits;
+    const unsigned long long* l = lists + (lane + 32 * i) * a.k_max;
+    p[i] = 0;
+    head[i] = (has && k > 0) ? l[0] : 0ull;
+    next[i] = (has && k > 1) ? l[1] : 0ull;
+  }
   WarpRankWriter out(a, row, lse);
   for (int r = 0; r < k; ++r) {
-    const uint64_t key = warp_max_key(head);
-    if (key != 0ull && head == key) {  // the one holder moves on
-      head = next;
-      ++p;
-      next = (p + 1 < k) ? mine[p + 1] : 0ull;
+    uint64_t best = head[0];
+#pragma unroll
+    for (int i = 1; i < SPL; ++i) best = max(best, head[i]);
+    const uint64_t key = warp_max_key(best);
+    if (key != 0ull && best == key) {  // the one holder moves that list on
+#pragma unroll
+      for (int i = 0; i < SPL; ++i) {
+        if (head[i] == key) {
+          head[i] = next[i];
+          ++p[i];
+          next[i] = (p[i] + 1 < k) ? lists[(lane + 32 * i) * a.k_max + p[i] + 1] : 0ull;
+        }
+      }
     }
     out.put(r, k, lane, key);
   }
@@ -571,14 +585,18 @@ cudaError_t launch_merge(int rows, int splits, int V, int k_max, Partials parts,
   a.samp = samp ? *samp : SampleArgs{};
   a.rec = rec ? *rec : RecordOut{nullptr, 0, 0};
   const int sms = num_sms > 0 ? num_sms : 1;
-  if (splits <= 32 && k_max <= kWarpMaxK) {
+  if (splits <= 4 * 32 && k_max <= kWarpMaxK) {
+    // rows spread over the SMs first, up to 8 per CTA, within 48 KB of lists per CTA
     const size_t per_warp = static_cast<size_t>(splits) * k_max * sizeof(unsigned long long);
     int rpc = 1;
     while (rpc < kWarpRowsPerCtaMax && static_cast<int64_t>(rows) > static_cast<int64_t>(2 * rpc) * sms &&
-           2 * rpc * per_warp <= kSlotsSmemMax)
-      rpc *= 2;
-    return launch_kernel(merge_partials_slots_kernel, dim3((rows + rpc - 1) / rpc), dim3(rpc * 32), rpc * per_warp,
-                         stream, pdl, a);
+           (rpc + 1) * per_warp <= kSlotsSmemMax)
+      ++rpc;
+    const dim3 grid((rows + rpc - 1) / rpc), block(rpc * 32);
+    const size_t smem = rpc * per_warp;
+    if (splits <= 32) return launch_kernel(merge_partials_slots_kernel<1>, grid, block, smem, stream, pdl, a);
+    if (splits <= 64) return launch_kernel(merge_partials_slots_kernel<2>, grid, block, smem, stream, pdl, a);
+    return launch_kernel(merge_partials_slots_kernel<4>, grid, block, smem, stream, pdl, a);
   }
   if (static_cast<int64_t>(splits) * k_max <= kWarpItems && k_max <= kWarpMaxK) {
     // rows spread over the SMs first: one warp per CTA while there are SMs to spare
