@@ -28,6 +28,14 @@
  *   keeps no per-call state; scratch memory is the caller's `workspace`.
  * - Every call is enqueued on `stream` and returns without waiting for the
  *   GPU: no host synchronisation and no device->host copy happens inside.
+ * - Kernels are launched with programmatic dependent launch, so a call's
+ *   first kernel may start while the kernel enqueued before it finishes.
+ *   Before it waits for that kernel it reads only the head weights W (projection
+ *   entry points) or the logits and selected ids of its first chunks (logits
+ *   entry points).  Those inputs must therefore not be written by a kernel
+ *   enqueued right before the call that itself triggers programmatic dependent
+ *   launch before writing them (ordinary kernels, and this library's own, do
+ *   not).
  * - Host-side argument checks return an error status and launch nothing.
  *   Errors only visible on the device (bad cu_seqlens, an id out of range)
  *   set bits (LMH_DS_*) in the caller's optional `dev_status` word with an

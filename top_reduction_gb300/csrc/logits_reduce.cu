@@ -707,34 +707,15 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
     const int64_t total = static_cast<int64_t>(a.rows) * a.cpr;
     const int64_t first_dynamic = static_cast<int64_t>(S) * gridDim.x;
     const uint64_t policy = l2_evict_first_policy();  // logits are read once; the block maxima stay in L2
-    // The kernel may start while its predecessor (the previous call's select kernel,
-    // which still reads the workspace and records the ticket's base) runs: wait for
-    // it before reading the base, the first ticket, load or workspace write (the
-    // consumers write only data that arrived after this point).
-    pdl_wait();
-    // Read through L2 (another kernel wrote them; an L1 line of an earlier call could be stale).
-    TicketState* tk = a.parts.ticket;
-    const unsigned long long base = __ldcg(&tk->base);
-    const bool dynamic = __ldcg(&tk->check) == ~base;  // the same in every CTA: nothing writes these now
-    uint32_t issued = 0;
-    int64_t next = blockIdx.x;
     int sel_row = -1, sel_id = -1;
-    for (;; ++issued) {
-      const int s = static_cast<int>(issued % S);
-      if (issued >= static_cast<uint32_t>(S) &&
-          !wait_or_abort(&empty[s], ((issued / S) & 1u) ^ 1u, abort_flag, a.dev_status, a.wait_ns))
-        break;
-      const int64_t c = next;
+    // Stage s <- chunk c (false: c is past the end, and stage s gets the end marker).
+    auto issue = [&](int s, int64_t c) {
       StreamDesc& d = desc[s];
       if (c >= total) {
         d.row = -1;
         mbar_arrive(&full[s]);  // end marker: completes with no bytes
-        ++issued;
-        break;
+        return false;
       }
-      next = (issued + 1 < static_cast<uint32_t>(S) || !dynamic)
-                 ? blockIdx.x + static_cast<int64_t>(issued + 1) * gridDim.x
-                 : first_dynamic + static_cast<int64_t>(atomicAdd(&tk->ticket, 1ull) - base);
       const int row = static_cast<int>(c / a.cpr);
       const int ci = static_cast<int>(c - static_cast<int64_t>(row) * a.cpr);
       const int lb = ci * CH;
@@ -754,6 +735,33 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
       mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(ne * ES));
       bulk_load_hint(stages + static_cast<size_t>(s) * kTChunkBytes, src, static_cast<uint32_t>(ne * ES), &full[s],
                      policy);
+      return true;
+    };
+    // A CTA's first S chunks are fixed: they go out before the grid-dependency wait, so
+    // they stream while the kernel before this one (the previous call's select kernel)
+    // still runs.  They read only the call's inputs, which were complete before that
+    // kernel left its own wait; the workspace (the ticket, the partials) is touched
+    // only after this kernel's wait, and the consumers wait too before writing it.
+    uint32_t issued = 0;
+    bool ended = false;
+    for (; issued < static_cast<uint32_t>(S) && !ended; ++issued)
+      ended = !issue(static_cast<int>(issued), blockIdx.x + static_cast<int64_t>(issued) * gridDim.x);
+    pdl_wait();
+    // Read through L2 (another kernel wrote them; an L1 line of an earlier call could be stale).
+    TicketState* tk = a.parts.ticket;
+    const unsigned long long base = __ldcg(&tk->base);
+    const bool dynamic = __ldcg(&tk->check) == ~base;  // the same in every CTA: nothing writes these now
+    auto draw = [&](uint32_t n) -> int64_t {  // the chunk of this CTA's n-th load (n >= S)
+      return !dynamic ? blockIdx.x + static_cast<int64_t>(n) * gridDim.x
+                      : first_dynamic + static_cast<int64_t>(atomicAdd(&tk->ticket, 1ull) - base);
+    };
+    int64_t next = ended ? total : draw(issued);  // drawn one chunk ahead
+    for (; !ended; ++issued) {
+      const int s = static_cast<int>(issued % S);
+      if (!wait_or_abort(&empty[s], ((issued / S) & 1u) ^ 1u, abort_flag, a.dev_status, a.wait_ns)) break;
+      const int64_t c = next;
+      if (c < total) next = draw(issued + 1);
+      ended = !issue(s, c);
     }
     // Copies still in flight (only after an abort) land before the CTA exits;
     // these waits keep the full limit whatever a.wait_ns is.
@@ -770,6 +778,7 @@ __global__ void __launch_bounds__(kTThreads, kTCtasPerSm) logits_stream_tma_kern
   const uint64_t keep_policy = l2_evict_last_policy();
   const int bi = c / TPB;
   const float L = kLog2e;
+  pdl_wait();  // the stages may fill before the kernel before this one ends; the workspace may not be written
   for (uint32_t i = 0;; ++i) {
     const int s = static_cast<int>(i % S);
     const bool ok = wait_or_abort(&full[s], (i / S) & 1u, abort_flag, a.dev_status, a.wait_ns);
