@@ -209,6 +209,26 @@ def test_full_vocabulary_ragged(lmh, dtype, V):
     assert np.max(np.abs(o["topk_logprobs"].cpu().numpy() - _oracle_full(x, orc["lse"]))) <= 1e-5
 
 
+def test_back_to_back_calls_overlap(lmh):
+    """Calls enqueued back to back on one stream and one workspace, with no synchronisation
+    between them: each stream kernel may start (and load its first chunks) while the previous
+    call's select kernel still reads the workspace.  Every call still matches the oracle."""
+    from top_reduction_gb300 import lmh as L
+    V = 60000
+    rows = (96, 64, 96, 80, 96)
+    need = max(L.workspace_bytes(r, 0, V, 20, L.PATH_FROM_LOGITS) for r in rows)
+    ws = torch.empty((need,), dtype=torch.uint8, device="cuda")
+    chunks = [workloads.logits_chunk("normal", seed=60 + i, rows=r, V=V) for i, r in enumerate(rows)]
+    dev = [(c["logits"].cuda(), c["sel"].cuda()) for c in chunks]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    outs = [lmh.logprobs_from_logits(x, sel=s, k_max=20, workspace=ws, dev_status=st) for x, s in dev]
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for i, (c, o) in enumerate(zip(chunks, outs)):
+        check_from_logits(o, oracle_ref(c["logits"], c["sel"], 20), 20, what="call %d" % i)
+
+
 def test_reused_workspace_schedules(lmh):
     """One workspace over several calls: its first call finds no valid chunk-counter base and
     hands out the chunks in a fixed order; the later calls draw them from the counter. Every
