@@ -500,8 +500,16 @@ __global__ void __launch_bounds__(kWarpRowsPerCtaMax * 32) merge_partials_slots_
   const int n = a.splits * a.k_max;
   unsigned long long* lists = s_lists + static_cast<int64_t>(w) * n;
   const unsigned long long* src = a.parts.part_keys + static_cast<int64_t>(row) * n;
-  for (int i = lane; i < n; i += 32) lists[i] = src[i];  // entries past a list's first k are never read
+  // asynchronous copies (cp.async, 8 bytes each): all of a lane's copies are in flight at
+  // once, and the warp waits for them after the row head's loads have gone out too;
+  // entries past a list's first k are never read
+  for (int i = lane; i < n; i += 32)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(lists + i)),
+                 "l"(__cvta_generic_to_global(src + i))
+                 : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
   const float lse = warp_row_head(a, row, lane);
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
   if (a.k_max == 0) return;
   __syncwarp();
 
