@@ -489,7 +489,8 @@ __global__ void __launch_bounds__(kWarpRowsPerCtaMax * 32) merge_partials_warp_k
 // ---------------------------------------------------------------------------
 template <int SPL>
 __global__ void __launch_bounds__(kWarpRowsPerCtaMax * 32) merge_partials_slots_kernel(const MergeArgs a) {
-  extern __shared__ unsigned long long s_lists[];  // per warp: splits * k_max keys
+  extern __shared__ __align__(16) unsigned long long s_lists[];  // per warp: splits * k_max keys
+  __shared__ __align__(8) uint64_t s_bar[kWarpRowsPerCtaMax];     // per warp: its bulk copy
   pdl_wait();  // the partials come from the kernel launched just before
   pdl_launch_dependents();  // a following kernel may be scheduled; it waits for this grid before using its results
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -500,16 +501,37 @@ __global__ void __launch_bounds__(kWarpRowsPerCtaMax * 32) merge_partials_slots_
   const int n = a.splits * a.k_max;
   unsigned long long* lists = s_lists + static_cast<int64_t>(w) * n;
   const unsigned long long* src = a.parts.part_keys + static_cast<int64_t>(row) * n;
-  // asynchronous copies (cp.async, 8 bytes each): all of a lane's copies are in flight at
-  // once, and the warp waits for them after the row head's loads have gone out too;
-  // entries past a list's first k are never read
-  for (int i = lane; i < n; i += 32)
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(lists + i)),
-                 "l"(__cvta_generic_to_global(src + i))
-                 : "memory");
-  asm volatile("cp.async.commit_group;" ::: "memory");
+  // The row's lists are one contiguous block: one bulk copy when it is large (at least 512
+  // keys, an even number from a 16-byte aligned address), else asynchronous 8-byte copies
+  // (cp.async), all of a lane's in flight at once (cheaper to start for a small block).
+  // Either way the warp waits after the row head's loads have gone out too; entries past
+  // a list's first k are never read.
+  const bool bulk = n >= 512 && (n & 1) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+  uint64_t* bar = &s_bar[w];
+  if (bulk) {
+    if (lane == 0) {
+      mbar_init(bar, 1);
+      mbar_init_fence();
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * 8u);
+      bulk_load(lists, src, static_cast<uint32_t>(n) * 8u, bar);
+    }
+    __syncwarp();
+  } else {
+    for (int i = lane; i < n; i += 32)
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(lists + i)),
+                   "l"(__cvta_generic_to_global(src + i))
+                   : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
   const float lse = warp_row_head(a, row, lane);
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  if (bulk) {
+    if (!mbar_wait(bar, 0)) {  // (bounded) the copy lands before the warp goes on
+      set_status(a.dev_status, LMH_DS_TIMEOUT);
+      mbar_wait(bar, 0);
+    }
+  } else {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+  }
   if (a.k_max == 0) return;
   __syncwarp();
 
