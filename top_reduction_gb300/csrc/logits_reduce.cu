@@ -20,7 +20,9 @@
 //         mbarriers); four consumer warps read them, each thread owning 128
 //         contiguous bytes (one bf16/f16 block, half an f32 block), so a
 //         block's maximum needs no exchange between lanes; one (m, s) pair
-//         per warp and chunk.
+//         per warp and chunk.  A CTA's first three chunks are fixed and go
+//         out before the grid-dependency wait, so in a sequence of calls they
+//         stream while the previous call's select kernel runs.
 //       - logits_stream_regs_kernel (any element-aligned layout; two CTAs
 //         per SM): the flattened (row, 64-block) space is cut into equal
 //         contiguous ranges, one per CTA; every thread loads 16-byte vectors
